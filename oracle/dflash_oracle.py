@@ -1,0 +1,294 @@
+"""Float64 CPU oracle for the DFlash per-cycle hot path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports, calls or links
+this module: only the test-suite, the smoke check and the bench's CPU-baseline
+leg use it.  It shares no code with the CUDA library.
+
+Everything is the plain definition written out in NumPy float64.  bf16 inputs
+(uint16 bit patterns) are read as exact float64 values.  Where the pages leave
+a step open, the reading taken is stated next to the function.
+
+Sources (web pages on DFlash; cited by page and section):
+  [P1] "DFlash双实现对比：PyTorch与MLX代码架构差异深度分析" (hotelren.com)
+       §1 model definition (Qwen3 RMSNorm / rotary embedding reused),
+       §2 attention (dual-source K/V: ctx ⊕ block, Q from the block only,
+          non-causal inside the block), §3 KV-cache crop, §4 target-layer
+          hidden states concatenated by target_layer_ids.
+  [P2] "dflash-mlx" lossless speculative decoding (dpshk.com)
+       块扩散草稿 (block = staged token + 15 masks; drafter reads target hidden),
+       单次前向验证 (the nine-step cycle ①–⑨),
+       保证二 (acceptance = sum(cumprod(draft == posterior)); prefix semantics;
+          the first rejected position takes the target's own token),
+       保证三 (caches cut back to the committed length).
+
+Parity pins: see tests/test_oracle_*.py.  Every function below is pinned there
+by something other than itself (brute force, closed forms, invariants,
+worked cases from [P2]).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+BLOCK = 16
+
+
+# ---------------------------------------------------------------------------
+# elementary pieces
+# ---------------------------------------------------------------------------
+def bf16_to_f64(bits) -> np.ndarray:
+    """Exact float64 value of bf16 bit patterns (uint16)."""
+    b = np.asarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def as_f64(x) -> np.ndarray:
+    """uint16 arrays are bf16 bit patterns; everything else is converted to float64."""
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return bf16_to_f64(x)
+    return x.astype(np.float64)
+
+
+def rms_norm(x: np.ndarray, weight, eps: float) -> np.ndarray:
+    """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * weight.
+
+    The Qwen3 RMSNorm the drafter reuses ([P1] §1).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    y = x / np.sqrt(ms + eps)
+    if weight is not None:
+        y = y * as_f64(weight)
+    return y
+
+
+def rope_inv_freq(head_dim: int, theta: float) -> np.ndarray:
+    """inv_freq[d] = theta^(-2d/D) for d < D/2 (Qwen3 rotary embedding, [P1] §1)."""
+    d = np.arange(head_dim // 2, dtype=np.float64)
+    return theta ** (-2.0 * d / head_dim)
+
+
+def apply_rope(x: np.ndarray, positions: np.ndarray, theta: float) -> np.ndarray:
+    """Rotate-half RoPE: for d < D/2 with angle = pos * inv_freq[d]
+         x'[d]       = x[d] cos - x[d + D/2] sin
+         x'[d + D/2] = x[d + D/2] cos + x[d] sin
+    ``positions`` has the shape of ``x`` without its last axis.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    D = x.shape[-1]
+    half = D // 2
+    pos = np.asarray(positions, dtype=np.float64)
+    assert pos.shape == x.shape[:-1], (pos.shape, x.shape)
+    ang = pos[..., None] * rope_inv_freq(D, theta)
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+# ---------------------------------------------------------------------------
+# a1: context projection
+# ---------------------------------------------------------------------------
+def ctx_project(layer_hidden, w_fc, hidden_norm_w, w_k, w_v, k_norm_w, positions,
+                n_kv_heads: int, head_dim: int, rope_theta: float, rms_eps: float) -> dict:
+    """Context K/V for the drafter from the target's selected-layer hidden states.
+
+    [P1] §4: the hidden states of the layers listed in target_layer_ids are
+    concatenated; [P1] §2 / [P2] 块扩散草稿: the drafter's context K/V are
+    projected from them.  Steps:
+        X  = [h_l1 | h_l2 | ... | h_lnL]              (concat on the feature axis)
+        Y  = X W_fc^T
+        Y^ = RMSNorm(Y) * g_h            (if hidden_norm_w is given)
+        K  = RoPE_pos(RMSNorm_head(Y^ W_k^T) * g_k)   (per-head norm if k_norm_w given)
+        V  = Y^ W_v^T
+    layer_hidden: nL arrays [N, H]; positions: [N] absolute token positions.
+    Returns y, yhat [N, H]; k, v [N, Hkv, D].
+    """
+    xs = [as_f64(h) for h in layer_hidden]
+    x = np.concatenate(xs, axis=-1)
+    y = x @ as_f64(w_fc).T
+    yhat = rms_norm(y, hidden_norm_w, rms_eps) if hidden_norm_w is not None else y
+    N = y.shape[0]
+    k = (yhat @ as_f64(w_k).T).reshape(N, n_kv_heads, head_dim)
+    if k_norm_w is not None:
+        k = rms_norm(k, k_norm_w, rms_eps)
+    pos = np.broadcast_to(np.asarray(positions, dtype=np.float64)[:, None], (N, n_kv_heads))
+    k = apply_rope(k, pos, rope_theta)
+    v = (yhat @ as_f64(w_v).T).reshape(N, n_kv_heads, head_dim)
+    return {"y": y, "yhat": yhat, "k": k, "v": v}
+
+
+# ---------------------------------------------------------------------------
+# a2: dual-source block attention
+# ---------------------------------------------------------------------------
+def block_attention(q_blk, k_blk, v_blk, ctx_k, ctx_v, seq_len, rope_theta: float,
+                    scale: float) -> np.ndarray:
+    """Drafter attention over ctx K/V concatenated with the block's own K/V.
+
+    [P1] §2: Q comes only from the block tokens; K/V = concat(context K/V,
+    block K/V); no causal mask inside the block.  GQA: query head h reads KV
+    head floor(h / G) with G = Hq / Hkv.  Block token j sits at position
+    L_b + j ([P2] 单次前向验证 ③: the staged token follows the context); ctx K
+    is stored already rotated, block Q/K are rotated here.
+
+    q_blk [B,T,Hq,D], k_blk/v_blk [B,T,Hkv,D] (pre-RoPE); ctx_k/ctx_v: per
+    sequence arrays with at least L_b rows [.., Hkv, D]; seq_len [B] = L_b.
+    Returns O [B,T,Hq,D] float64.
+    """
+    q_blk, k_blk, v_blk = as_f64(q_blk), as_f64(k_blk), as_f64(v_blk)
+    B, T, Hq, D = q_blk.shape
+    Hkv = k_blk.shape[2]
+    G = Hq // Hkv
+    out = np.zeros((B, T, Hq, D), dtype=np.float64)
+    for b in range(B):
+        L = int(seq_len[b])
+        pos = L + np.arange(T, dtype=np.float64)
+        q = apply_rope(q_blk[b], np.broadcast_to(pos[:, None], (T, Hq)), rope_theta)
+        kb = apply_rope(k_blk[b], np.broadcast_to(pos[:, None], (T, Hkv)), rope_theta)
+        keys = np.concatenate([as_f64(ctx_k[b][:L]).reshape(L, Hkv, D), kb], axis=0)
+        vals = np.concatenate([as_f64(ctx_v[b][:L]).reshape(L, Hkv, D), v_blk[b]], axis=0)
+        for h in range(Hq):
+            g = h // G
+            s = (q[:, h, :] @ keys[:, g, :].T) * scale        # [T, L+T], no mask
+            s = s - s.max(axis=1, keepdims=True)
+            p = np.exp(s)
+            p = p / p.sum(axis=1, keepdims=True)
+            out[b, :, h, :] = p @ vals[:, g, :]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# a3: verification epilogue
+# ---------------------------------------------------------------------------
+def lm_head_argmax(hidden, w_lm, chunk: int = 8192) -> dict:
+    """Greedy argmax of logits = hidden W_lm^T, never materialising all logits.
+
+    [P2] 保证一: every verify position's logits give their greedy argmax (the
+    posterior).  Exact ties go to the lowest vocabulary index (the pages are
+    silent; this reading is the one the kernels implement).
+    Also returns, per row, the top-2 gap (max - second max, 0 on exact ties)
+    and the max logit, which decide whether a position is a near tie.
+    hidden [N, H]; w_lm [V, H].  Vocabulary rows are processed in chunks.
+    """
+    h = as_f64(hidden)
+    N = h.shape[0]
+    V = np.asarray(w_lm).shape[0]
+    best = np.full(N, -np.inf)
+    second = np.full(N, -np.inf)
+    idx = np.zeros(N, dtype=np.int64)
+    rows = np.arange(N)
+    for v0 in range(0, V, chunk):
+        w = as_f64(w_lm[v0:v0 + chunk])
+        logits = h @ w.T                                   # [N, c]
+        c_idx = np.argmax(logits, axis=1)                  # first maximum in the chunk
+        c1 = logits[rows, c_idx]
+        logits[rows, c_idx] = -np.inf
+        c2 = logits.max(axis=1) if logits.shape[1] > 1 else np.full(N, -np.inf)
+        new_second = np.maximum(np.maximum(np.minimum(best, c1), second), c2)
+        take = c1 > best                                   # strictly greater: earlier chunk wins ties
+        idx = np.where(take, v0 + c_idx, idx)
+        best = np.maximum(best, c1)
+        second = new_second
+    return {"posterior": idx.astype(np.int32), "max": best, "gap": best - second}
+
+
+def acceptance_length(drafted, posterior) -> int:
+    """[P2] 保证二: matches = (drafted == posterior); a = sum(cumprod(matches)).
+
+    drafted = block[1:16] (the 15 drafts); posterior = post[0:15], where
+    post[i] is the target's greedy token after block position i.
+    """
+    m = (np.asarray(drafted) == np.asarray(posterior)).astype(np.int64)
+    return int(np.sum(np.cumprod(m)))
+
+
+def verify_accept(hidden, w_lm, block_ids, len_before, out_tokens=None, out_cap=None,
+                  chunk: int = 8192) -> dict:
+    """Verification epilogue of one cycle ([P2] 单次前向验证 ⑤–⑧).
+
+    hidden [B,T,H] final-normed target hidden states of [staged + 15 drafts];
+    block_ids [B,T]; len_before [B] committed-token count before the cycle.
+      posterior[b, i] = argmax_v logits[b, i, v]        (⑤, 保证一)
+      a_b = sum(cumprod(block[b, 1:] == posterior[b, :15]))   (⑥, 保证二)
+      commit block[b, 0..a_b] at out_tokens[b, len_before[b] + i]   (⑦)
+      next_staged[b] = posterior[b, a_b]                (⑧; a_b = 15 is the bonus token)
+      commit_len[b] = len_before[b] + 1 + a_b
+    A sequence whose commit would pass ``out_cap`` is left uncommitted
+    (flag ``overflow``), matching the library's error behaviour.
+    """
+    block_ids = np.asarray(block_ids)
+    B, T = block_ids.shape
+    H = np.asarray(hidden).shape[-1]
+    am = lm_head_argmax(np.asarray(hidden).reshape(B * T, H), w_lm, chunk)
+    post = am["posterior"].reshape(B, T)
+    if out_tokens is None:
+        cap = int(out_cap) if out_cap is not None else int(np.max(len_before)) + T
+        out_tokens = np.zeros((B, cap), dtype=np.int32)
+    out_tokens = np.array(out_tokens, dtype=np.int32, copy=True)
+    cap = out_tokens.shape[1]
+    accept = np.zeros(B, dtype=np.int32)
+    next_staged = np.zeros(B, dtype=np.int32)
+    commit_len = np.zeros(B, dtype=np.int32)
+    overflow = np.zeros(B, dtype=bool)
+    for b in range(B):
+        a = acceptance_length(block_ids[b, 1:T], post[b, 0:T - 1])
+        accept[b] = a
+        start = int(len_before[b])
+        if start + 1 + a > cap:
+            overflow[b] = True
+            commit_len[b] = start
+            continue
+        out_tokens[b, start:start + a + 1] = block_ids[b, 0:a + 1]
+        next_staged[b] = post[b, a]
+        commit_len[b] = start + 1 + a
+    return {"posterior": post, "gap": am["gap"].reshape(B, T), "max": am["max"].reshape(B, T),
+            "accept": accept, "next_staged": next_staged, "commit_len": commit_len,
+            "out_tokens": out_tokens, "overflow": overflow}
+
+
+def near_tie_mask(gap: np.ndarray, maxv: np.ndarray, rel: float = 1e-3) -> np.ndarray:
+    """Positions whose top-2 gap is at most rel * |max logit| (excluded from the
+    bit-exact comparison of token ids, and counted)."""
+    return gap <= rel * np.abs(maxv)
+
+
+# ---------------------------------------------------------------------------
+# a4: KV-cache crop (and page reservation for the next block's rows)
+# ---------------------------------------------------------------------------
+def kv_crop_lengths(seq_len, new_len) -> tuple:
+    """[P1] §3 / [P2] 保证三: after acceptance the cache keeps only the committed
+    prefix: seq_len[b] <- new_len[b].  A request to grow (new_len > seq_len) or a
+    negative length is invalid: that sequence is left unchanged and flagged."""
+    seq_len = np.array(seq_len, dtype=np.int64, copy=True)
+    new_len = np.asarray(new_len, dtype=np.int64)
+    bad = (new_len > seq_len) | (new_len < 0)
+    seq_len = np.where(bad, seq_len, new_len)
+    return seq_len.astype(np.int32), bad
+
+
+def kv_crop_paged(seq_len, page_table, free_pages: set, new_len, page_size: int) -> dict:
+    """Paged crop: lengths as in :func:`kv_crop_lengths`; every mapped page whose
+    first token index is >= new_len goes back to the free set and its table slot
+    becomes -1.  The partially filled last page is kept.  (Reading: the pages do
+    not describe paging; releasing whole pages beyond the length is the plain one.)"""
+    table = np.array(page_table, dtype=np.int32, copy=True)
+    free = set(free_pages)
+    out_len, bad = kv_crop_lengths(seq_len, new_len)
+    for b in range(table.shape[0]):
+        if bad[b]:
+            continue
+        first_released = -(-int(out_len[b]) // page_size)
+        for p in range(first_released, table.shape[1]):
+            if table[b, p] >= 0:
+                free.add(int(table[b, p]))
+                table[b, p] = -1
+    return {"seq_len": out_len, "page_table": table, "free": free, "bad": bad}
+
+
+def pages_needed(write_pos, n_rows: int, page_size: int) -> list:
+    """Page-table slots that must be mapped to write rows [pos, pos + n_rows)."""
+    out = []
+    for pos in np.asarray(write_pos):
+        p0 = int(pos) // page_size
+        p1 = (int(pos) + n_rows - 1) // page_size
+        out.append(list(range(p0, p1 + 1)))
+    return out
