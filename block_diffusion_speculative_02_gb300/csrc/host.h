@@ -1,0 +1,91 @@
+// Host-side plumbing shared by the ABI entry points: argument checks, the
+// workspace layout, tensor-map encoding and launch helpers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "../../include/dflash.h"
+
+namespace dflash {
+
+constexpr int kBlock = 16;          // staged token + 15 mask positions
+constexpr int kMaxCtxLayers = 8;
+constexpr int kMaxTokens = 512;     // batch * 16
+constexpr int kMaxViews = 4;
+
+// Split-K / split-KV plan for one set of shapes on one device.  The workspace
+// layout and every launch derive from the same plan, so they always agree.
+struct Plan {
+  int num_sms;
+  int ntok;             // batch * 16
+  // context projection
+  int fc_out_tiles;     // hidden / 128
+  int fc_k_tiles;       // nL * hidden / 64
+  int fc_tok_chunks;    // ceil(ntok / 256)
+  int fc_splits;
+  int kv_out_tiles;     // 2 * Hkv * D / 128
+  int kv_k_tiles;       // hidden / 64
+  int kv_tok_chunks;    // ceil(ntok / 128)  (hi + lo columns per chunk)
+  int kv_splits;
+  // block attention
+  int att_rows;         // (Hq / Hkv) * 16 query rows per KV head
+  int att_splits;
+  // workspace offsets (bytes)
+  size_t off_status, off_tickets, off_keys, off_pos, off_fc, off_yhat, off_kv, off_att_o,
+      off_att_ml, total;
+};
+
+int check_dims(const dflash_dims* d);
+int make_plan(const dflash_dims& d, Plan* p);
+int current_num_sms();
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with the given row
+// pitch (bytes), box = box_cols x box_rows, 128-byte swizzle.
+int make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
+                      uint64_t row_pitch_bytes, uint32_t box_cols, uint32_t box_rows);
+// 3-D bf16 tensor map over [d2][d1][d0] with pitches (bytes) for d1 and d2.
+int make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
+                      uint64_t d2, uint64_t pitch1, uint64_t pitch2, uint32_t box0,
+                      uint32_t box1, uint32_t box2);
+
+// inv_freq table of the rotary embedding (theta^(-2d/D), d < D/2) as float
+// hi/lo pairs; filled in double precision on the host.
+void fill_rope_table(float* hi, float* lo, int head_dim, double theta);
+
+// Raise the dynamic shared-memory limit of a kernel once per device.
+int set_smem_limit(const void* func, int bytes);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int cuda_err(cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_E_CUDA; }
+
+template <typename T>
+inline T* ws_at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// Launch with programmatic dependent launch allowed, so that a kernel's
+// prologue may overlap the tail of the previous kernel on the stream.
+template <typename... KArgs, typename... Args>
+inline int launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                  cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  return cuda_err(e);
+}
+
+}  // namespace dflash

@@ -1,0 +1,372 @@
+// a3 — verification epilogue: LM-head GEMM with fused greedy argmax, then
+// acceptance + commit, in one persistent kernel.
+//
+// "dflash-mlx" lossless speculative decoding (dpshk.com), 单次前向验证 ⑤–⑧ and
+// 保证一/保证二: every verify position takes the target's greedy argmax
+// (posterior); acceptance = sum(cumprod(draft == posterior)); 1 + a tokens are
+// committed and the target's token at the first rejected position is the
+// next staged token.
+//
+// Design (GB300): the LM head is a skinny GEMM (16*B token rows against V
+// vocabulary rows) that streams W_lm from HBM exactly once.  It is computed
+// "swap-AB" on the 5th-generation tensor cores: a vocabulary tile of 128 rows
+// is the MMA's M, the token rows are its N, so the fp32 accumulator
+// [128 vocab x ntok] lives in TMEM.  Each CTA owns one contiguous vocabulary
+// range (balanced to 8 rows), streamed through a deep TMA pipeline of
+// 128-row x 64-col swizzled tiles.  The epilogue reduces every token column
+// over the tile's 128 rows with one redux.sync + ballot per column and keeps a
+// 64-bit key (order-preserving fp32 bits << 32 | ~row) per token in shared
+// memory, so logits never leave the SM.  The last CTA to finish (atomic
+// ticket, no waiting) turns the keys into the posterior and runs the
+// acceptance and the commit.
+//
+// Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues the
+// MMAs, warps 2-5 drain the accumulators.
+#include "common.cuh"
+#include "host.h"
+
+namespace dflash {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kTileRows = 128;           // vocabulary rows per MMA (M)
+constexpr int kATileBytes = kTileRows * 128;
+constexpr int kUnitRows = 8;             // balancing granule = one 8-row TMA box
+constexpr int kSmemBudget = 224 * 1024;
+constexpr int kMaxStages = 12;
+
+struct LmParams {
+  int vocab, hidden, ntok;
+  int ntok_box, n_xbox;                  // token rows per X box, X boxes per stage
+  int n_units;                           // ceil(vocab / 8)
+  int n_stages, stage_bytes;
+  int n_acc, tmem_cols;
+  unsigned long long* keys;              // [ntok] workspace, zero between calls
+  uint32_t* ticket;
+  uint32_t* status;
+  int batch;
+  const int32_t* block_ids;
+  const int32_t* len_before;
+  int32_t* posterior;
+  int32_t* accept_len;
+  int32_t* next_staged;
+  int32_t* commit_len;
+  int32_t* out_tokens;
+  int out_cap;
+};
+
+__device__ __forceinline__ void accept_and_commit(const LmParams& p, int b) {
+  int post[kBlock], blk[kBlock];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < kBlock; ++i) {
+    const unsigned long long k = __ldcg(&p.keys[b * kBlock + i]);
+    post[i] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
+    blk[i] = p.block_ids[b * kBlock + i];
+    bad |= (blk[i] < 0 || blk[i] >= p.vocab);
+  }
+  // a = sum(cumprod(block[1:] == posterior[:15]))
+  int a = 0;
+  bool run = true;
+#pragma unroll
+  for (int i = 0; i < kBlock - 1; ++i) {
+    run = run && (blk[i + 1] == post[i]);
+    a += run ? 1 : 0;
+  }
+#pragma unroll
+  for (int i = 0; i < kBlock; ++i) p.posterior[b * kBlock + i] = post[i];
+  p.accept_len[b] = a;
+  if (bad) set_status(p.status, DFLASH_ST_BAD_TOKEN);
+  const int lb = p.len_before[b];
+  if (lb < 0 || lb + 1 + a > p.out_cap) {
+    set_status(p.status, DFLASH_ST_OUT_OVERFLOW);
+    return;
+  }
+  int32_t* dst = p.out_tokens + static_cast<size_t>(b) * p.out_cap + lb;
+  int staged = post[0];
+#pragma unroll
+  for (int i = 0; i < kBlock; ++i) {
+    if (i <= a) dst[i] = blk[i];
+    if (i == a) staged = post[i];
+  }
+  p.next_staged[b] = staged;
+  p.commit_len[b] = lb + 1 + a;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+lmhead_argmax_accept_kernel(const __grid_constant__ CUtensorMap tm_w,
+                            const __grid_constant__ CUtensorMap tm_w8,
+                            const __grid_constant__ CUtensorMap tm_x, const LmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_smem_1024(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.n_stages * p.stage_bytes);
+  uint64_t* empty = full + p.n_stages;
+  uint64_t* tfull = empty + p.n_stages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  unsigned long long* best = reinterpret_cast<unsigned long long*>(tmem_slot + 4);
+
+  // this CTA's vocabulary rows [r0, r1)
+  const int u0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.n_units / gridDim.x);
+  const int u1 =
+      static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.n_units / gridDim.x);
+  const int r0 = u0 * kUnitRows;
+  const int r1 = min(u1 * kUnitRows, p.vocab);
+  const int n_tiles = (r1 - r0 + kTileRows - 1) / kTileRows;
+  const int k_steps = p.hidden / 64;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.n_stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < p.ntok; i += kThreads) best[i] = 0ull;
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_w8);
+    tma_prefetch_desc(&tm_x);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // the hidden states may be produced by the previous kernel on the stream
+  griddep_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_x = l2_policy_evict_last();
+      const uint32_t x_bytes = static_cast<uint32_t>(p.n_xbox * p.ntok_box * 128);
+      uint32_t stage = 0, phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int row0 = r0 + t * kTileRows;
+        const int rows = min(kTileRows, r1 - row0);
+        const int nb8 = (rows + kUnitRows - 1) / kUnitRows;
+        const uint32_t a_bytes = rows == kTileRows ? kATileBytes : nb8 * 1024;
+        for (int kt = 0; kt < k_steps; ++kt) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* a = smem + stage * p.stage_bytes;
+          uint8_t* b = a + kATileBytes;
+          mbar_arrive_expect_tx(&full[stage], a_bytes + x_bytes);
+          if (rows == kTileRows) {
+            tma_load_2d(a, &tm_w, &full[stage], kt * 64, row0, pol_w);
+          } else {
+            for (int j = 0; j < nb8; ++j)
+              tma_load_2d(a + 1024 * j, &tm_w8, &full[stage], kt * 64, row0 + kUnitRows * j,
+                          pol_w);
+          }
+          for (int c = 0; c < p.n_xbox; ++c)
+            tma_load_2d(b + c * p.ntok_box * 128, &tm_x, &full[stage], kt * 64, c * p.ntok_box,
+                        pol_x);
+          ++issued;
+          if (++stage == static_cast<uint32_t>(p.n_stages)) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy still in flight land before the CTA can exit
+        for (int s = 0; s < p.n_stages && s < issued; ++s) {
+          const int last = s + ((issued - 1 - s) / p.n_stages) * p.n_stages;
+          mbar_wait_drain(&full[s], static_cast<uint32_t>((last / p.n_stages) & 1), p.status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      const uint32_t smem_base = smem_u32(smem);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int acc = t % p.n_acc;
+        const uint32_t acc_phase = static_cast<uint32_t>((t / p.n_acc) & 1);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_base = tmem_base + static_cast<uint32_t>(acc * p.ntok);
+        for (int kt = 0; kt < k_steps; ++kt) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_base + stage * p.stage_bytes;
+          const uint32_t b_addr = a_addr + kATileBytes;
+          const uint64_t adesc = umma_sdesc_sw128(a_addr);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            for (int c = 0; c * 256 < p.ntok; ++c) {
+              const int n = min(256, p.ntok - c * 256);
+              const uint64_t bdesc = umma_sdesc_sw128(b_addr + c * 256 * 128);
+              umma_bf16(d_base + c * 256, adesc + 2 * kk, bdesc + 2 * kk,
+                        umma_idesc_bf16(kTileRows, n), (kt | kk) != 0);
+            }
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == static_cast<uint32_t>(p.n_stages)) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok) umma_commit(&tfull[acc]);
+      }
+      umma_commit(done);
+      mbar_wait_drain(done, 0, p.status);
+    }
+  } else {
+    // ---------------- epilogue: argmax over the tile's 128 rows ----------------
+    const int q = warp & 3;  // TMEM lanes this warp may read: 32q .. 32q+31
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int acc = t % p.n_acc;
+      const uint32_t acc_phase = static_cast<uint32_t>((t / p.n_acc) & 1);
+      const bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;  // keep the warp converged for tcgen05.ld
+      tc_fence_after();
+      const int row0 = r0 + t * kTileRows;
+      const int rows = min(kTileRows, r1 - row0);
+      const bool valid = (q * 32 + lane) < rows;
+      for (int c0 = 0; c0 < p.ntok; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tmem_base + lane_base + static_cast<uint32_t>(acc * p.ntok + c0), v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t key = valid ? float_order_key(__uint_as_float(v[j])) : 0u;
+          const uint32_t m = warp_max_u32(key);
+          const uint32_t ball = __ballot_sync(0xffffffffu, valid && key == m);
+          if (ball != 0u && lane == j) {
+            const uint32_t row = static_cast<uint32_t>(row0 + q * 32 + (__ffs(ball) - 1));
+            atomicMax(&best[c0 + j],
+                      (static_cast<unsigned long long>(m) << 32) | (0xFFFFFFFFu - row));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  __syncthreads();
+  griddep_launch_dependents();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+  if (warp >= 2) {
+    const int et = threadIdx.x - 64;
+    for (int i = et; i < p.ntok; i += 128) {
+      const unsigned long long b = best[i];
+      if (b) atomicMax(&p.keys[i], b);
+    }
+    __threadfence();
+    named_bar_sync(1, 128);
+    if (et == 0) *last_flag = (atomicAdd(p.ticket, 1u) == gridDim.x - 1) ? 1 : 0;
+    named_bar_sync(1, 128);
+    if (*last_flag) {
+      __threadfence();
+      for (int b = et; b < p.batch; b += 128) accept_and_commit(p, b);
+      named_bar_sync(1, 128);
+      for (int i = et; i < p.ntok; i += 128) p.keys[i] = 0ull;
+      if (et == 0) *p.ticket = 0u;
+    }
+  }
+}
+
+}  // namespace
+}  // namespace dflash
+
+using namespace dflash;
+
+extern "C" int dflash_verify_accept(const dflash_dims* dims, const void* hidden,
+                                    const void* w_lm, const int32_t* block_ids,
+                                    const int32_t* len_before, int32_t* posterior,
+                                    int32_t* accept_len, int32_t* next_staged,
+                                    int32_t* commit_len, int32_t* out_tokens, int32_t out_cap,
+                                    void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (!hidden || !w_lm || !block_ids || !len_before || !posterior || !accept_len ||
+      !next_staged || !commit_len || !out_tokens || out_cap < 1)
+    return DFLASH_E_ARG;
+  if (!aligned16(hidden) || !aligned16(w_lm)) return DFLASH_E_ALIGN;
+  if (!ws) return DFLASH_E_WORKSPACE;
+  Plan plan;
+  if ((rc = make_plan(*dims, &plan))) return rc;
+  if (ws_bytes < plan.total) return DFLASH_E_WORKSPACE;
+
+  LmParams p = {};
+  p.vocab = dims->vocab;
+  p.hidden = dims->hidden;
+  p.ntok = plan.ntok;
+  p.ntok_box = p.ntok <= 256 ? p.ntok : 256;
+  p.n_xbox = (p.ntok + p.ntok_box - 1) / p.ntok_box;
+  p.n_units = (p.vocab + kUnitRows - 1) / kUnitRows;
+  const int x_bytes = ((p.n_xbox * p.ntok_box * 128) + 1023) / 1024 * 1024;
+  p.stage_bytes = kATileBytes + x_bytes;
+  const int fixed = 1024 /*alignment slack*/ + 8 * 5 + 16 + 8 * p.ntok + 64;
+  p.n_stages = (kSmemBudget - fixed) / (p.stage_bytes + 16);
+  if (p.n_stages > kMaxStages) p.n_stages = kMaxStages;
+  if (p.n_stages < 2) return DFLASH_E_UNSUPPORTED;
+  p.n_acc = (2 * p.ntok <= 512) ? 2 : 1;
+  int cols = 32;
+  while (cols < p.n_acc * p.ntok) cols *= 2;
+  p.tmem_cols = cols;
+  p.keys = ws_at<unsigned long long>(ws, plan.off_keys);
+  p.ticket = ws_at<uint32_t>(ws, plan.off_tickets);
+  p.status = ws_at<uint32_t>(ws, plan.off_status);
+  p.batch = dims->batch;
+  p.block_ids = block_ids;
+  p.len_before = len_before;
+  p.posterior = posterior;
+  p.accept_len = accept_len;
+  p.next_staged = next_staged;
+  p.commit_len = commit_len;
+  p.out_tokens = out_tokens;
+  p.out_cap = out_cap;
+
+  CUtensorMap tm_w, tm_w8, tm_x;
+  const uint64_t pitch = static_cast<uint64_t>(dims->hidden) * 2;
+  if ((rc = make_tmap_2d_bf16(&tm_w, w_lm, dims->hidden, dims->vocab, pitch, 64, kTileRows)))
+    return rc;
+  if ((rc = make_tmap_2d_bf16(&tm_w8, w_lm, dims->hidden, dims->vocab, pitch, 64, kUnitRows)))
+    return rc;
+  if ((rc = make_tmap_2d_bf16(&tm_x, hidden, dims->hidden, p.ntok, pitch, 64, p.ntok_box)))
+    return rc;
+
+  const int smem = p.n_stages * (p.stage_bytes + 16) + fixed;
+  if ((rc = set_smem_limit(reinterpret_cast<const void*>(lmhead_argmax_accept_kernel), smem)))
+    return rc;
+  const int grid = plan.num_sms < p.n_units ? plan.num_sms : p.n_units;
+  return launch(lmhead_argmax_accept_kernel, dim3(grid), dim3(kThreads), smem,
+                reinterpret_cast<cudaStream_t>(stream), tm_w, tm_w8, tm_x, p);
+}

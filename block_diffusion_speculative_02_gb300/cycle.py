@@ -1,0 +1,66 @@
+"""One draft/verify cycle as a sequence of the four ABI calls.
+
+"dflash-mlx" (dpshk.com) 单次前向验证 ⑤–⑨ and "DFlash双实现对比"
+(hotelren.com) §2–§4: verify the block (LM head + greedy argmax +
+acceptance + commit), project the block's target hidden states into the
+drafter's context K/V, crop the target and drafter caches to the committed
+length, then run the drafter's dual-source block attention for the next
+block.  This module only holds device buffers and issues the calls; every
+step runs in the CUDA library.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import List, Optional
+
+import torch
+
+from .dflash import (Dims, KVView, dflash_block_attention, dflash_ctx_project, dflash_kv_crop,
+                     dflash_verify_accept)
+
+
+@dataclass
+class CycleWeights:
+    w_lm: torch.Tensor               # bf16 [V, H]
+    w_fc: torch.Tensor               # bf16 [H, nL*H]
+    hidden_norm_w: Optional[torch.Tensor]  # bf16 [H]
+    w_k: torch.Tensor                # bf16 [Hkv*D, H]
+    w_v: torch.Tensor                # bf16 [Hkv*D, H]
+    k_norm_w: Optional[torch.Tensor]  # bf16 [D]
+
+
+@dataclass
+class CycleState:
+    """Inputs, outputs and caches of one cycle for a batch of sequences."""
+    layer_hidden: List[torch.Tensor]  # nL x bf16 [B*16, H]  (selected target layers)
+    verify_hidden: torch.Tensor       # bf16 [B*16, H]        (final-normed target hidden)
+    block_ids: torch.Tensor           # int32 [B, 16]
+    len_before: torch.Tensor          # int32 [B] committed length before the cycle
+    write_pos: torch.Tensor           # int32 [B] first context row of the block
+    q_blk: torch.Tensor               # bf16 [B, 16, Hq, D]   (next block, pre-RoPE)
+    k_blk: torch.Tensor               # bf16 [B, 16, Hkv, D]
+    v_blk: torch.Tensor               # bf16 [B, 16, Hkv, D]
+    draft_cache: KVView
+    target_view: KVView
+    posterior: torch.Tensor           # int32 [B, 16]
+    accept_len: torch.Tensor          # int32 [B]
+    next_staged: torch.Tensor         # int32 [B]
+    commit_len: torch.Tensor          # int32 [B]
+    out_tokens: torch.Tensor          # int32 [B, out_cap]
+    attn_out: torch.Tensor            # bf16 [B, 16, Hq, D]
+
+
+def run_cycle(dims: Dims, w: CycleWeights, st: CycleState, ws: torch.Tensor,
+              scale: Optional[float] = None, stream=None):
+    """Issue one cycle on the current (or given) stream."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(dims.head_dim)
+    dflash_verify_accept(dims, st.verify_hidden, w.w_lm, st.block_ids, st.len_before,
+                         st.posterior, st.accept_len, st.next_staged, st.commit_len,
+                         st.out_tokens, ws, stream)
+    dflash_ctx_project(dims, st.layer_hidden, w.w_fc, w.hidden_norm_w, w.w_k, w.w_v, w.k_norm_w,
+                       st.write_pos, st.draft_cache, ws, stream)
+    dflash_kv_crop([st.target_view, st.draft_cache], st.commit_len, dims.batch, ws, stream)
+    dflash_block_attention(dims, st.q_blk, st.k_blk, st.v_blk, st.draft_cache, scale,
+                           st.attn_out, ws, stream)

@@ -1,0 +1,210 @@
+/*
+ * dflash.h — C ABI of the DFlash per-cycle hot path on one GB300 (sm_103a).
+ *
+ * One draft/verify cycle of block-diffusion speculative decoding, as the
+ * DFlash pages describe it:
+ *   [P1] "DFlash双实现对比：PyTorch与MLX代码架构差异深度分析" (hotelren.com)
+ *        §2 attention (dual-source K/V), §3 KV-cache crop, §4 target-layer
+ *        hidden states concatenated by target_layer_ids.
+ *   [P2] "dflash-mlx" lossless speculative decoding (dpshk.com)
+ *        块扩散草稿 (block = staged token + 15 masks; drafter reads target
+ *        hidden states), 单次前向验证 ①–⑨ (the cycle), 保证二 (acceptance
+ *        = sum(cumprod(draft == posterior))), 保证三 (cache cut back to the
+ *        committed length).
+ *
+ * Conventions shared by every call
+ *  - All pointers are borrowed.  Device buffers are owned by the caller; the
+ *    library never allocates device memory.  Scratch lives in a caller
+ *    workspace of dflash_workspace_bytes() bytes, zeroed once with
+ *    dflash_workspace_init(); every call leaves its part of it zeroed again.
+ *    Calls that share a workspace must be ordered on the GPU (same stream or
+ *    events), except dflash_ctx_project and dflash_verify_accept, which use
+ *    disjoint parts of it and may run concurrently on two streams.
+ *  - Every call is asynchronous on `stream` and never synchronises the host,
+ *    except dflash_read_status.  Lengths stay on the device, so a whole cycle
+ *    can be captured in a CUDA graph.
+ *  - A negative return value is a host-detected error (bad argument, layout,
+ *    alignment, workspace too small, CUDA launch error): nothing is launched.
+ *  - Errors found on the device (a length out of range, an exhausted page
+ *    pool, ...) set DFLASH_ST_* bits in a status word inside the workspace,
+ *    leave the offending sequence's state unchanged, and never trap.  Read
+ *    them with dflash_read_status.
+ *  - bf16 is IEEE bfloat16; every bf16 result is rounded to nearest even.
+ *    Matrix products accumulate in fp32.
+ *  - Device pointers handed to TMA (weights, hidden states, caches) must be
+ *    16-byte aligned and their rows a multiple of 16 bytes.
+ */
+#ifndef DFLASH_H_
+#define DFLASH_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define DFLASH_API __attribute__((visibility("default")))
+#else
+#define DFLASH_API
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* dflash_stream_t;
+
+/* Host-side return codes. */
+#define DFLASH_OK 0
+#define DFLASH_E_ARG (-1)          /* null pointer, bad size or shape        */
+#define DFLASH_E_ALIGN (-2)        /* pointer or row pitch not 16-B aligned   */
+#define DFLASH_E_UNSUPPORTED (-3)  /* shape the kernels do not implement      */
+#define DFLASH_E_WORKSPACE (-4)    /* workspace null or too small             */
+#define DFLASH_E_CUDA (-5)         /* CUDA runtime/driver error at launch     */
+
+/* Device status-word bits (OR-ed; read with dflash_read_status). */
+#define DFLASH_ST_CROP_GROW (1u << 0)     /* crop asked to grow or go negative      */
+#define DFLASH_ST_OUT_OVERFLOW (1u << 1)  /* commit would pass out_cap              */
+#define DFLASH_ST_PAGE_MISSING (1u << 2)  /* unmapped page inside a used range      */
+#define DFLASH_ST_POOL_EMPTY (1u << 3)    /* page pool exhausted while reserving    */
+#define DFLASH_ST_BAD_TOKEN (1u << 4)     /* block id outside [0, vocab)            */
+#define DFLASH_ST_CAPACITY (1u << 5)      /* length or write past the cache capacity */
+#define DFLASH_ST_TIMEOUT (1u << 6)       /* a bounded in-kernel wait gave up       */
+
+/* Model and cycle shapes.  block must be 16 (staged token + 15 masks,
+ * [P2] 块扩散草稿 step 1).  Supported: head_dim in {64, 128};
+ * n_q_heads % n_kv_heads == 0 with (n_q_heads / n_kv_heads) * 16 <= 128;
+ * hidden % 128 == 0; (n_kv_heads * head_dim) % 128 == 0; 1 <= n_ctx_layers <= 8;
+ * batch * 16 <= 512. */
+typedef struct {
+  int32_t batch;         /* B: sequences in the step                       */
+  int32_t block;         /* T: tokens per block, 16                        */
+  int32_t hidden;        /* H: target (and drafter) hidden size            */
+  int32_t n_q_heads;     /* Hq                                             */
+  int32_t n_kv_heads;    /* Hkv                                            */
+  int32_t head_dim;      /* D                                              */
+  int32_t vocab;         /* V                                              */
+  int32_t n_ctx_layers;  /* nL: target layers concatenated ([P1] §4)       */
+  int32_t max_ctx;       /* upper bound on any context length; sizes the
+                            attention split-K scratch                       */
+  float rope_theta;      /* RoPE base (Qwen3: 1e6)                          */
+  float rms_eps;         /* RMSNorm epsilon (1e-6)                          */
+} dflash_dims;
+
+/* A KV cache as the kernels see it.
+ *  contiguous (page_table == NULL): k, v are bf16 [B, capacity, Hkv, D].
+ *  paged      (page_table != NULL): k, v are bf16 [n_pages, page_size, Hkv, D];
+ *             page_table is int32 [B, max_pages] (-1 = unmapped); the free
+ *             pages are free_list[0 .. *free_count) (int32, device).
+ *  seq_len is int32 [B] on the device: the number of valid rows.
+ *  k and v may be NULL for dflash_kv_crop, which touches only lengths and pages. */
+typedef struct {
+  void* k;
+  void* v;
+  int32_t* seq_len;
+  int32_t* page_table;
+  int32_t* free_list;
+  int32_t* free_count;
+  int32_t capacity;    /* contiguous: rows per sequence; paged: max_pages * page_size */
+  int32_t page_size;   /* paged: 16                                                   */
+  int32_t max_pages;   /* paged: page-table columns                                   */
+  int32_t n_pages;     /* paged: pool size                                            */
+} dflash_kv_view;
+
+/* Bytes of workspace needed by every call below for these shapes on the
+ * current device (split counts depend on its SM count).  0 on bad dims. */
+DFLASH_API size_t dflash_workspace_bytes(const dflash_dims* dims);
+
+/* Zero a workspace (cudaMemsetAsync on `stream`). */
+DFLASH_API int dflash_workspace_init(void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/*
+ * a1 — context projection ([P1] §4 and §2; [P2] 块扩散草稿 step 3).
+ *   X  = [h_1 | ... | h_nL]                rows = B*16 tokens, nL*H features
+ *   Y  = X W_fc^T                           fp32, H features
+ *   Y^ = RMSNorm(Y) * hidden_norm_w         (skipped when hidden_norm_w == NULL)
+ *   K  = RoPE_pos(RMSNorm_head(Y^ W_k^T) * k_norm_w)   (head norm skipped when NULL)
+ *   V  = Y^ W_v^T
+ * and writes K, V (bf16) into `cache` at rows write_pos[b] + t, t = 0..15,
+ * RoPE position = that row index.  For a paged cache, unmapped pages covering
+ * those rows are first taken from the free list.  Finally
+ * cache->seq_len[b] = write_pos[b] + 16 (the crop then trims it to the
+ * committed length).  write_pos may alias cache->seq_len.
+ *   layer_hidden: HOST array of nL device pointers, each bf16 [B*16, H]
+ *                 (row b*16 + t), in target_layer_ids order.
+ *   w_fc: bf16 [H, nL*H] (row = output feature).  w_k, w_v: bf16 [Hkv*D, H].
+ *   hidden_norm_w: bf16 [H] or NULL.  k_norm_w: bf16 [D] or NULL.
+ *   write_pos: int32 [B] device.
+ * Errors: DFLASH_ST_CAPACITY / DFLASH_ST_PAGE_MISSING / DFLASH_ST_POOL_EMPTY
+ * skip the affected rows.
+ */
+DFLASH_API int dflash_ctx_project(const dflash_dims* dims, const void* const* layer_hidden,
+                       const void* w_fc, const void* hidden_norm_w, const void* w_k,
+                       const void* w_v, const void* k_norm_w, const int32_t* write_pos,
+                       const dflash_kv_view* cache, void* ws, size_t ws_bytes,
+                       dflash_stream_t stream);
+
+/*
+ * a2 — dual-source block attention ([P1] §2; [P2] 块扩散草稿).
+ * For sequence b (L = cache->seq_len[b]), query head h, block row i:
+ *   q   = RoPE_{L+i}(q_blk[b,i,h])
+ *   K   = ctx K rows 0..L-1 of KV head g = h / (Hq/Hkv)   (stored rotated)
+ *         ⊕ RoPE_{L+j}(k_blk[b,j,g]), j = 0..15
+ *   V   = ctx V rows 0..L-1 ⊕ v_blk[b,j,g]
+ *   out[b,i,h] = softmax(q K^T * scale) V      (no mask: non-causal in the block)
+ *   q_blk: bf16 [B,16,Hq,D]; k_blk, v_blk: bf16 [B,16,Hkv,D] (before RoPE);
+ *   out: bf16 [B,16,Hq,D].  Lengths above cache capacity set DFLASH_ST_CAPACITY
+ *   (that sequence's output is left unwritten); unmapped pages inside the
+ *   length set DFLASH_ST_PAGE_MISSING and are read as zeros.
+ */
+DFLASH_API int dflash_block_attention(const dflash_dims* dims, const void* q_blk, const void* k_blk,
+                           const void* v_blk, const dflash_kv_view* cache, float scale,
+                           void* out, void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/*
+ * a3 — verification epilogue ([P2] 单次前向验证 ⑤–⑧, 保证一, 保证二).
+ *   logits[b,i,:] = hidden[b,i,:] W_lm^T        (fp32, never written to memory)
+ *   posterior[b,i] = argmax (lowest index on exact ties)
+ *   accept_len[b] = sum_{i<15} prod_{j<=i} [block_ids[b,j+1] == posterior[b,j]]
+ *   out_tokens[b, len_before[b] + i] = block_ids[b,i], i = 0..accept_len[b]
+ *   next_staged[b] = posterior[b, accept_len[b]]
+ *   commit_len[b]  = len_before[b] + 1 + accept_len[b]
+ *   hidden: bf16 [B,16,H] (final-normed); w_lm: bf16 [V,H];
+ *   block_ids, posterior: int32 [B,16]; len_before, accept_len, next_staged,
+ *   commit_len: int32 [B]; out_tokens: int32 [B, out_cap].
+ *   len_before may alias commit_len.  A commit that would pass out_cap sets
+ *   DFLASH_ST_OUT_OVERFLOW and leaves out_tokens, next_staged and commit_len of
+ *   that sequence unchanged (posterior and accept_len are still written).
+ *   Block ids outside [0, vocab) set DFLASH_ST_BAD_TOKEN (they never match).
+ */
+DFLASH_API int dflash_verify_accept(const dflash_dims* dims, const void* hidden, const void* w_lm,
+                         const int32_t* block_ids, const int32_t* len_before,
+                         int32_t* posterior, int32_t* accept_len, int32_t* next_staged,
+                         int32_t* commit_len, int32_t* out_tokens, int32_t out_cap,
+                         void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/*
+ * a4 — KV-cache crop ([P1] §3; [P2] 单次前向验证 ⑨, 保证三).
+ * For each of the n_views caches (target view, drafter view, ...) and each
+ * sequence b: seq_len[b] <- new_len[b].  Rows below new_len are untouched.
+ * Paged views: every mapped page that starts at or after new_len[b] is pushed
+ * back on the free list and its table slot set to -1 (the partly used last
+ * page is kept).  new_len > seq_len or new_len < 0 sets DFLASH_ST_CROP_GROW
+ * and leaves that sequence unchanged.  n_views <= 4.  views is a HOST array.
+ */
+DFLASH_API int dflash_kv_crop(const dflash_kv_view* views, int32_t n_views, const int32_t* new_len,
+                   int32_t batch, void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/* Copy the status word to *host_status (synchronises `stream`); if clear != 0
+ * reset it to zero afterwards. */
+DFLASH_API int dflash_read_status(void* ws, uint32_t* host_status, int clear, dflash_stream_t stream);
+
+/* Text for a return code. */
+DFLASH_API const char* dflash_status_string(int code);
+
+/* Library ABI version (major * 100 + minor). */
+DFLASH_API int dflash_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H_ */

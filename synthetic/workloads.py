@@ -316,3 +316,34 @@ def pack_contiguous(per_seq: list, capacity: int, row_shape) -> np.ndarray:
     for b, rows in enumerate(per_seq):
         out[b, :rows.shape[0]] = rows
     return out
+
+
+# --------------------------------------------------------------------------
+# device-side generation (bench workloads: same distributions, generated on
+# the GPU with a seeded torch generator so that gigabytes of weights do not
+# have to be drawn on the host)
+# --------------------------------------------------------------------------
+def device_generator(cfg: CycleConfig, stream_name: str, device="cuda"):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(1000 * (1 + cfg.seed_index) + STREAMS.index(stream_name))
+    return g
+
+
+def device_normal_bf16(gen, shape, std: float = 1.0, mean: float = 0.0, device="cuda"):
+    """i.i.d. N(mean, std^2) as a CUDA bf16 tensor (round to nearest even)."""
+    import torch
+    x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    if mean != 0.0:
+        x.add_(mean)
+    return x.to(torch.bfloat16)
+
+
+def device_unit_rms_rows_bf16(gen, shape, device="cuda"):
+    """Rows of N(0,1) values rescaled to unit root-mean-square, CUDA bf16."""
+    import torch
+    x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    x = x / x.pow(2).mean(dim=-1, keepdim=True).sqrt()
+    return x.to(torch.bfloat16)
