@@ -260,7 +260,7 @@ def build_workload(cfg, n_sets: int, device="cuda"):
 
 def algorithmic_bytes(cfg, lens) -> dict:
     """Bytes one cycle must move at least: every weight once, the context KV of
-    one drafter layer once, activations once (SURVEY-style accounting)."""
+    one drafter layer once, activations once."""
     B, H, V = cfg.batch, cfg.hidden, cfg.vocab
     Hq, Hkv, D, nL = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.n_ctx_layers
     T = 16

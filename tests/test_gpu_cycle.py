@@ -1,0 +1,124 @@
+"""Several consecutive draft/verify cycles on the GPU, state carried on the
+device (write position aliasing the drafter length, committed length
+aliasing the next cycle's len_before), against the oracle run through the
+same sequence: ctx rows, lengths, pages, tokens and attention outputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle.dflash_oracle import block_attention as ref_attention
+from oracle.dflash_oracle import ctx_project as ref_project
+from oracle.dflash_oracle import bf16_to_f64, kv_crop_lengths
+from oracle.dflash_oracle import verify_accept as ref_verify
+from synthetic import (draw_accept_lengths, make_block_ids, make_paged_layout, normal_bf16,
+                       pack_contiguous, scatter_paged, unit_rms_rows_bf16)
+from tests.gpu_helpers import assert_close_bf16, check_verify, dev_bf16, dev_i32, host_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_three_cycles_carry_state(paged):
+    import block_diffusion_speculative_02_gb300 as dfl
+    from block_diffusion_speculative_02_gb300.cycle import CycleState, CycleWeights, run_cycle
+
+    rng = np.random.default_rng(42 + paged)
+    B, H, Hq, Hkv, D, V, nL = 2, 256, 4, 2, 64, 4096, 2
+    theta, eps = 1e6, 1e-6
+    L0 = np.array([100, 37], np.int32)
+    w_lm = normal_bf16(rng, (V, H), 0.02)
+    w_fc = normal_bf16(rng, (H, nL * H), 0.02)
+    gh = normal_bf16(rng, (H,), 0.02, 1.0)
+    wk = normal_bf16(rng, (Hkv * D, H), 0.02)
+    wv = normal_bf16(rng, (Hkv * D, H), 0.02)
+    gk = normal_bf16(rng, (D,), 0.02, 1.0)
+    ctx_k = [normal_bf16(rng, (int(L), Hkv, D)) for L in L0]
+    ctx_v = [normal_bf16(rng, (int(L), Hkv, D)) for L in L0]
+    cap = 200
+    dims = dfl.make_dims(B, H, Hq, Hkv, D, V, nL, cap, theta, eps)
+    ws = dfl.alloc_workspace(dims)
+    if paged:
+        lay = make_paged_layout(rng, L0, reserve_tokens=64, max_len=cap)
+        draft = dfl.KVView(dev_bf16(scatter_paged(lay, ctx_k, (Hkv, D))),
+                           dev_bf16(scatter_paged(lay, ctx_v, (Hkv, D))), dev_i32(L0),
+                           capacity=lay.max_pages * 16, page_table=dev_i32(lay.page_table),
+                           free_list=dev_i32(lay.free_list), free_count=dev_i32([lay.free_count]))
+    else:
+        draft = dfl.KVView(dev_bf16(pack_contiguous(ctx_k, cap, (Hkv, D))),
+                           dev_bf16(pack_contiguous(ctx_v, cap, (Hkv, D))), dev_i32(L0),
+                           capacity=cap)
+    target = dfl.KVView(None, None, dev_i32(L0 + 16), capacity=cap)
+    w = CycleWeights(dev_bf16(w_lm), dev_bf16(w_fc), dev_bf16(gh), dev_bf16(wk), dev_bf16(wv),
+                     dev_bf16(gk))
+    commit = dev_i32(L0)                         # len_before of the next cycle aliases it
+    out_tokens = torch.full((B, cap + 16), -1, dtype=torch.int32, device="cuda")
+    ref_out = np.full((B, cap + 16), -1, np.int32)
+    # oracle state: float64 context rows and lengths
+    ref_k = [bf16_to_f64(x) for x in ctx_k]
+    ref_v = [bf16_to_f64(x) for x in ctx_v]
+    L = L0.copy()
+    for cyc in range(3):
+        hv = unit_rms_rows_bf16(rng, (B, 16, H))
+        layers = [unit_rms_rows_bf16(rng, (B * 16, H)) for _ in range(nL)]
+        q = normal_bf16(rng, (B, 16, Hq, D))
+        kb = normal_bf16(rng, (B, 16, Hkv, D))
+        vb = normal_bf16(rng, (B, 16, Hkv, D))
+        post0 = ref_verify(hv, w_lm, np.zeros((B, 16), np.int32), L, out_cap=cap + 16)
+        blk = make_block_ids(rng, post0["posterior"], draw_accept_lengths(rng, ("uniform",), B), V)
+        # ---- oracle cycle ----
+        rv = ref_verify(hv, w_lm, blk, L, out_tokens=ref_out)
+        ref_out = rv["out_tokens"]
+        pos = np.repeat(L, 16) + np.tile(np.arange(16), B)
+        rp = ref_project(layers, w_fc, gh, wk, wv, gk, pos, Hkv, D, theta, eps)
+        for b in range(B):
+            ref_k[b] = np.concatenate([ref_k[b][:L[b]], rp["k"][16 * b:16 * b + 16]])
+            ref_v[b] = np.concatenate([ref_v[b][:L[b]], rp["v"][16 * b:16 * b + 16]])
+        newL, bad = kv_crop_lengths(L + 16, rv["commit_len"])
+        assert not bad.any()
+        ro = ref_attention(q, kb, vb, ref_k, ref_v, newL, theta, 1 / math.sqrt(D))
+        # ---- GPU cycle ----
+        target.seq_len.copy_(commit + 16)        # the target's verify forward appended 16 rows
+        st = CycleState(
+            layer_hidden=[dev_bf16(x) for x in layers], verify_hidden=dev_bf16(hv.reshape(B * 16, H)),
+            block_ids=dev_i32(blk), len_before=commit, write_pos=draft.seq_len,
+            q_blk=dev_bf16(q), k_blk=dev_bf16(kb), v_blk=dev_bf16(vb), draft_cache=draft,
+            target_view=target, posterior=torch.zeros((B, 16), dtype=torch.int32, device="cuda"),
+            accept_len=torch.zeros(B, dtype=torch.int32, device="cuda"),
+            next_staged=torch.zeros(B, dtype=torch.int32, device="cuda"), commit_len=commit,
+            out_tokens=out_tokens,
+            attn_out=torch.zeros((B, 16, Hq, D), dtype=torch.bfloat16, device="cuda"))
+        run_cycle(dims, w, st, ws)
+        torch.cuda.synchronize()
+        assert dfl.dflash_read_status(ws) == 0
+        got = {"posterior": st.posterior.cpu().numpy(), "accept": st.accept_len.cpu().numpy(),
+               "next_staged": st.next_staged.cpu().numpy(),
+               "commit_len": commit.cpu().numpy(), "out_tokens": out_tokens.cpu().numpy()}
+        info = check_verify(rv, got, L)
+        assert info["excluded_seqs"] == 0
+        assert np.array_equal(draft.seq_len.cpu().numpy(), newL)
+        assert np.array_equal(target.seq_len.cpu().numpy(), newL)
+        assert_close_bf16(host_f64(st.attn_out), ro)
+        # the block's context rows as written on the GPU (first 1 + a of them survive)
+        kk = host_f64(draft.k)
+        for b in range(B):
+            for t in range(int(newL[b] - L[b])):
+                r = int(L[b]) + t
+                if paged:
+                    pg = draft.page_table.cpu().numpy()[b, r // 16]
+                    row = kk[pg, r % 16]
+                else:
+                    row = kk[b, r]
+                np.testing.assert_allclose(row, ref_k[b][r], atol=2e-2)
+        L = newL
+        ref_k = [ref_k[b][:L[b]] for b in range(B)]
+        ref_v = [ref_v[b][:L[b]] for b in range(B)]
+    if paged:
+        fc = int(draft.free_count.item())
+        table = draft.page_table.cpu().numpy()
+        mapped = set(table[table >= 0].tolist())
+        free = set(draft.free_list.cpu().numpy()[:fc].tolist())
+        assert mapped.isdisjoint(free) and len(mapped) + len(free) == lay.n_pages
+        for b in range(B):
+            assert (table[b] >= 0).sum() == -(-int(L[b]) // 16)

@@ -7,7 +7,7 @@ import torch
 
 from oracle.dflash_oracle import ctx_project as ref_project
 from oracle.dflash_oracle import pages_needed
-from synthetic import (CONFIGS, make_cycle_inputs, make_paged_layout, normal_bf16,
+from synthetic import (CONFIG_BY_NAME, make_cycle_inputs, make_paged_layout, normal_bf16,
                        unit_rms_rows_bf16)
 from tests.gpu_helpers import assert_close_bf16, dev_bf16, dev_i32, host_bits, host_f64
 
@@ -180,9 +180,10 @@ def test_project_flags_an_exhausted_page_pool():
     assert int(view.free_count.item()) == 0
 
 
-@pytest.mark.parametrize("idx", [1, 2, 3, 4])
-def test_project_full_size(idx):
-    cfg = CONFIGS[idx]
+@pytest.mark.parametrize("name", ["qwen3_4b_b1", "qwen3_8b_b1", "qwen3_8b_b32_paged",
+                                  "qwen3_32b_b4_32k"])
+def test_project_full_size(name):
+    cfg = CONFIG_BY_NAME[name]
     inp = make_cycle_inputs(cfg, with_lm=False)
     pos = inp.ctx_len
     _, _, ek, ev = check_project(inp.layer_hidden, inp.w_fc, inp.hidden_norm_w, inp.w_k, inp.w_v,

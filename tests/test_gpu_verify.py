@@ -5,7 +5,7 @@ import pytest
 import torch
 
 from oracle.dflash_oracle import verify_accept as ref_verify
-from synthetic import (CONFIGS, draw_accept_lengths, make_block_ids, make_cycle_inputs,
+from synthetic import (CONFIG_BY_NAME, draw_accept_lengths, make_block_ids, make_cycle_inputs,
                        normal_bf16, unit_rms_rows_bf16)
 from tests.gpu_helpers import check_verify, dev_bf16, dev_i32
 
@@ -143,10 +143,11 @@ def test_overflow_and_bad_token_set_status_and_skip_commit():
     check_verify({k: v[:1] for k, v in ref.items()}, {k: v[:1] for k, v in r.items()}, lb[:1])
 
 
-@pytest.mark.parametrize("idx", [1, 2, 3, 4])
-def test_verify_parity_full_size(idx):
+@pytest.mark.parametrize("name", ["qwen3_4b_b1", "qwen3_8b_b1", "qwen3_8b_b32_paged",
+                                  "qwen3_32b_b4_32k"])
+def test_verify_parity_full_size(name):
     """The benchmark configurations at full size (vocabulary 151936)."""
-    cfg = CONFIGS[idx]
+    cfg = CONFIG_BY_NAME[name]
     inp = make_cycle_inputs(cfg)
     B = cfg.batch
     ref0 = ref_verify(inp.verify_hidden, inp.w_lm, np.zeros((B, 16), np.int32),

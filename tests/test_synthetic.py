@@ -3,7 +3,7 @@ draft planting and the paged-cache layout."""
 import numpy as np
 import torch
 
-from synthetic import (CONFIGS, bf16_bits_to_f32, draw_accept_lengths, f32_to_bf16_bits,
+from synthetic import (CONFIG_BY_NAME, CONFIGS, bf16_bits_to_f32, draw_accept_lengths, f32_to_bf16_bits,
                        geometric_ratio_for_mean, make_block_ids, make_paged_layout,
                        scatter_paged)
 
@@ -70,6 +70,6 @@ def test_paged_layout_is_a_partition():
 def test_config_shapes():
     names = [c.name for c in CONFIGS]
     assert names[2] == "qwen3_8b_b1"
-    c = CONFIGS[2]
+    c = CONFIG_BY_NAME["qwen3_8b_b1"]
     assert (c.hidden, c.n_q_heads, c.n_kv_heads, c.head_dim, c.vocab, c.ctx_in) == \
         (4096, 32, 8, 128, 151936, 20480)
