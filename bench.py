@@ -45,6 +45,8 @@ def parse_args(argv=None):
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sets", type=int, default=0,
+                    help="rotating input sets (0: enough to exceed twice the L2 size)")
     return ap.parse_args(argv)
 
 
@@ -395,7 +397,7 @@ def main(argv=None):
 
     kv_bytes_per_set = 2 * cfg.n_kv_heads * cfg.head_dim * 2 * (
         cfg.batch * (cfg.ctx_len or cfg.ctx_len_range[1]) + 32)
-    n_sets = max(1, min(16, math.ceil(2 * L2_BYTES / max(1, kv_bytes_per_set))))
+    n_sets = args.sets or max(1, min(16, math.ceil(2 * L2_BYTES / max(1, kv_bytes_per_set))))
     dims, w, states, accepts, ws, lens = build_workload(cfg, n_sets)
     stream = torch.cuda.current_stream()
 

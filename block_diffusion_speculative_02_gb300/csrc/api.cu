@@ -11,6 +11,10 @@ namespace dflash {
 
 namespace {
 
+#ifndef DFLASH_TMAP_L2_PROMOTION
+#define DFLASH_TMAP_L2_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+#endif
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -86,6 +90,7 @@ int make_plan(const dflash_dims& d, Plan* p) {
     const int by_len = (d.max_ctx + 4095) / 4096;
     if (s < by_len) s = by_len;
     if (s > pages) s = pages;
+    if (s > 64) s = 64;  // the split merge keeps one split per lane, two per lane at most
     if (s < 1) s = 1;
     q.att_splits = s;
   }
@@ -94,6 +99,10 @@ int make_plan(const dflash_dims& d, Plan* p) {
   q.off_tickets = off; off += 192;
   q.off_keys = off;    off = align_up(off + sizeof(unsigned long long) * q.ntok, 256);
   q.off_pos = off;     off = align_up(off + sizeof(int32_t) * d.batch, 256);
+  q.off_ctx_tickets = off;
+  off = align_up(off + sizeof(uint32_t) * (q.fc_out_tiles * q.fc_tok_chunks +
+                                           q.kv_out_tiles * q.kv_tok_chunks), 256);
+  q.off_ss = off;      off = align_up(off + sizeof(float) * (size_t)q.fc_out_tiles * q.ntok, 256);
   q.off_fc = off;
   off = align_up(off + sizeof(float) * (size_t)q.fc_splits * q.ntok * d.hidden, 256);
   q.off_yhat = off;    off = align_up(off + 2 * sizeof(uint16_t) * (size_t)q.ntok * d.hidden, 1024);
@@ -118,7 +127,7 @@ int make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_SWIZZLE_128B, DFLASH_TMAP_L2_PROMOTION,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_E_ALIGN;
 }
@@ -134,7 +143,7 @@ int make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t 
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_SWIZZLE_128B, DFLASH_TMAP_L2_PROMOTION,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DFLASH_OK : DFLASH_E_ALIGN;
 }

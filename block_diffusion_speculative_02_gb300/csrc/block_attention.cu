@@ -436,7 +436,11 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
 }
 
 // Merge the split partials by log-sum-exp: one warp per output row (b, i, h).
-__global__ void attn_combine_kernel(const CombineParams p) {
+// Lane s holds split s's (max, sum) and weight, broadcast by shuffles; the
+// O loads of consecutive splits are independent, so they overlap in flight.
+constexpr int kMaxSplits = 64;
+
+__global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p) {
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -451,26 +455,40 @@ __global__ void attn_combine_kernel(const CombineParams p) {
   const int g = h / p.group, w = h - g * p.group;
   const int rr = w * kBlock + i;
   const size_t unit0 = (static_cast<size_t>(b) * p.n_kv_heads + g) * p.splits;
-  float M = -INFINITY;
-  for (int s = lane; s < p.splits; s += 32)
-    M = fmaxf(M, p.part_ml[((unit0 + s) * p.rows + rr) * 2]);
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int s = lane + 32 * j;
+    if (s < p.splits) {
+      const float2 ml =
+          *reinterpret_cast<const float2*>(p.part_ml + ((unit0 + s) * p.rows + rr) * 2);
+      m[j] = ml.x;
+      l[j] = ml.y;
+    }
+  }
+  float M = fmaxf(m[0], m[1]);
 #pragma unroll
   for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float wgt[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) wgt[j] = m[j] == -INFINITY ? 0.f : exp2f(m[j] - M);
+  float lsum = wgt[0] * l[0] + wgt[1] * l[1];
+#pragma unroll
+  for (int off = 16; off; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
   const int D = p.head_dim;
   const int per = D / 32;  // 2 or 4 elements per lane
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float lsum = 0.f;
+  const float* base = p.part_o + (unit0 * p.rows + rr) * D + lane * per;
+  const size_t stride = static_cast<size_t>(p.rows) * D;
+#pragma unroll 8
   for (int s = 0; s < p.splits; ++s) {
-    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + ((unit0 + s) * p.rows + rr) * 2);
-    const float wgt = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-    lsum += wgt * ml.y;
-    const float* src = p.part_o + ((unit0 + s) * p.rows + rr) * D + lane * per;
+    const float ws = __shfl_sync(0xffffffffu, wgt[s >> 5], s & 31);
     if (per == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src);
-      acc[0] += wgt * v.x; acc[1] += wgt * v.y; acc[2] += wgt * v.z; acc[3] += wgt * v.w;
+      const float4 v = *reinterpret_cast<const float4*>(base + s * stride);
+      acc[0] += ws * v.x; acc[1] += ws * v.y; acc[2] += ws * v.z; acc[3] += ws * v.w;
     } else {
-      const float2 v = *reinterpret_cast<const float2*>(src);
-      acc[0] += wgt * v.x; acc[1] += wgt * v.y;
+      const float2 v = *reinterpret_cast<const float2*>(base + s * stride);
+      acc[0] += ws * v.x; acc[1] += ws * v.y;
     }
   }
   const float inv = 1.f / lsum;

@@ -6,21 +6,21 @@
 // projected from them.  "dflash-mlx" (dpshk.com) 块扩散草稿 step 3: the
 // drafter reads the target's multi-layer hidden states.
 //
-// Pipeline of four kernels on one stream:
-//  1. fc GEMM   Y_part[s] = X[:, k-split s] W_fc[:, k-split s]^T   (split-K)
-//     X is never materialised: the k-loop reads layer floor(k / H) through its
-//     own tensor map, which is the concatenation.
-//  2. reduce    Y = sum_s Y_part[s] (fp32), Y^ = RMSNorm(Y) * g_h, stored as a
-//     bf16 pair hi + lo (Y^ ~= hi + lo to ~2^-17) so that the next GEMM does not
-//     lose the fp32 precision of Y^; also snapshots the write positions,
-//     reserves pages of a paged cache and sets seq_len = pos + 16.
-//  3. kv GEMM   [K;V]_part[s] = [hi;lo] W_{k|v}^T                (split-K)
-//  4. finish    sum splits and hi+lo, per-head RMSNorm of K, RoPE at the row
-//     positions, bf16 store into the cache rows.
-// Both GEMMs are "swap-AB" on the 5th-generation tensor cores: 128 output
-// features are the MMA's M, the token rows its N, accumulators in TMEM, the
-// weight stream staged by a TMA pipeline; they are memory-bound at small
-// batch, so the grid is split along K until every SM streams weights.
+// Two kernels on one stream, both "swap-AB" split-K GEMMs on the
+// 5th-generation tensor cores (128 output features are the MMA's M, the token
+// rows its N, fp32 accumulators in TMEM, the weight stream staged by a TMA
+// pipeline; memory-bound at small batch, so K is split until every SM streams
+// weights).  The last split CTA of each output tile (atomic ticket, no
+// waiting) reduces the split partials in split order and finishes the tile:
+//  1. fc GEMM   Y = X W_fc^T.  X is never materialised: the k-loop reads
+//     layer floor(k / H) through its own tensor map, which is the
+//     concatenation.  Finisher: g_h * Y stored as a bf16 pair hi + lo
+//     (exact to ~2^-17, so the next GEMM keeps Y's fp32 precision) and the
+//     tile's partial sums of Y^2.  CTA 0 also snapshots the write positions,
+//     maps the pages the block needs and sets seq_len = pos + 16.
+//  2. K/V GEMM  [K;V] = [hi;lo] W_{k|v}^T.  Finisher: the RMSNorm scale of Y
+//     (one factor per token row, so it commutes with the GEMM), per-head
+//     RMSNorm and RoPE for K, bf16 store into the cache rows.
 #include "common.cuh"
 #include "host.h"
 
@@ -37,6 +37,7 @@ struct LayerMaps {
 };
 
 struct GemmParams {
+  int mode;          // kModeFc or kModeKv (selects the finisher)
   int k_tiles;       // K / 64
   int splits;
   int out_tiles;     // output features / 128
@@ -46,12 +47,171 @@ struct GemmParams {
   int chunk_rows;    // token rows per chunk (B box rows)
   int n_chunks;
   int hilo;          // 1: B = [hi rows ; lo rows] of a 2*n_tok-row matrix, summed in the epilogue
-  int ld_out;        // features per output row
+  int ld_out;        // features per partial row
   int mma_n;         // MMA N = chunk_rows * (1 + hilo)
   int n_stages, stage_bytes, tmem_cols;
   float* part;       // [splits][n_tok][ld_out]
+  uint32_t* tickets; // [out_tiles * n_chunks], zero between calls
   uint32_t* status;
+  // shared by both finishers
+  int hidden, fc_out_tiles;
+  float rms_eps;
+  const uint16_t* hidden_norm_w;  // [H] or null
+  uint16_t* yhat;                 // [2][n_tok][H]: hi, lo of g_h * Y
+  float* ss;                      // [fc_out_tiles][n_tok]: partial sums of Y^2
+  // fc kernel, CTA 0: write positions, page reservation, lengths
+  int batch;
+  const int32_t* write_pos;
+  int32_t* pos_snapshot;
+  dflash_kv_view cache;
+  // kv finisher
+  int n_kv_heads, head_dim;
+  const uint16_t* k_norm_w;       // [D] or null
+  RopeTable rope;
 };
+
+constexpr int kModeFc = 0;
+constexpr int kModeKv = 1;
+
+// Per sequence: snapshot the write position, map the pages that rows
+// pos..pos+15 need (popping the free list), and set seq_len = pos + 16.
+__device__ void reserve_block_rows(const GemmParams& p, int b) {
+  const int pos = p.write_pos[b];
+  p.pos_snapshot[b] = pos;
+  const dflash_kv_view& v = p.cache;
+  const int limit = v.page_table ? v.max_pages * v.page_size : v.capacity;
+  if (pos < 0 || pos + kBlock > limit) {
+    set_status(p.status, DFLASH_ST_CAPACITY);
+    return;
+  }
+  if (v.page_table) {
+    int32_t* tbl = v.page_table + static_cast<size_t>(b) * v.max_pages;
+    for (int pg = pos / v.page_size; pg <= (pos + kBlock - 1) / v.page_size; ++pg) {
+      if (tbl[pg] >= 0) continue;
+      const int slot = atomicSub(v.free_count, 1) - 1;
+      if (slot < 0) {
+        atomicAdd(v.free_count, 1);
+        set_status(p.status, DFLASH_ST_POOL_EMPTY);
+        break;
+      }
+      tbl[pg] = v.free_list[slot];
+    }
+  }
+  v.seq_len[b] = pos + kBlock;
+}
+
+// Sum of the split partials of feature f for token row tok, in split order.
+__device__ __forceinline__ float sum_splits(const GemmParams& p, int tok, int f) {
+  const float* src = p.part + static_cast<size_t>(tok) * p.ld_out + f;
+  const size_t stride = static_cast<size_t>(p.n_tok) * p.ld_out;
+  float y = 0.f;
+#pragma unroll 8
+  for (int s = 0; s < p.splits; ++s) y += src[s * stride];
+  return y;
+}
+
+// fc finisher (last split CTA of an output tile): Y = sum of the splits;
+// hi/lo bf16 pair of g_h * Y for the next GEMM; partial sums of Y^2 over this
+// tile's 128 features (the RMSNorm scale itself is applied after the K/V GEMM,
+// since it is one factor per token row).
+__device__ void finish_fc(const GemmParams& p, int o, int c, float* red) {
+  const int et = threadIdx.x - 64, warp = et >> 5, lane = et & 31;
+  const int f = o * 128 + et;
+  const float g = p.hidden_norm_w ? bf16_bits_to_float(p.hidden_norm_w[f]) : 1.f;
+  const int t0 = c * p.chunk_rows;
+  const int nt = min(p.chunk_rows, p.n_tok - t0);
+  for (int j = 0; j < nt; ++j) {
+    const int tok = t0 + j;
+    const float y = sum_splits(p, tok, f);
+    const float gy = y * g;
+    const uint16_t hi = float_to_bf16_bits(gy);
+    p.yhat[static_cast<size_t>(tok) * p.hidden + f] = hi;
+    p.yhat[(static_cast<size_t>(p.n_tok) + tok) * p.hidden + f] =
+        float_to_bf16_bits(gy - bf16_bits_to_float(hi));
+    float sq = y * y;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+    if (lane == 0) red[warp * 256 + j] = sq;
+  }
+  named_bar_sync(1, 128);
+  for (int j = et; j < nt; j += 128)
+    p.ss[static_cast<size_t>(o) * p.n_tok + t0 + j] =
+        red[j] + red[256 + j] + red[512 + j] + red[768 + j];
+}
+
+// kv finisher (last split CTA of an output tile): K or V rows of 128 features
+// (one or two heads) for every token of the chunk: sum of the splits, the
+// RMSNorm scale of Y, per-head RMSNorm and RoPE for K, bf16 store into the
+// cache row write_pos + t.
+__device__ void finish_kv(const GemmParams& p, int o, int c, float* smem_f) {
+  const int et = threadIdx.x - 64, warp = et >> 5, lane = et & 31;
+  const int D = p.head_dim;
+  const bool is_k = o < p.a_split;
+  const int feat = (is_k ? o : o - p.a_split) * 128 + et;  // within Hkv * D
+  const int head = feat / D, d = feat - head * D;
+  const int t0 = c * p.chunk_rows;
+  const int nt = min(p.chunk_rows, p.n_tok - t0);
+  float* rbuf = smem_f;            // [256] per-token RMSNorm scale of Y
+  float* red = smem_f + 256;       // [4] per-warp sums
+  float* kbuf = smem_f + 264;      // [128] values for the RoPE partner exchange
+  for (int j = et; j < nt; j += 128) {
+    float r = 1.f;
+    if (p.hidden_norm_w) {
+      float tot = 0.f;
+      for (int q = 0; q < p.fc_out_tiles; ++q) tot += p.ss[static_cast<size_t>(q) * p.n_tok + t0 + j];
+      r = rsqrtf(tot / p.hidden + p.rms_eps);
+    }
+    rbuf[j] = r;
+  }
+  named_bar_sync(1, 128);
+  const float gk = (is_k && p.k_norm_w) ? bf16_bits_to_float(p.k_norm_w[d]) : 1.f;
+  const int half = D / 2;
+  const int fi = d < half ? d : d - half;
+  const dflash_kv_view& cv = p.cache;
+  const int limit = cv.page_table ? cv.max_pages * cv.page_size : cv.capacity;
+  uint16_t* dst_base = static_cast<uint16_t*>(is_k ? cv.k : cv.v);
+  for (int j = 0; j < nt; ++j) {
+    const int tok = t0 + j;
+    float val = sum_splits(p, tok, o * 128 + et) * rbuf[j];
+    if (is_k) {
+      if (p.k_norm_w) {
+        float sq = val * val;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        if (lane == 0) red[warp] = sq;
+        named_bar_sync(1, 128);
+        const float tot = D == 128 ? red[0] + red[1] + red[2] + red[3]
+                                   : red[(warp >> 1) * 2] + red[(warp >> 1) * 2 + 1];
+        val = val * rsqrtf(tot / D + p.rms_eps) * gk;
+      }
+      kbuf[et] = val;
+      named_bar_sync(1, 128);
+      const int b = tok / kBlock, t = tok - (tok / kBlock) * kBlock;
+      const int pos = p.pos_snapshot[b] + t;
+      float sn, cs;
+      sincosf(rope_angle(pos, p.rope.hi[fi], p.rope.lo[fi]), &sn, &cs);
+      const float partner = d < half ? kbuf[et + half] : kbuf[et - half];
+      val = d < half ? val * cs - partner * sn : val * cs + partner * sn;
+      named_bar_sync(1, 128);  // kbuf and red are reused by the next token
+    }
+    const int b = tok / kBlock, t = tok - b * kBlock;
+    const int pos0 = p.pos_snapshot[b];
+    if (pos0 < 0 || pos0 + kBlock > limit) continue;  // flagged by the reservation
+    const int pos = pos0 + t;
+    size_t row;
+    if (cv.page_table) {
+      const int page = cv.page_table[static_cast<size_t>(b) * cv.max_pages + pos / cv.page_size];
+      if (page < 0) {
+        if (et == 0) set_status(p.status, DFLASH_ST_PAGE_MISSING);
+        continue;
+      }
+      row = static_cast<size_t>(page) * cv.page_size + pos % cv.page_size;
+    } else {
+      row = static_cast<size_t>(b) * cv.capacity + pos;
+    }
+    dst_base[(row * p.n_kv_heads + head) * D + d] = float_to_bf16_bits(val);
+  }
+}
 
 __global__ void __launch_bounds__(kGemmThreads)
 splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
@@ -65,6 +225,7 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
   uint64_t* tfull = empty + p.n_stages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   int unit = blockIdx.x;
   const int o = unit % p.out_tiles;
@@ -81,6 +242,7 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
     }
     mbar_init(tfull, 1);
     *abort_flag = 0;
+    *last_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -152,6 +314,9 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
       mbar_wait_drain(tfull, 0, p.status);
     }
   } else {
+    if (p.mode == kModeFc && blockIdx.x == 0) {
+      for (int b = threadIdx.x - 64; b < p.batch; b += 128) reserve_block_rows(p, b);
+    }
     // epilogue: TMEM lane = output feature, column = token (hi, then lo)
     const int q = warp & 3;
     const bool ok = mbar_wait(tfull, 0, abort_flag, p.status);
@@ -177,150 +342,26 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
     }
   }
   __syncthreads();
-  griddep_launch_dependents();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, p.tmem_cols);
   }
-}
-
-// ---------------------------------------------------------------------------
-struct ReduceParams {
-  int n_tok, hidden, splits, batch;
-  float rms_eps;
-  const float* part;            // [splits][n_tok][hidden]
-  const uint16_t* norm_w;       // [hidden] or null
-  uint16_t* yhat;               // [2][n_tok][hidden]  (hi, lo)
-  const int32_t* write_pos;     // [batch]
-  int32_t* pos_snapshot;        // [batch]
-  dflash_kv_view cache;
-  uint32_t* status;
-};
-
-__global__ void __launch_bounds__(256) fc_reduce_norm_kernel(const ReduceParams p) {
-  griddep_wait();
-  const int row = blockIdx.x;
-  __shared__ float red[8];
-  if (row == 0) {
-    // bookkeeping, one thread per sequence: positions, page reservation, length
-    for (int b = threadIdx.x; b < p.batch; b += blockDim.x) {
-      const int pos = p.write_pos[b];
-      p.pos_snapshot[b] = pos;
-      const dflash_kv_view& v = p.cache;
-      const int limit = v.page_table ? v.max_pages * v.page_size : v.capacity;
-      if (pos < 0 || pos + kBlock > limit) {
-        set_status(p.status, DFLASH_ST_CAPACITY);
-        continue;
-      }
-      if (v.page_table) {
-        int32_t* tbl = v.page_table + static_cast<size_t>(b) * v.max_pages;
-        for (int pg = pos / v.page_size; pg <= (pos + kBlock - 1) / v.page_size; ++pg) {
-          if (tbl[pg] >= 0) continue;
-          const int slot = atomicSub(v.free_count, 1) - 1;
-          if (slot < 0) {
-            atomicAdd(v.free_count, 1);
-            set_status(p.status, DFLASH_ST_POOL_EMPTY);
-            break;
-          }
-          tbl[pg] = v.free_list[slot];
-        }
-      }
-      v.seq_len[b] = pos + kBlock;
+  if (warp >= 2) {
+    // the last split CTA of (output tile, token chunk) reduces and finishes it
+    __threadfence();
+    named_bar_sync(1, 128);
+    uint32_t* ticket = p.tickets + o * p.n_chunks + c;
+    if (threadIdx.x == 64) *last_flag = (atomicAdd(ticket, 1u) == static_cast<uint32_t>(p.splits - 1));
+    named_bar_sync(1, 128);
+    if (*last_flag) {
+      __threadfence();
+      // the pipeline is drained: its shared memory is free for the finisher
+      float* scratch = reinterpret_cast<float*>(smem);
+      if (p.mode == kModeFc) finish_fc(p, o, c, scratch); else finish_kv(p, o, c, scratch);
+      if (threadIdx.x == 64) *ticket = 0u;
     }
   }
-  const int H = p.hidden;
-  float ss = 0.f;
-  for (int f = threadIdx.x; f < H; f += blockDim.x) {
-    float y = 0.f;
-    for (int s = 0; s < p.splits; ++s) y += p.part[(static_cast<size_t>(s) * p.n_tok + row) * H + f];
-    ss += y * y;
-  }
-  float rs = 1.f;
-  if (p.norm_w) {
-#pragma unroll
-    for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
-    __syncthreads();
-    float tot = 0.f;
-    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) tot += red[i];
-    rs = rsqrtf(tot / H + p.rms_eps);
-  }
-  uint16_t* hi = p.yhat + static_cast<size_t>(row) * H;
-  uint16_t* lo = p.yhat + (static_cast<size_t>(p.n_tok) + row) * H;
-  for (int f = threadIdx.x; f < H; f += blockDim.x) {
-    float y = 0.f;
-    for (int s = 0; s < p.splits; ++s) y += p.part[(static_cast<size_t>(s) * p.n_tok + row) * H + f];
-    if (p.norm_w) y = y * rs * bf16_bits_to_float(p.norm_w[f]);
-    const uint16_t h = float_to_bf16_bits(y);
-    hi[f] = h;
-    lo[f] = float_to_bf16_bits(y - bf16_bits_to_float(h));
-  }
   griddep_launch_dependents();
-}
-
-// ---------------------------------------------------------------------------
-struct FinishParams {
-  int n_tok, n_kv_heads, head_dim, splits, ld;   // ld = 2 * Hkv * D
-  float rms_eps;
-  const float* part;          // [splits][n_tok][ld]: K features then V features
-  const uint16_t* k_norm_w;   // [D] or null
-  const int32_t* pos_snapshot;
-  dflash_kv_view cache;
-  uint32_t* status;
-  RopeTable rope;
-};
-
-// One CTA per (token row, KV head); thread d owns feature d of the head.
-__global__ void __launch_bounds__(128) kv_finish_kernel(const FinishParams p) {
-  griddep_wait();
-  const int row = blockIdx.x, g = blockIdx.y, d = threadIdx.x;
-  const int D = p.head_dim;
-  const int b = row / kBlock, t = row - b * kBlock;
-  __shared__ float kbuf[128];
-  __shared__ float red[4];
-  float k = 0.f, v = 0.f;
-  for (int s = 0; s < p.splits; ++s) {
-    const float* src = p.part + (static_cast<size_t>(s) * p.n_tok + row) * p.ld;
-    k += src[g * D + d];
-    v += src[p.n_kv_heads * D + g * D + d];
-  }
-  if (p.k_norm_w) {
-    float ss = k * k;
-#pragma unroll
-    for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-    if ((d & 31) == 0) red[d >> 5] = ss;
-    __syncthreads();
-    float tot = 0.f;
-    for (int i = 0; i < D / 32; ++i) tot += red[i];
-    k = k * rsqrtf(tot / D + p.rms_eps) * bf16_bits_to_float(p.k_norm_w[d]);
-  }
-  kbuf[d] = k;
-  __syncthreads();
-  const int pos = p.pos_snapshot[b] + t;
-  const int half = D / 2;
-  const int fi = d < half ? d : d - half;
-  float sn, cs;
-  sincosf(rope_angle(pos, p.rope.hi[fi], p.rope.lo[fi]), &sn, &cs);
-  const float kr = d < half ? k * cs - kbuf[d + half] * sn : k * cs + kbuf[d - half] * sn;
-  griddep_launch_dependents();
-
-  const dflash_kv_view& c = p.cache;
-  const int limit = c.page_table ? c.max_pages * c.page_size : c.capacity;
-  if (p.pos_snapshot[b] < 0 || p.pos_snapshot[b] + kBlock > limit) return;  // flagged earlier
-  size_t rowidx;
-  if (c.page_table) {
-    const int page = c.page_table[static_cast<size_t>(b) * c.max_pages + pos / c.page_size];
-    if (page < 0) {
-      if (d == 0) set_status(p.status, DFLASH_ST_PAGE_MISSING);
-      return;
-    }
-    rowidx = static_cast<size_t>(page) * c.page_size + pos % c.page_size;
-  } else {
-    rowidx = static_cast<size_t>(b) * c.capacity + pos;
-  }
-  const size_t off = (rowidx * p.n_kv_heads + g) * D + d;
-  static_cast<uint16_t*>(c.k)[off] = float_to_bf16_bits(kr);
-  static_cast<uint16_t*>(c.v)[off] = float_to_bf16_bits(v);
 }
 
 int gemm_smem(int stage_bytes, int n_stages) {
@@ -380,9 +421,28 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
   float* part_kv = ws_at<float>(ws, plan.off_kv);
   int32_t* pos_snap = ws_at<int32_t>(ws, plan.off_pos);
 
-  // ---- 1. fc GEMM ----
+  GemmParams common = {};
+  common.status = status;
+  common.hidden = H;
+  common.fc_out_tiles = plan.fc_out_tiles;
+  common.rms_eps = dims->rms_eps;
+  common.hidden_norm_w = static_cast<const uint16_t*>(hidden_norm_w);
+  common.yhat = yhat;
+  common.ss = ws_at<float>(ws, plan.off_ss);
+  common.batch = dims->batch;
+  common.write_pos = write_pos;
+  common.pos_snapshot = pos_snap;
+  common.cache = *cache;
+  common.n_kv_heads = dims->n_kv_heads;
+  common.head_dim = dims->head_dim;
+  common.k_norm_w = static_cast<const uint16_t*>(k_norm_w);
+  fill_rope_table(common.rope.hi, common.rope.lo, dims->head_dim, dims->rope_theta);
+  uint32_t* tickets = ws_at<uint32_t>(ws, plan.off_ctx_tickets);
+
+  // ---- 1. fc GEMM; its finisher writes hi/lo of g_h * Y and sums of Y^2 ----
   {
-    GemmParams g = {};
+    GemmParams g = common;
+    g.mode = kModeFc;
     g.k_tiles = plan.fc_k_tiles;
     g.splits = plan.fc_splits;
     g.out_tiles = plan.fc_out_tiles;
@@ -395,7 +455,7 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
     g.ld_out = H;
     g.mma_n = g.chunk_rows;
     g.part = part_fc;
-    g.status = status;
+    g.tickets = tickets;
     const int smem = setup_gemm(g, g.chunk_rows);
     CUtensorMap ta;
     if ((rc = make_tmap_2d_bf16(&ta, w_fc, static_cast<uint64_t>(nL) * H, H,
@@ -412,26 +472,10 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
     if ((rc = launch(splitk_gemm_kernel, dim3(grid), dim3(kGemmThreads), smem, st, ta, ta, lm, g)))
       return rc;
   }
-  // ---- 2. reduce + RMSNorm + hi/lo split; positions and pages ----
+  // ---- 2. K/V GEMM on [hi; lo]; its finisher scales, normalises, rotates, stores ----
   {
-    ReduceParams r = {};
-    r.n_tok = ntok;
-    r.hidden = H;
-    r.splits = plan.fc_splits;
-    r.batch = dims->batch;
-    r.rms_eps = dims->rms_eps;
-    r.part = part_fc;
-    r.norm_w = static_cast<const uint16_t*>(hidden_norm_w);
-    r.yhat = yhat;
-    r.write_pos = write_pos;
-    r.pos_snapshot = pos_snap;
-    r.cache = *cache;
-    r.status = status;
-    if ((rc = launch(fc_reduce_norm_kernel, dim3(ntok), dim3(256), 0, st, r))) return rc;
-  }
-  // ---- 3. kv GEMM on [hi; lo] ----
-  {
-    GemmParams g = {};
+    GemmParams g = common;
+    g.mode = kModeKv;
     g.k_tiles = plan.kv_k_tiles;
     g.splits = plan.kv_splits;
     g.out_tiles = plan.kv_out_tiles;
@@ -444,7 +488,7 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
     g.ld_out = 2 * kvd;
     g.mma_n = 2 * g.chunk_rows;
     g.part = part_kv;
-    g.status = status;
+    g.tickets = tickets + plan.fc_out_tiles * plan.fc_tok_chunks;
     const int smem = setup_gemm(g, 2 * g.chunk_rows);
     CUtensorMap tk, tv;
     if ((rc = make_tmap_2d_bf16(&tk, w_k, H, kvd, static_cast<uint64_t>(H) * 2, 64, 128)))
@@ -459,25 +503,6 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
     if ((rc = set_smem_limit(reinterpret_cast<const void*>(splitk_gemm_kernel), smem))) return rc;
     const int grid = g.out_tiles * g.splits * g.n_chunks;
     if ((rc = launch(splitk_gemm_kernel, dim3(grid), dim3(kGemmThreads), smem, st, tk, tv, lm, g)))
-      return rc;
-  }
-  // ---- 4. finish: reduce, k_norm, RoPE, store ----
-  {
-    FinishParams f = {};
-    f.n_tok = ntok;
-    f.n_kv_heads = dims->n_kv_heads;
-    f.head_dim = dims->head_dim;
-    f.splits = plan.kv_splits;
-    f.ld = 2 * kvd;
-    f.rms_eps = dims->rms_eps;
-    f.part = part_kv;
-    f.k_norm_w = static_cast<const uint16_t*>(k_norm_w);
-    f.pos_snapshot = pos_snap;
-    f.cache = *cache;
-    f.status = status;
-    fill_rope_table(f.rope.hi, f.rope.lo, dims->head_dim, dims->rope_theta);
-    if ((rc = launch(kv_finish_kernel, dim3(ntok, dims->n_kv_heads), dim3(dims->head_dim), 0, st,
-                     f)))
       return rc;
   }
   return DFLASH_OK;

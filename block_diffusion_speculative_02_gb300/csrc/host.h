@@ -36,8 +36,8 @@ struct Plan {
   int att_rows;         // (Hq / Hkv) * 16 query rows per KV head
   int att_splits;
   // workspace offsets (bytes)
-  size_t off_status, off_tickets, off_keys, off_pos, off_fc, off_yhat, off_kv, off_att_o,
-      off_att_ml, total;
+  size_t off_status, off_tickets, off_keys, off_pos, off_ctx_tickets, off_ss, off_fc, off_yhat,
+      off_kv, off_att_o, off_att_ml, total;
 };
 
 int check_dims(const dflash_dims* d);

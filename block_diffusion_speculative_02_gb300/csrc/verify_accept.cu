@@ -34,10 +34,16 @@ constexpr int kATileBytes = kTileRows * 128;
 constexpr int kUnitRows = 8;             // balancing granule = one 8-row TMA box
 constexpr int kSmemBudget = 224 * 1024;
 constexpr int kMaxStages = 12;
+#ifndef DFLASH_LM_CHUNKS_PER_STAGE
+#define DFLASH_LM_CHUNKS_PER_STAGE 2
+#endif
+constexpr int kLmChunksPerStage = DFLASH_LM_CHUNKS_PER_STAGE;  // power of two
 
 struct LmParams {
   int vocab, hidden, ntok;
-  int ntok_box, n_xbox;                  // token rows per X box, X boxes per stage
+  int ntok_box, n_xbox;                  // token rows per X box, X boxes per 64-col chunk
+  int kb;                                // 64-column K chunks per pipeline stage
+  int x_chunk;                           // bytes of the token tile of one chunk
   int n_units;                           // ceil(vocab / 8)
   int n_stages, stage_bytes;
   int n_acc, tmem_cols;
@@ -119,7 +125,8 @@ lmhead_argmax_accept_kernel(const __grid_constant__ CUtensorMap tm_w,
   const int r0 = u0 * kUnitRows;
   const int r1 = min(u1 * kUnitRows, p.vocab);
   const int n_tiles = (r1 - r0 + kTileRows - 1) / kTileRows;
-  const int k_steps = p.hidden / 64;
+  const int k_stages = p.hidden / 64 / p.kb;
+  const int a_stage = p.kb * kATileBytes;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.n_stages; ++s) {
@@ -156,7 +163,11 @@ lmhead_argmax_accept_kernel(const __grid_constant__ CUtensorMap tm_w,
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
+#ifdef DFLASH_LM_W_EVICT_NORMAL
+      const uint64_t pol_w = l2_policy_evict_normal();
+#else
       const uint64_t pol_w = l2_policy_evict_first();
+#endif
       const uint64_t pol_x = l2_policy_evict_last();
       const uint32_t x_bytes = static_cast<uint32_t>(p.n_xbox * p.ntok_box * 128);
       uint32_t stage = 0, phase = 0;
@@ -167,24 +178,30 @@ lmhead_argmax_accept_kernel(const __grid_constant__ CUtensorMap tm_w,
         const int rows = min(kTileRows, r1 - row0);
         const int nb8 = (rows + kUnitRows - 1) / kUnitRows;
         const uint32_t a_bytes = rows == kTileRows ? kATileBytes : nb8 * 1024;
-        for (int kt = 0; kt < k_steps; ++kt) {
+        for (int ks = 0; ks < k_stages; ++ks) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
             ok = false;
             break;
           }
           uint8_t* a = smem + stage * p.stage_bytes;
-          uint8_t* b = a + kATileBytes;
-          mbar_arrive_expect_tx(&full[stage], a_bytes + x_bytes);
-          if (rows == kTileRows) {
-            tma_load_2d(a, &tm_w, &full[stage], kt * 64, row0, pol_w);
-          } else {
-            for (int j = 0; j < nb8; ++j)
-              tma_load_2d(a + 1024 * j, &tm_w8, &full[stage], kt * 64, row0 + kUnitRows * j,
-                          pol_w);
+          uint8_t* b = a + a_stage;
+          mbar_arrive_expect_tx(&full[stage], p.kb * (a_bytes + x_bytes));
+          // the kb chunks of one stage are issued back to back, so every
+          // vocabulary row is requested as kb*128 contiguous bytes at once
+          for (int j = 0; j < p.kb; ++j) {
+            const int kcol = (ks * p.kb + j) * 64;
+            uint8_t* aj = a + j * kATileBytes;
+            if (rows == kTileRows) {
+              tma_load_2d(aj, &tm_w, &full[stage], kcol, row0, pol_w);
+            } else {
+              for (int i = 0; i < nb8; ++i)
+                tma_load_2d(aj + 1024 * i, &tm_w8, &full[stage], kcol, row0 + kUnitRows * i,
+                            pol_w);
+            }
+            for (int c = 0; c < p.n_xbox; ++c)
+              tma_load_2d(b + j * p.x_chunk + c * p.ntok_box * 128, &tm_x, &full[stage], kcol,
+                          c * p.ntok_box, pol_x);
           }
-          for (int c = 0; c < p.n_xbox; ++c)
-            tma_load_2d(b + c * p.ntok_box * 128, &tm_x, &full[stage], kt * 64, c * p.ntok_box,
-                        pol_x);
           ++issued;
           if (++stage == static_cast<uint32_t>(p.n_stages)) {
             stage = 0;
@@ -212,22 +229,24 @@ lmhead_argmax_accept_kernel(const __grid_constant__ CUtensorMap tm_w,
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
         const uint32_t d_base = tmem_base + static_cast<uint32_t>(acc * p.ntok);
-        for (int kt = 0; kt < k_steps; ++kt) {
+        for (int ks = 0; ks < k_stages; ++ks) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_addr = smem_base + stage * p.stage_bytes;
-          const uint32_t b_addr = a_addr + kATileBytes;
-          const uint64_t adesc = umma_sdesc_sw128(a_addr);
+          const uint32_t b_addr = a_addr + a_stage;
+          for (int j = 0; j < p.kb; ++j) {
+            const uint64_t adesc = umma_sdesc_sw128(a_addr + j * kATileBytes);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            for (int c = 0; c * 256 < p.ntok; ++c) {
-              const int n = min(256, p.ntok - c * 256);
-              const uint64_t bdesc = umma_sdesc_sw128(b_addr + c * 256 * 128);
-              umma_bf16(d_base + c * 256, adesc + 2 * kk, bdesc + 2 * kk,
-                        umma_idesc_bf16(kTileRows, n), (kt | kk) != 0);
+            for (int kk = 0; kk < 4; ++kk) {
+              for (int c = 0; c * 256 < p.ntok; ++c) {
+                const int n = min(256, p.ntok - c * 256);
+                const uint64_t bdesc = umma_sdesc_sw128(b_addr + j * p.x_chunk + c * 256 * 128);
+                umma_bf16(d_base + c * 256, adesc + 2 * kk, bdesc + 2 * kk,
+                          umma_idesc_bf16(kTileRows, n), (ks | j | kk) != 0);
+              }
             }
           }
           umma_commit(&empty[stage]);
@@ -331,9 +350,14 @@ extern "C" int dflash_verify_accept(const dflash_dims* dims, const void* hidden,
   p.ntok_box = p.ntok <= 256 ? p.ntok : 256;
   p.n_xbox = (p.ntok + p.ntok_box - 1) / p.ntok_box;
   p.n_units = (p.vocab + kUnitRows - 1) / kUnitRows;
-  const int x_bytes = ((p.n_xbox * p.ntok_box * 128) + 1023) / 1024 * 1024;
-  p.stage_bytes = kATileBytes + x_bytes;
+  p.x_chunk = ((p.n_xbox * p.ntok_box * 128) + 1023) / 1024 * 1024;
   const int fixed = 1024 /*alignment slack*/ + 8 * 5 + 16 + 8 * p.ntok + 64;
+  // as many 64-column chunks per stage as divide K and still leave three stages
+  p.kb = kLmChunksPerStage;
+  while (p.kb > 1 && ((p.hidden / 64) % p.kb ||
+                      (kSmemBudget - fixed) / (p.kb * (kATileBytes + p.x_chunk) + 16) < 3))
+    p.kb >>= 1;
+  p.stage_bytes = p.kb * (kATileBytes + p.x_chunk);
   p.n_stages = (kSmemBudget - fixed) / (p.stage_bytes + 16);
   if (p.n_stages > kMaxStages) p.n_stages = kMaxStages;
   if (p.n_stages < 2) return DFLASH_E_UNSUPPORTED;

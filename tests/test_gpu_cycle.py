@@ -10,7 +10,7 @@ import torch
 
 from oracle.dflash_oracle import block_attention as ref_attention
 from oracle.dflash_oracle import ctx_project as ref_project
-from oracle.dflash_oracle import bf16_to_f64, kv_crop_lengths
+from oracle.dflash_oracle import bf16_to_f64, kv_crop_lengths, near_tie_mask
 from oracle.dflash_oracle import verify_accept as ref_verify
 from synthetic import (draw_accept_lengths, make_block_ids, make_paged_layout, normal_bf16,
                        pack_contiguous, scatter_paged, unit_rms_rows_bf16)
@@ -60,7 +60,13 @@ def test_three_cycles_carry_state(paged):
     ref_v = [bf16_to_f64(x) for x in ctx_v]
     L = L0.copy()
     for cyc in range(3):
-        hv = unit_rms_rows_bf16(rng, (B, 16, H))
+        # verify inputs without near ties (the rule would exclude them and the two
+        # sides' states could then diverge in the next cycle)
+        while True:
+            hv = unit_rms_rows_bf16(rng, (B, 16, H))
+            probe = ref_verify(hv, w_lm, np.zeros((B, 16), np.int32), L, out_cap=cap + 16)
+            if not near_tie_mask(probe["gap"], probe["max"]).any():
+                break
         layers = [unit_rms_rows_bf16(rng, (B * 16, H)) for _ in range(nL)]
         q = normal_bf16(rng, (B, 16, Hq, D))
         kb = normal_bf16(rng, (B, 16, Hkv, D))
