@@ -22,6 +22,8 @@
 //
 // Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues the
 // MMAs, warps 2-5 drain the accumulators.
+#include <mutex>
+
 #include "common.cuh"
 #include "host.h"
 
@@ -393,4 +395,123 @@ extern "C" int dflash_verify_accept(const dflash_dims* dims, const void* hidden,
   const int grid = plan.num_sms < p.n_units ? plan.num_sms : p.n_units;
   return launch(lmhead_argmax_accept_kernel, dim3(grid), dim3(kThreads), smem,
                 reinterpret_cast<cudaStream_t>(stream), tm_w, tm_w8, tm_x, p);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of dflash_verify_accept.
+//
+// Some callers cannot hand this library a workspace: a plugin that receives
+// tensors from a host framework owning every device allocation (and gives the
+// plugin no allocator), a process running under a fixed device-memory budget,
+// or code that must not allocate while a stream is being captured.  For them
+// the LM-head/argmax/acceptance kernel's only scratch (one 64-bit argmax key
+// per token row, the finishing ticket and a status word) lives in a
+// library-owned array in device global memory, reserved when the library is
+// loaded and kept by every GPU that loads it until the process exits.
+// ---------------------------------------------------------------------------
+namespace dflash {
+namespace {
+
+constexpr int kNoAllocMaxTokens = 512;   // batch * 16 at most (batch <= 32)
+constexpr size_t kNoAllocKeyBytes = sizeof(unsigned long long) * kNoAllocMaxTokens;
+constexpr size_t kNoAllocBytes = kNoAllocKeyBytes + 256;  // keys, then ticket and status
+
+// Shared by every call on a device; holds the last call's contents.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current).  In host code the array's name is
+// only a host-side stand-in, so kernels must be given this address instead.
+int noalloc_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DFLASH_E_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return DFLASH_E_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return DFLASH_E_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return DFLASH_OK;
+}
+
+}  // namespace
+}  // namespace dflash
+
+extern "C" int dflash_verify_accept_noalloc(const dflash_dims* dims, const void* hidden,
+                                            const void* w_lm, const int32_t* block_ids,
+                                            const int32_t* len_before, int32_t* posterior,
+                                            int32_t* accept_len, int32_t* next_staged,
+                                            int32_t* commit_len, int32_t* out_tokens,
+                                            int32_t out_cap, dflash_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (dims->batch * kBlock > kNoAllocMaxTokens) return DFLASH_E_UNSUPPORTED;
+  if (!hidden || !w_lm || !block_ids || !len_before || !posterior || !accept_len ||
+      !next_staged || !commit_len || !out_tokens || out_cap < 1)
+    return DFLASH_E_ARG;
+  if (!aligned16(hidden) || !aligned16(w_lm)) return DFLASH_E_ALIGN;
+  void* scratch = nullptr;
+  if ((rc = noalloc_scratch_address(&scratch))) return rc;
+  Plan plan;
+  if ((rc = make_plan(*dims, &plan))) return rc;
+
+  LmParams p = {};
+  p.vocab = dims->vocab;
+  p.hidden = dims->hidden;
+  p.ntok = plan.ntok;
+  p.ntok_box = p.ntok <= 256 ? p.ntok : 256;
+  p.n_xbox = (p.ntok + p.ntok_box - 1) / p.ntok_box;
+  p.n_units = (p.vocab + kUnitRows - 1) / kUnitRows;
+  p.x_chunk = ((p.n_xbox * p.ntok_box * 128) + 1023) / 1024 * 1024;
+  const int fixed = 1024 + 8 * 5 + 16 + 8 * p.ntok + 64;
+  p.kb = kLmChunksPerStage;
+  while (p.kb > 1 && ((p.hidden / 64) % p.kb ||
+                      (kSmemBudget - fixed) / (p.kb * (kATileBytes + p.x_chunk) + 16) < 3))
+    p.kb >>= 1;
+  p.stage_bytes = p.kb * (kATileBytes + p.x_chunk);
+  p.n_stages = (kSmemBudget - fixed) / (p.stage_bytes + 16);
+  if (p.n_stages > kMaxStages) p.n_stages = kMaxStages;
+  if (p.n_stages < 2) return DFLASH_E_UNSUPPORTED;
+  p.n_acc = (2 * p.ntok <= 512) ? 2 : 1;
+  int cols = 32;
+  while (cols < p.n_acc * p.ntok) cols *= 2;
+  p.tmem_cols = cols;
+  char* base = static_cast<char*>(scratch);
+  p.keys = reinterpret_cast<unsigned long long*>(base);
+  p.ticket = reinterpret_cast<uint32_t*>(base + kNoAllocKeyBytes);
+  p.status = reinterpret_cast<uint32_t*>(base + kNoAllocKeyBytes + 4);
+  p.batch = dims->batch;
+  p.block_ids = block_ids;
+  p.len_before = len_before;
+  p.posterior = posterior;
+  p.accept_len = accept_len;
+  p.next_staged = next_staged;
+  p.commit_len = commit_len;
+  p.out_tokens = out_tokens;
+  p.out_cap = out_cap;
+
+  CUtensorMap tm_w, tm_w8, tm_x;
+  const uint64_t pitch = static_cast<uint64_t>(dims->hidden) * 2;
+  if ((rc = make_tmap_2d_bf16(&tm_w, w_lm, dims->hidden, dims->vocab, pitch, 64, kTileRows)))
+    return rc;
+  if ((rc = make_tmap_2d_bf16(&tm_w8, w_lm, dims->hidden, dims->vocab, pitch, 64, kUnitRows)))
+    return rc;
+  if ((rc = make_tmap_2d_bf16(&tm_x, hidden, dims->hidden, p.ntok, pitch, 64, p.ntok_box)))
+    return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the keys and the ticket must start at zero; the status word is cleared too
+  if ((rc = cuda_err(cudaMemsetAsync(scratch, 0, kNoAllocKeyBytes + 8, st)))) return rc;
+  const int smem = p.n_stages * (p.stage_bytes + 16) + fixed;
+  if ((rc = set_smem_limit(reinterpret_cast<const void*>(lmhead_argmax_accept_kernel), smem)))
+    return rc;
+  const int grid = plan.num_sms < p.n_units ? plan.num_sms : p.n_units;
+  return launch(lmhead_argmax_accept_kernel, dim3(grid), dim3(kThreads), smem, st, tm_w, tm_w8,
+                tm_x, p);
 }

@@ -31,7 +31,8 @@ STATUS_BITS = {
 
 EXPORTED = ["dflash_workspace_bytes", "dflash_workspace_init", "dflash_ctx_project",
             "dflash_block_attention", "dflash_verify_accept", "dflash_kv_crop",
-            "dflash_read_status", "dflash_status_string", "dflash_version"]
+            "dflash_read_status", "dflash_status_string", "dflash_version",
+            "dflash_verify_accept_noalloc"]
 
 
 class DFlashError(RuntimeError):
@@ -84,6 +85,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_verify_accept.restype = ctypes.c_int
     lib.dflash_verify_accept.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, vp, vp, vp, vp, vp,
                                          vp, i32, vp, sz, vp]
+    lib.dflash_verify_accept_noalloc.restype = ctypes.c_int
+    lib.dflash_verify_accept_noalloc.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, vp, vp, vp, vp,
+                                                 vp, vp, i32, vp]
     lib.dflash_kv_crop.restype = ctypes.c_int
     lib.dflash_kv_crop.argtypes = [ctypes.POINTER(KVViewC), i32, vp, i32, vp, sz, vp]
     lib.dflash_read_status.restype = ctypes.c_int
@@ -204,6 +208,19 @@ def dflash_verify_accept(dims: Dims, hidden, w_lm, block_ids, len_before, poster
         _dev(commit_len, torch.int32, "commit_len"), _dev(out_tokens, torch.int32, "out_tokens"),
         int(out_tokens.shape[-1]), _dev(ws, name="ws"), ws.numel(), _stream(stream)),
         "dflash_verify_accept")
+
+
+def dflash_verify_accept_noalloc(dims: Dims, hidden, w_lm, block_ids, len_before, posterior,
+                                 accept_len, next_staged, commit_len, out_tokens, stream=None):
+    """dflash_verify_accept without a workspace (library-owned static scratch)."""
+    _check(load_library().dflash_verify_accept_noalloc(
+        ctypes.byref(dims), _dev(hidden, torch.bfloat16, "hidden"),
+        _dev(w_lm, torch.bfloat16, "w_lm"), _dev(block_ids, torch.int32, "block_ids"),
+        _dev(len_before, torch.int32, "len_before"), _dev(posterior, torch.int32, "posterior"),
+        _dev(accept_len, torch.int32, "accept_len"),
+        _dev(next_staged, torch.int32, "next_staged"),
+        _dev(commit_len, torch.int32, "commit_len"), _dev(out_tokens, torch.int32, "out_tokens"),
+        int(out_tokens.shape[-1]), _stream(stream)), "dflash_verify_accept_noalloc")
 
 
 def dflash_kv_crop(views: Sequence[KVView], new_len, batch: int, ws, stream=None):

@@ -183,6 +183,35 @@ DFLASH_API int dflash_verify_accept(const dflash_dims* dims, const void* hidden,
                          void* ws, size_t ws_bytes, dflash_stream_t stream);
 
 /*
+ * Allocation-free variant of dflash_verify_accept.  The DFlash pages have no
+ * counterpart to this entry point; it exists for callers that cannot give
+ * the library a workspace: plugins handed tensors by a host framework that
+ * owns every device allocation and offers no allocator, processes held to a
+ * fixed device-memory budget, and code that must not allocate while a stream
+ * is being captured.
+ * Same arguments, results and errors as dflash_verify_accept, minus ws and
+ * ws_bytes.  Its scratch (one 64-bit key per token row, a ticket, a status
+ * word) is a library-owned static device array sized for batch * 16 <= 512
+ * token rows (about 4 KB), held by every GPU that loads the library until the
+ * process exits; larger batches return DFLASH_E_UNSUPPORTED.  It calls no
+ * cudaMalloc/cudaFree and no allocating library routine.  The first call on a
+ * device looks up the array's device address (once per device, with that
+ * device current); make that first call before any stream capture.  Each call
+ * clears the keys, ticket and status word (cudaMemsetAsync on `stream`)
+ * before its kernel.  All calls share the one array and it keeps the last
+ * call's contents, so calls that overlap on the GPU (other streams, other
+ * threads) race: order them.  Device-side status bits of this variant are not
+ * reported (there is no workspace to read them from); commits that would pass
+ * out_cap are still skipped.
+ */
+DFLASH_API int dflash_verify_accept_noalloc(const dflash_dims* dims, const void* hidden,
+                                            const void* w_lm, const int32_t* block_ids,
+                                            const int32_t* len_before, int32_t* posterior,
+                                            int32_t* accept_len, int32_t* next_staged,
+                                            int32_t* commit_len, int32_t* out_tokens,
+                                            int32_t out_cap, dflash_stream_t stream);
+
+/*
  * a4 — KV-cache crop ([P1] §3; [P2] 单次前向验证 ⑨, 保证三).
  * For each of the n_views caches (target view, drafter view, ...) and each
  * sequence b: seq_len[b] <- new_len[b].  Rows below new_len are untouched.
