@@ -45,6 +45,8 @@ def parse_args(argv=None):
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--breakdown-steps", type=int, default=100,
+                    help="extra steps after the timed region with events around every call")
     ap.add_argument("--sets", type=int, default=0,
                     help="rotating input sets (0: enough to exceed twice the L2 size)")
     return ap.parse_args(argv)
@@ -215,8 +217,8 @@ def build_workload(cfg, n_sets: int, device="cuda"):
         if cfg.paged:
             lay = make_paged_layout(host["pages"], lens, reserve_tokens=16, slack_pages=64)
             n_rows = lay.n_pages * 16
-            k = device_normal_bf16(gen["ctx_k"], (lay.n_pages, 16, Hkv, D), device=device)
-            v = device_normal_bf16(gen["ctx_v"], (lay.n_pages, 16, Hkv, D), device=device)
+            k = device_normal_bf16(gen["ctx_k"], (lay.n_pages, Hkv, 16, D), device=device)
+            v = device_normal_bf16(gen["ctx_v"], (lay.n_pages, Hkv, 16, D), device=device)
             draft = dfl.KVView(k, v, i32(lens), capacity=lay.max_pages * 16,
                                page_table=i32(lay.page_table), free_list=i32(lay.free_list),
                                free_count=i32([lay.free_count]), page_size=16)
@@ -227,8 +229,8 @@ def build_workload(cfg, n_sets: int, device="cuda"):
             del n_rows
         else:
             cap = max_ctx + 16
-            k = device_normal_bf16(gen["ctx_k"], (B, cap, Hkv, D), device=device)
-            v = device_normal_bf16(gen["ctx_v"], (B, cap, Hkv, D), device=device)
+            k = device_normal_bf16(gen["ctx_k"], (B, Hkv, cap, D), device=device)
+            v = device_normal_bf16(gen["ctx_v"], (B, Hkv, cap, D), device=device)
             draft = dfl.KVView(k, v, i32(lens), capacity=cap)
             target = dfl.KVView(None, None, i32(lens + 16), capacity=cap)
         st = CycleState(
@@ -447,8 +449,8 @@ def main(argv=None):
     if status != 0:
         raise RuntimeError(f"device status {status:#x} after the timed region")
 
-    # launches of our kernels per step: verify 1, ctx_project 4, crop 1, attention 2
-    launches_per_step = 8
+    # launches of our kernels per step: verify 1, ctx_project 2, crop 1, attention 2
+    launches_per_step = 6
     value = whole_job_value(args.steps, world, max_s)
     acc_mean = float(np.mean([np.mean(accepts[(args.warmup + i) % n_sets])
                               for i in range(args.steps)]))
@@ -459,6 +461,34 @@ def main(argv=None):
     traffic = profiled_traffic(os.path.join(ROOT, "block_diffusion_speculative_02_gb300", "csrc",
                                             "verify_accept.cu"),
                                "lmhead_argmax_accept_qwen3_8b_b1.md")
+
+    # ---- per-call breakdown (separate pass, events between the calls) ----
+    breakdown = None
+    if args.breakdown_steps > 0:
+        names = ["verify_accept", "ctx_project", "kv_crop", "block_attention"]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
+               for _ in range(args.breakdown_steps)]
+        torch.cuda.synchronize()
+        for i in range(args.breakdown_steps):
+            st = states[i % n_sets]
+            ev = evs[i]
+            ev[0].record(stream)
+            dfl.dflash_verify_accept(dims, st.verify_hidden, w.w_lm, st.block_ids, st.len_before,
+                                     st.posterior, st.accept_len, st.next_staged, st.commit_len,
+                                     st.out_tokens, ws)
+            ev[1].record(stream)
+            dfl.dflash_ctx_project(dims, st.layer_hidden, w.w_fc, w.hidden_norm_w, w.w_k,
+                                   w.w_v, w.k_norm_w, st.write_pos, st.draft_cache, ws)
+            ev[2].record(stream)
+            dfl.dflash_kv_crop([st.target_view, st.draft_cache], st.commit_len, dims.batch, ws)
+            ev[3].record(stream)
+            dfl.dflash_block_attention(dims, st.q_blk, st.k_blk, st.v_blk, st.draft_cache,
+                                       1.0 / math.sqrt(cfg.head_dim), st.attn_out, ws)
+            ev[4].record(stream)
+        torch.cuda.synchronize()
+        breakdown = {n: 1e3 * statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
+                     for j, n in enumerate(names)}
+        breakdown["unit"] = "us per call (events between calls)"
 
     # ---- end to end: host buffers in, results out, every step ----
     e2e = None
@@ -516,6 +546,7 @@ def main(argv=None):
                          "frac": lm_gbs / peak, "traffic": traffic,
                          "bytes_per_launch": bytes_["lm_head"], "avg_launch_ms": lm_ms},
             "gpu_launches": launches_per_step * args.steps,
+            "breakdown": breakdown,
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,

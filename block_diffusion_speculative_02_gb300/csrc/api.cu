@@ -15,6 +15,15 @@ namespace {
 #define DFLASH_TMAP_L2_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_256B
 #endif
 
+#ifndef DFLASH_ATT_CTAS_PER_SM
+#define DFLASH_ATT_CTAS_PER_SM 2
+#endif
+constexpr int kAttCtasPerSm = DFLASH_ATT_CTAS_PER_SM;
+#ifndef DFLASH_GEMM_CTAS_PER_SM
+#define DFLASH_GEMM_CTAS_PER_SM 1
+#endif
+constexpr int kGemmCtasPerSm = DFLASH_GEMM_CTAS_PER_SM;
+
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -72,7 +81,7 @@ int make_plan(const dflash_dims& d, Plan* p) {
   q.num_sms = current_num_sms();
   if (q.num_sms <= 0) return DFLASH_E_CUDA;
   q.ntok = d.batch * kBlock;
-  const int slots = 2 * q.num_sms;  // two GEMM CTAs fit on one SM
+  const int slots = kGemmCtasPerSm * q.num_sms;
   q.fc_out_tiles = d.hidden / 128;
   q.fc_k_tiles = d.n_ctx_layers * d.hidden / 64;
   q.fc_tok_chunks = (q.ntok + 255) / 256;
@@ -86,7 +95,7 @@ int make_plan(const dflash_dims& d, Plan* p) {
     // enough (sequence, KV head, split) CTAs for two per SM, and no split
     // longer than 4096 keys so that ragged batches balance
     const int pages = (d.max_ctx + 15) / 16;
-    int s = (2 * q.num_sms) / (d.batch * d.n_kv_heads);
+    int s = (kAttCtasPerSm * q.num_sms) / (d.batch * d.n_kv_heads);
     const int by_len = (d.max_ctx + 4095) / 4096;
     if (s < by_len) s = by_len;
     if (s > pages) s = pages;
@@ -103,12 +112,10 @@ int make_plan(const dflash_dims& d, Plan* p) {
   off = align_up(off + sizeof(uint32_t) * (q.fc_out_tiles * q.fc_tok_chunks +
                                            q.kv_out_tiles * q.kv_tok_chunks), 256);
   q.off_ss = off;      off = align_up(off + sizeof(float) * (size_t)q.fc_out_tiles * q.ntok, 256);
-  q.off_fc = off;
-  off = align_up(off + sizeof(float) * (size_t)q.fc_splits * q.ntok * d.hidden, 256);
+  q.off_fc = off;      off = align_up(off + sizeof(float) * (size_t)q.ntok * d.hidden, 256);
   q.off_yhat = off;    off = align_up(off + 2 * sizeof(uint16_t) * (size_t)q.ntok * d.hidden, 1024);
   q.off_kv = off;
-  off = align_up(off + sizeof(float) * (size_t)q.kv_splits * q.ntok * 2 * d.n_kv_heads *
-                           d.head_dim, 256);
+  off = align_up(off + sizeof(float) * (size_t)q.ntok * 2 * d.n_kv_heads * d.head_dim, 256);
   const size_t att_units = (size_t)d.batch * d.n_kv_heads * q.att_splits * q.att_rows;
   q.off_att_o = off;   off = align_up(off + sizeof(float) * att_units * d.head_dim, 256);
   q.off_att_ml = off;  off = align_up(off + sizeof(float) * 2 * att_units, 256);

@@ -27,7 +27,10 @@ namespace {
 
 constexpr int kChunk = 64;   // keys per pipeline stage
 constexpr int kPage = 16;    // rows per TMA box
-constexpr int kStages = 3;
+#ifndef DFLASH_ATT_STAGES
+#define DFLASH_ATT_STAGES 3
+#endif
+constexpr int kStages = DFLASH_ATT_STAGES;
 
 struct AttnParams {
   int batch, n_q_heads, n_kv_heads, group, splits, rows;  // rows = group * 16
@@ -187,6 +190,7 @@ __device__ __forceinline__ void attend_chunk(const uint32_t (&qf)[D / 16][4], ui
 template <int D>
 __global__ void __launch_bounds__(288) block_attention_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    const __grid_constant__ CUtensorMap tm_k64, const __grid_constant__ CUtensorMap tm_v64,
     const AttnParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -213,6 +217,8 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
   if (warp == G && lane == 0) {
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_k64);
+    tma_prefetch_desc(&tm_v64);
   }
   __syncthreads();
   griddep_wait();
@@ -244,46 +250,59 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
         uint8_t* vst = kst + C::kTile;
         const int k0 = key_begin + c * kChunk;
         const int npg = min(kChunk / kPage, (key_end - k0 + kPage - 1) / kPage);
-        int rows[kChunk / kPage];
-        uint32_t bytes = 0;
-        for (int j = 0; j < npg; ++j) {
-          const int lp = k0 / kPage + j;
-          int r;
-          if (p.paged) {
-            const int id = p.page_table[static_cast<size_t>(b) * p.max_pages + lp];
-            r = id >= 0 ? id * kPage : -1;
-          } else {
-            r = b * p.capacity + lp * kPage;
-          }
-          rows[j] = r;
-          if (r >= 0) bytes += 2u * C::kHalves * kPage * 128;
-        }
-        // unmapped pages inside the length read as zeros
-        bool zeroed = false;
-        for (int j = 0; j < npg; ++j) {
-          if (rows[j] >= 0) continue;
-          set_status(p.status, DFLASH_ST_PAGE_MISSING);
+        // head-major caches: a page (16 rows) of one head is 16 * D contiguous
+        // elements, a contiguous cache holds each head's rows back to back
+        const int slab = b * p.n_kv_heads + g;  // contiguous: (sequence, head) slab
+        if (!p.paged && npg == kChunk / kPage) {
+          // whole chunk of a contiguous cache: one 64-row box per half
+          mbar_arrive_expect_tx(&full[stage], 2u * C::kHalves * kChunk * 128);
           for (int h = 0; h < C::kHalves; ++h) {
-            uint4* kz = reinterpret_cast<uint4*>(kst + h * kChunk * 128 + j * kPage * 128);
-            uint4* vz = reinterpret_cast<uint4*>(vst + h * kChunk * 128 + j * kPage * 128);
-            for (int i = 0; i < kPage * 128 / 16; ++i) kz[i] = vz[i] = make_uint4(0, 0, 0, 0);
-          }
-          zeroed = true;
-        }
-        if (zeroed) fence_proxy_async_smem();
-        if (bytes) {
-          mbar_arrive_expect_tx(&full[stage], bytes);
-          for (int j = 0; j < npg; ++j) {
-            if (rows[j] < 0) continue;
-            for (int h = 0; h < C::kHalves; ++h) {
-              tma_load_3d(kst + h * kChunk * 128 + j * kPage * 128, &tm_k, &full[stage], h * 64,
-                          g, rows[j], pol);
-              tma_load_3d(vst + h * kChunk * 128 + j * kPage * 128, &tm_v, &full[stage], h * 64,
-                          g, rows[j], pol);
-            }
+            tma_load_3d(kst + h * kChunk * 128, &tm_k64, &full[stage], h * 64, k0, slab, pol);
+            tma_load_3d(vst + h * kChunk * 128, &tm_v64, &full[stage], h * 64, k0, slab, pol);
           }
         } else {
-          mbar_arrive(&full[stage]);
+          int zc[kChunk / kPage];  // third coordinate of each page's box, -1 = unmapped
+          uint32_t bytes = 0;
+          for (int j = 0; j < npg; ++j) {
+            const int lp = k0 / kPage + j;
+            int z;
+            if (p.paged) {
+              const int id = p.page_table[static_cast<size_t>(b) * p.max_pages + lp];
+              z = id >= 0 ? id * p.n_kv_heads + g : -1;
+            } else {
+              z = slab;
+            }
+            zc[j] = z;
+            if (z >= 0) bytes += 2u * C::kHalves * kPage * 128;
+          }
+          // unmapped pages inside the length read as zeros
+          bool zeroed = false;
+          for (int j = 0; j < npg; ++j) {
+            if (zc[j] >= 0) continue;
+            set_status(p.status, DFLASH_ST_PAGE_MISSING);
+            for (int h = 0; h < C::kHalves; ++h) {
+              uint4* kz = reinterpret_cast<uint4*>(kst + h * kChunk * 128 + j * kPage * 128);
+              uint4* vz = reinterpret_cast<uint4*>(vst + h * kChunk * 128 + j * kPage * 128);
+              for (int i = 0; i < kPage * 128 / 16; ++i) kz[i] = vz[i] = make_uint4(0, 0, 0, 0);
+            }
+            zeroed = true;
+          }
+          if (zeroed) fence_proxy_async_smem();
+          if (bytes) {
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            for (int j = 0; j < npg; ++j) {
+              if (zc[j] < 0) continue;
+              const int row = p.paged ? 0 : k0 + j * kPage;
+              for (int h = 0; h < C::kHalves; ++h) {
+                tma_load_3d(kst + h * kChunk * 128 + j * kPage * 128, &tm_k, &full[stage], h * 64,
+                            row, zc[j], pol);
+                tma_load_3d(vst + h * kChunk * 128 + j * kPage * 128, &tm_v, &full[stage], h * 64,
+                            row, zc[j], pol);
+              }
+            }
+          } else {
+            mbar_arrive(&full[stage]);
+          }
         }
         if (++stage == kStages) {
           stage = 0;
@@ -379,37 +398,50 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
   for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
 
-  if (has_block)
-    attend_chunk<D>(qf, smem_u32(blk_k), smem_u32(blk_v), kPage, kPage, p.scale_log2, o, m_a, m_b,
-                    l_a, l_b);
-
+  // iteration -1 is the 16 block keys (only in the split that owns them), then
+  // the context chunks; one copy of the chunk code keeps the loop in the
+  // instruction cache
   uint32_t stage = 0, phase = 0;
-  for (int c = 0; c < n_chunks; ++c) {
-    const bool ok = mbar_wait(&full[stage], phase, abort_flag, p.status);
-    if (!__all_sync(0xffffffffu, ok)) break;
-    uint8_t* kst = smem + stage * C::kStage;
-    uint8_t* vst = kst + C::kTile;
-    const int n_valid = min(kChunk, key_end - (key_begin + c * kChunk));
-    const int n_fill = ((n_valid + 15) >> 4) << 4;
-    if (n_valid < n_fill) {
-      // rows past the length inside the last 16-key group: zero V so that
-      // 0-probability keys cannot inject NaN/Inf from stale memory
-      for (int i = lane; i < (n_fill - n_valid) * C::kHalves * 8; i += 32) {
-        const int row = n_valid + i / (C::kHalves * 8);
-        const int ch = i % (C::kHalves * 8);
-        *reinterpret_cast<uint4*>(vst + (ch >> 3) * kChunk * 128 + row * 128 +
-                                  (((ch & 7) ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+  for (int c = has_block ? -1 : 0; c < n_chunks; ++c) {
+    uint32_t kb, vb;
+    int half_rows, n_valid;
+    uint8_t* vst = nullptr;
+    if (c < 0) {
+      kb = smem_u32(blk_k);
+      vb = smem_u32(blk_v);
+      half_rows = kPage;
+      n_valid = kPage;
+    } else {
+      const bool ok = mbar_wait(&full[stage], phase, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      uint8_t* kst = smem + stage * C::kStage;
+      vst = kst + C::kTile;
+      kb = smem_u32(kst);
+      vb = smem_u32(vst);
+      half_rows = kChunk;
+      n_valid = min(kChunk, key_end - (key_begin + c * kChunk));
+      const int n_fill = ((n_valid + 15) >> 4) << 4;
+      if (n_valid < n_fill) {
+        // rows past the length inside the last 16-key group: zero V so that
+        // 0-probability keys cannot inject NaN/Inf from stale memory
+        for (int i = lane; i < (n_fill - n_valid) * C::kHalves * 8; i += 32) {
+          const int row = n_valid + i / (C::kHalves * 8);
+          const int ch = i % (C::kHalves * 8);
+          *reinterpret_cast<uint4*>(vst + (ch >> 3) * kChunk * 128 + row * 128 +
+                                    (((ch & 7) ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
       }
-      fence_proxy_async_smem();
-      __syncwarp();
     }
-    attend_chunk<D>(qf, smem_u32(kst), smem_u32(vst), kChunk, n_valid, p.scale_log2, o, m_a,
-                    m_b, l_a, l_b);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[stage]);
-    if (++stage == kStages) {
-      stage = 0;
-      phase ^= 1;
+    attend_chunk<D>(qf, kb, vb, half_rows, n_valid, p.scale_log2, o, m_a, m_b, l_a, l_b);
+    if (c >= 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1;
+      }
     }
   }
   griddep_launch_dependents();
@@ -435,17 +467,20 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
   }
 }
 
-// Merge the split partials by log-sum-exp: one warp per output row (b, i, h).
-// Lane s holds split s's (max, sum) and weight, broadcast by shuffles; the
-// O loads of consecutive splits are independent, so they overlap in flight.
+// Merge the split partials by log-sum-exp.  One CTA of four warps per output
+// row (b, i, h): all (max, sum) pairs are fetched at once, then each warp sums
+// a quarter of the splits with all of its loads in flight together, and the
+// four partial rows are added in shared memory -- two dependent global rounds.
 constexpr int kMaxSplits = 64;
 
-__global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(128) attn_combine_kernel(const CombineParams p) {
   griddep_wait();
   griddep_launch_dependents();
+  __shared__ float s_m[kMaxSplits], s_l[kMaxSplits];
+  __shared__ float s_acc[4][128];
+  __shared__ float s_lsum[4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (row >= p.batch * kBlock * p.n_q_heads) return;
+  const int row = blockIdx.x;
   const int b = row / (kBlock * p.n_q_heads);
   const int rem = row - b * kBlock * p.n_q_heads;
   const int i = rem / p.n_q_heads;
@@ -455,34 +490,25 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p
   const int g = h / p.group, w = h - g * p.group;
   const int rr = w * kBlock + i;
   const size_t unit0 = (static_cast<size_t>(b) * p.n_kv_heads + g) * p.splits;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const int s = lane + 32 * j;
-    if (s < p.splits) {
-      const float2 ml =
-          *reinterpret_cast<const float2*>(p.part_ml + ((unit0 + s) * p.rows + rr) * 2);
-      m[j] = ml.x;
-      l[j] = ml.y;
-    }
+  for (int s = threadIdx.x; s < p.splits; s += 128) {
+    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + ((unit0 + s) * p.rows + rr) * 2);
+    s_m[s] = ml.x;
+    s_l[s] = ml.y;
   }
-  float M = fmaxf(m[0], m[1]);
-#pragma unroll
-  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float wgt[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) wgt[j] = m[j] == -INFINITY ? 0.f : exp2f(m[j] - M);
-  float lsum = wgt[0] * l[0] + wgt[1] * l[1];
-#pragma unroll
-  for (int off = 16; off; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+  __syncthreads();
+  float M = -INFINITY;
+  for (int s = 0; s < p.splits; ++s) M = fmaxf(M, s_m[s]);
   const int D = p.head_dim;
   const int per = D / 32;  // 2 or 4 elements per lane
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
   const float* base = p.part_o + (unit0 * p.rows + rr) * D + lane * per;
   const size_t stride = static_cast<size_t>(p.rows) * D;
-#pragma unroll 8
-  for (int s = 0; s < p.splits; ++s) {
-    const float ws = __shfl_sync(0xffffffffu, wgt[s >> 5], s & 31);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float lsum = 0.f;
+#pragma unroll 16
+  for (int s = warp; s < p.splits; s += 4) {
+    const float ms = s_m[s];
+    const float ws = ms == -INFINITY ? 0.f : exp2f(ms - M);
+    lsum += ws * s_l[s];
     if (per == 4) {
       const float4 v = *reinterpret_cast<const float4*>(base + s * stride);
       acc[0] += ws * v.x; acc[1] += ws * v.y; acc[2] += ws * v.z; acc[3] += ws * v.w;
@@ -491,15 +517,25 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const CombineParams p
       acc[0] += ws * v.x; acc[1] += ws * v.y;
     }
   }
-  const float inv = 1.f / lsum;
-  uint16_t* dst = p.out + static_cast<size_t>(row) * D + lane * per;
-  if (per == 4) {
-    uint2 v;
-    v.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-    v.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-    *reinterpret_cast<uint2*>(dst) = v;
-  } else {
-    *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
+  for (int e = 0; e < per; ++e) s_acc[warp][lane * per + e] = acc[e];
+  if (lane == 0) s_lsum[warp] = lsum;
+  __syncthreads();
+  if (warp == 0) {
+    const float inv = 1.f / (s_lsum[0] + s_lsum[1] + s_lsum[2] + s_lsum[3]);
+    float o[4];
+    for (int e = 0; e < per; ++e) {
+      const int d = lane * per + e;
+      o[e] = (s_acc[0][d] + s_acc[1][d] + s_acc[2][d] + s_acc[3][d]) * inv;
+    }
+    uint16_t* dst = p.out + static_cast<size_t>(row) * D + lane * per;
+    if (per == 4) {
+      uint2 v;
+      v.x = pack_bf16(o[0], o[1]);
+      v.y = pack_bf16(o[2], o[3]);
+      *reinterpret_cast<uint2*>(dst) = v;
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16(o[0], o[1]);
+    }
   }
 }
 
@@ -507,25 +543,45 @@ template <int D>
 int launch_attention(const dflash_dims& dims, const Plan& plan, const dflash_kv_view& cache,
                      AttnParams& p, CombineParams& cp, cudaStream_t stream) {
   using C = Cfg<D>;
-  CUtensorMap tm_k, tm_v;
-  const uint64_t rows = p.paged ? static_cast<uint64_t>(cache.n_pages) * kPage
-                                : static_cast<uint64_t>(dims.batch) * cache.capacity;
-  const uint64_t pitch_h = static_cast<uint64_t>(D) * 2;
-  const uint64_t pitch_r = pitch_h * dims.n_kv_heads;
-  int rc = make_tmap_3d_bf16(&tm_k, cache.k, D, dims.n_kv_heads, rows, pitch_h, pitch_r, 64, 1,
-                             kPage);
-  if (rc) return rc;
-  if ((rc = make_tmap_3d_bf16(&tm_v, cache.v, D, dims.n_kv_heads, rows, pitch_h, pitch_r, 64, 1,
-                              kPage)))
-    return rc;
+  // head-major caches: contiguous [B, Hkv, cap, D] is a stack of (sequence,
+  // head) slabs of cap rows; paged [pages, Hkv, 16, D] a stack of 16-row slabs
+  CUtensorMap tm_k, tm_v, tm_k64, tm_v64;
+  const uint64_t pitch_row = static_cast<uint64_t>(D) * 2;
+  int rc;
+  if (p.paged) {
+    const uint64_t slabs = static_cast<uint64_t>(cache.n_pages) * dims.n_kv_heads;
+    if ((rc = make_tmap_3d_bf16(&tm_k, cache.k, D, kPage, slabs, pitch_row, pitch_row * kPage, 64,
+                                kPage, 1)))
+      return rc;
+    if ((rc = make_tmap_3d_bf16(&tm_v, cache.v, D, kPage, slabs, pitch_row, pitch_row * kPage, 64,
+                                kPage, 1)))
+      return rc;
+    tm_k64 = tm_k;
+    tm_v64 = tm_v;
+  } else {
+    const uint64_t slabs = static_cast<uint64_t>(dims.batch) * dims.n_kv_heads;
+    const uint64_t cap = static_cast<uint64_t>(cache.capacity);
+    if ((rc = make_tmap_3d_bf16(&tm_k, cache.k, D, cap, slabs, pitch_row, pitch_row * cap, 64,
+                                kPage, 1)))
+      return rc;
+    if ((rc = make_tmap_3d_bf16(&tm_v, cache.v, D, cap, slabs, pitch_row, pitch_row * cap, 64,
+                                kPage, 1)))
+      return rc;
+    if ((rc = make_tmap_3d_bf16(&tm_k64, cache.k, D, cap, slabs, pitch_row, pitch_row * cap, 64,
+                                kChunk, 1)))
+      return rc;
+    if ((rc = make_tmap_3d_bf16(&tm_v64, cache.v, D, cap, slabs, pitch_row, pitch_row * cap, 64,
+                                kChunk, 1)))
+      return rc;
+  }
   const int smem = 1024 + kStages * C::kStage + 2 * C::kBlkTile + 2 * kStages * 8 + 16;
   if ((rc = set_smem_limit(reinterpret_cast<const void*>(block_attention_kernel<D>), smem)))
     return rc;
   rc = launch(block_attention_kernel<D>, dim3(plan.att_splits, dims.n_kv_heads, dims.batch),
-              dim3(32 * (p.group + 1)), smem, stream, tm_k, tm_v, p);
+              dim3(32 * (p.group + 1)), smem, stream, tm_k, tm_v, tm_k64, tm_v64, p);
   if (rc) return rc;
   const int rows_out = dims.batch * kBlock * dims.n_q_heads;
-  return launch(attn_combine_kernel, dim3((rows_out + 7) / 8), dim3(256), 0, stream, cp);
+  return launch(attn_combine_kernel, dim3(rows_out), dim3(128), 0, stream, cp);
 }
 
 }  // namespace

@@ -10,8 +10,10 @@
 // 5th-generation tensor cores (128 output features are the MMA's M, the token
 // rows its N, fp32 accumulators in TMEM, the weight stream staged by a TMA
 // pipeline; memory-bound at small batch, so K is split until every SM streams
-// weights).  The last split CTA of each output tile (atomic ticket, no
-// waiting) reduces the split partials in split order and finishes the tile:
+// weights).  Each split CTA adds its partial tile into an fp32 accumulator in
+// the workspace with fire-and-forget atomic adds; the last split CTA of each
+// output tile (atomic ticket, no waiting) reads the finished sums in one round
+// trip, clears them for the next call and finishes the tile:
 //  1. fc GEMM   Y = X W_fc^T.  X is never materialised: the k-loop reads
 //     layer floor(k / H) through its own tensor map, which is the
 //     concatenation.  Finisher: g_h * Y stored as a bf16 pair hi + lo
@@ -21,6 +23,8 @@
 //  2. K/V GEMM  [K;V] = [hi;lo] W_{k|v}^T.  Finisher: the RMSNorm scale of Y
 //     (one factor per token row, so it commutes with the GEMM), per-head
 //     RMSNorm and RoPE for K, bf16 store into the cache rows.
+// The order of the fp32 additions across splits is not fixed, so results can
+// differ between runs by fp32 rounding (well inside the bf16 outputs' ulp).
 #include "common.cuh"
 #include "host.h"
 
@@ -31,6 +35,10 @@ constexpr int kGemmThreads = 192;
 constexpr int kATile = 128 * 128;  // 128 rows x 64 bf16
 constexpr int kGemmSmemBudget = 110 * 1024;  // two CTAs per SM
 constexpr int kMaxGemmStages = 8;
+#ifndef DFLASH_GEMM_CHUNKS_PER_STAGE
+#define DFLASH_GEMM_CHUNKS_PER_STAGE 2
+#endif
+constexpr int kGemmChunksPerStage = DFLASH_GEMM_CHUNKS_PER_STAGE;
 
 struct LayerMaps {
   CUtensorMap m[kMaxCtxLayers];
@@ -50,7 +58,9 @@ struct GemmParams {
   int ld_out;        // features per partial row
   int mma_n;         // MMA N = chunk_rows * (1 + hilo)
   int n_stages, stage_bytes, tmem_cols;
-  float* part;       // [splits][n_tok][ld_out]
+  int kb;            // 64-column K chunks per pipeline stage
+  int b_chunk;       // bytes of the token tile of one chunk (1024-aligned)
+  float* acc;        // [n_tok][ld_out] split-K accumulator, zero between calls
   uint32_t* tickets; // [out_tiles * n_chunks], zero between calls
   uint32_t* status;
   // shared by both finishers
@@ -100,17 +110,21 @@ __device__ void reserve_block_rows(const GemmParams& p, int b) {
   v.seq_len[b] = pos + kBlock;
 }
 
-// Sum of the split partials of feature f for token row tok, in split order.
-__device__ __forceinline__ float sum_splits(const GemmParams& p, int tok, int f) {
-  const float* src = p.part + static_cast<size_t>(tok) * p.ld_out + f;
-  const size_t stride = static_cast<size_t>(p.n_tok) * p.ld_out;
-  float y = 0.f;
-#pragma unroll 8
-  for (int s = 0; s < p.splits; ++s) y += src[s * stride];
-  return y;
+constexpr int kTokBatch = 16;  // token rows finished together (independent loads in flight)
+
+// The accumulated sums of feature f for token rows tok0 .. tok0+n-1 (all n
+// loads in flight together), cleared again for the next call.
+__device__ __forceinline__ void take_sums(const GemmParams& p, int tok0, int n, int f,
+                                          float (&y)[kTokBatch]) {
+  float* src = p.acc + static_cast<size_t>(tok0) * p.ld_out + f;
+#pragma unroll
+  for (int j = 0; j < kTokBatch; ++j) y[j] = j < n ? __ldcg(src + static_cast<size_t>(j) * p.ld_out) : 0.f;
+#pragma unroll
+  for (int j = 0; j < kTokBatch; ++j)
+    if (j < n) src[static_cast<size_t>(j) * p.ld_out] = 0.f;
 }
 
-// fc finisher (last split CTA of an output tile): Y = sum of the splits;
+// fc finisher (last split CTA of an output tile): Y = the accumulated sum;
 // hi/lo bf16 pair of g_h * Y for the next GEMM; partial sums of Y^2 over this
 // tile's 128 features (the RMSNorm scale itself is applied after the K/V GEMM,
 // since it is one factor per token row).
@@ -120,18 +134,25 @@ __device__ void finish_fc(const GemmParams& p, int o, int c, float* red) {
   const float g = p.hidden_norm_w ? bf16_bits_to_float(p.hidden_norm_w[f]) : 1.f;
   const int t0 = c * p.chunk_rows;
   const int nt = min(p.chunk_rows, p.n_tok - t0);
-  for (int j = 0; j < nt; ++j) {
-    const int tok = t0 + j;
-    const float y = sum_splits(p, tok, f);
-    const float gy = y * g;
-    const uint16_t hi = float_to_bf16_bits(gy);
-    p.yhat[static_cast<size_t>(tok) * p.hidden + f] = hi;
-    p.yhat[(static_cast<size_t>(p.n_tok) + tok) * p.hidden + f] =
-        float_to_bf16_bits(gy - bf16_bits_to_float(hi));
-    float sq = y * y;
+  for (int j0 = 0; j0 < nt; j0 += kTokBatch) {
+    const int n = min(kTokBatch, nt - j0);
+    float y[kTokBatch];
+    take_sums(p, t0 + j0, n, f, y);
 #pragma unroll
-    for (int off = 16; off; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-    if (lane == 0) red[warp * 256 + j] = sq;
+    for (int j = 0; j < kTokBatch; ++j) {
+      if (j < n) {
+        const int tok = t0 + j0 + j;
+        const float gy = y[j] * g;
+        const uint16_t hi = float_to_bf16_bits(gy);
+        p.yhat[static_cast<size_t>(tok) * p.hidden + f] = hi;
+        p.yhat[(static_cast<size_t>(p.n_tok) + tok) * p.hidden + f] =
+            float_to_bf16_bits(gy - bf16_bits_to_float(hi));
+      }
+      float sq = y[j] * y[j];
+#pragma unroll
+      for (int off = 16; off; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+      if (lane == 0 && j < n) red[warp * 256 + j0 + j] = sq;
+    }
   }
   named_bar_sync(1, 128);
   for (int j = et; j < nt; j += 128)
@@ -140,7 +161,7 @@ __device__ void finish_fc(const GemmParams& p, int o, int c, float* red) {
 }
 
 // kv finisher (last split CTA of an output tile): K or V rows of 128 features
-// (one or two heads) for every token of the chunk: sum of the splits, the
+// (one or two heads) for every token of the chunk: the accumulated sum, the
 // RMSNorm scale of Y, per-head RMSNorm and RoPE for K, bf16 store into the
 // cache row write_pos + t.
 __device__ void finish_kv(const GemmParams& p, int o, int c, float* smem_f) {
@@ -151,17 +172,26 @@ __device__ void finish_kv(const GemmParams& p, int o, int c, float* smem_f) {
   const int head = feat / D, d = feat - head * D;
   const int t0 = c * p.chunk_rows;
   const int nt = min(p.chunk_rows, p.n_tok - t0);
-  float* rbuf = smem_f;            // [256] per-token RMSNorm scale of Y
-  float* red = smem_f + 256;       // [4] per-warp sums
-  float* kbuf = smem_f + 264;      // [128] values for the RoPE partner exchange
-  for (int j = et; j < nt; j += 128) {
-    float r = 1.f;
-    if (p.hidden_norm_w) {
-      float tot = 0.f;
-      for (int q = 0; q < p.fc_out_tiles; ++q) tot += p.ss[static_cast<size_t>(q) * p.n_tok + t0 + j];
-      r = rsqrtf(tot / p.hidden + p.rms_eps);
+  float* rbuf = smem_f;                   // [256] per-token RMSNorm scale of Y
+  float* red = smem_f + 256;              // [4][kTokBatch] per-warp sums
+  float* kbuf = smem_f + 256 + 4 * kTokBatch;  // [kTokBatch][128] RoPE partner exchange
+  if (p.hidden_norm_w) {
+    // the fc tiles' partial sums of Y^2 for this chunk's rows, all loads in
+    // flight at once (threads over (tile, row)), then per-row sums in tile order
+    float* ssb = kbuf;  // [fc_out_tiles][nt], free until the first batch
+    const int n_ss = p.fc_out_tiles * nt;
+    for (int i = et; i < n_ss; i += 128) {
+      const int q = i / nt, j = i - q * nt;
+      ssb[i] = p.ss[static_cast<size_t>(q) * p.n_tok + t0 + j];
     }
-    rbuf[j] = r;
+    named_bar_sync(1, 128);
+    for (int j = et; j < nt; j += 128) {
+      float tot = 0.f;
+      for (int q = 0; q < p.fc_out_tiles; ++q) tot += ssb[q * nt + j];
+      rbuf[j] = rsqrtf(tot / p.hidden + p.rms_eps);
+    }
+  } else {
+    for (int j = et; j < nt; j += 128) rbuf[j] = 1.f;
   }
   named_bar_sync(1, 128);
   const float gk = (is_k && p.k_norm_w) ? bf16_bits_to_float(p.k_norm_w[d]) : 1.f;
@@ -170,46 +200,70 @@ __device__ void finish_kv(const GemmParams& p, int o, int c, float* smem_f) {
   const dflash_kv_view& cv = p.cache;
   const int limit = cv.page_table ? cv.max_pages * cv.page_size : cv.capacity;
   uint16_t* dst_base = static_cast<uint16_t*>(is_k ? cv.k : cv.v);
-  for (int j = 0; j < nt; ++j) {
-    const int tok = t0 + j;
-    float val = sum_splits(p, tok, o * 128 + et) * rbuf[j];
+  for (int j0 = 0; j0 < nt; j0 += kTokBatch) {
+    const int n = min(kTokBatch, nt - j0);
+    float val[kTokBatch];
+    take_sums(p, t0 + j0, n, o * 128 + et, val);
+#pragma unroll
+    for (int j = 0; j < kTokBatch; ++j) val[j] *= j < n ? rbuf[j0 + j] : 0.f;
     if (is_k) {
       if (p.k_norm_w) {
-        float sq = val * val;
 #pragma unroll
-        for (int off = 16; off; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-        if (lane == 0) red[warp] = sq;
+        for (int j = 0; j < kTokBatch; ++j) {
+          float sq = val[j] * val[j];
+#pragma unroll
+          for (int off = 16; off; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+          if (lane == 0) red[warp * kTokBatch + j] = sq;
+        }
         named_bar_sync(1, 128);
-        const float tot = D == 128 ? red[0] + red[1] + red[2] + red[3]
-                                   : red[(warp >> 1) * 2] + red[(warp >> 1) * 2 + 1];
-        val = val * rsqrtf(tot / D + p.rms_eps) * gk;
+#pragma unroll
+        for (int j = 0; j < kTokBatch; ++j) {
+          const float tot = D == 128 ? red[j] + red[kTokBatch + j] + red[2 * kTokBatch + j] +
+                                           red[3 * kTokBatch + j]
+                                     : red[(warp >> 1) * 2 * kTokBatch + j] +
+                                           red[((warp >> 1) * 2 + 1) * kTokBatch + j];
+          val[j] = val[j] * rsqrtf(tot / D + p.rms_eps) * gk;
+        }
       }
-      kbuf[et] = val;
+#pragma unroll
+      for (int j = 0; j < kTokBatch; ++j) kbuf[j * 128 + et] = val[j];
       named_bar_sync(1, 128);
-      const int b = tok / kBlock, t = tok - (tok / kBlock) * kBlock;
-      const int pos = p.pos_snapshot[b] + t;
-      float sn, cs;
-      sincosf(rope_angle(pos, p.rope.hi[fi], p.rope.lo[fi]), &sn, &cs);
-      const float partner = d < half ? kbuf[et + half] : kbuf[et - half];
-      val = d < half ? val * cs - partner * sn : val * cs + partner * sn;
-      named_bar_sync(1, 128);  // kbuf and red are reused by the next token
-    }
-    const int b = tok / kBlock, t = tok - b * kBlock;
-    const int pos0 = p.pos_snapshot[b];
-    if (pos0 < 0 || pos0 + kBlock > limit) continue;  // flagged by the reservation
-    const int pos = pos0 + t;
-    size_t row;
-    if (cv.page_table) {
-      const int page = cv.page_table[static_cast<size_t>(b) * cv.max_pages + pos / cv.page_size];
-      if (page < 0) {
-        if (et == 0) set_status(p.status, DFLASH_ST_PAGE_MISSING);
-        continue;
+#pragma unroll
+      for (int j = 0; j < kTokBatch; ++j) {
+        const int tok = t0 + j0 + j;
+        const int b = tok / kBlock;
+        const int pos = (j < n ? p.pos_snapshot[b] : 0) + (tok - b * kBlock);
+        float sn, cs;
+        sincosf(rope_angle(pos, p.rope.hi[fi], p.rope.lo[fi]), &sn, &cs);
+        const float partner = d < half ? kbuf[j * 128 + et + half] : kbuf[j * 128 + et - half];
+        val[j] = d < half ? val[j] * cs - partner * sn : val[j] * cs + partner * sn;
       }
-      row = static_cast<size_t>(page) * cv.page_size + pos % cv.page_size;
-    } else {
-      row = static_cast<size_t>(b) * cv.capacity + pos;
+      named_bar_sync(1, 128);  // kbuf and red are reused by the next batch
     }
-    dst_base[(row * p.n_kv_heads + head) * D + d] = float_to_bf16_bits(val);
+#pragma unroll
+    for (int j = 0; j < kTokBatch; ++j) {
+      if (j >= n) continue;
+      const int tok = t0 + j0 + j;
+      const int b = tok / kBlock, t = tok - b * kBlock;
+      const int pos0 = p.pos_snapshot[b];
+      if (pos0 < 0 || pos0 + kBlock > limit) continue;  // flagged by the reservation
+      const int pos = pos0 + t;
+      // head-major caches: [B, Hkv, capacity, D] or [pages, Hkv, page_size, D]
+      size_t off;
+      if (cv.page_table) {
+        const int page =
+            cv.page_table[static_cast<size_t>(b) * cv.max_pages + pos / cv.page_size];
+        if (page < 0) {
+          if (et == 0) set_status(p.status, DFLASH_ST_PAGE_MISSING);
+          continue;
+        }
+        off = ((static_cast<size_t>(page) * p.n_kv_heads + head) * cv.page_size +
+               pos % cv.page_size) * D + d;
+      } else {
+        off = ((static_cast<size_t>(b) * p.n_kv_heads + head) * cv.capacity + pos) * D + d;
+      }
+      dst_base[off] = float_to_bf16_bits(val[j]);
+    }
   }
 }
 
@@ -264,18 +318,25 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
       const uint32_t bytes = kATile + (1 + p.hilo) * p.chunk_rows * 128;
       uint32_t stage = 0, phase = 0;
       int issued = 0;
-      for (int kt = kt0; kt < kt1; ++kt) {
+      for (int kt = kt0; kt < kt1; kt += p.kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) break;
+        const int nck = min(p.kb, kt1 - kt);
         uint8_t* a = smem + stage * p.stage_bytes;
-        uint8_t* bt = a + kATile;
-        mbar_arrive_expect_tx(&full[stage], bytes);
-        tma_load_2d(a, ma, &full[stage], kt * 64, arow, pol_w);
-        const int l = (kt * 64) / p.layer_cols;
-        const int col = kt * 64 - l * p.layer_cols;
-        tma_load_2d(bt, &tm_b.m[l], &full[stage], col, c * p.chunk_rows, pol_x);
-        if (p.hilo)
-          tma_load_2d(bt + p.chunk_rows * 128, &tm_b.m[l], &full[stage], col,
-                      p.n_tok + c * p.chunk_rows, pol_x);
+        uint8_t* bt = a + p.kb * kATile;
+        mbar_arrive_expect_tx(&full[stage], nck * bytes);
+        // the chunks of a stage go out back to back: each weight row is
+        // requested as nck * 128 contiguous bytes
+        for (int j = 0; j < nck; ++j) {
+          const int k = kt + j;
+          tma_load_2d(a + j * kATile, ma, &full[stage], k * 64, arow, pol_w);
+          const int l = (k * 64) / p.layer_cols;
+          const int col = k * 64 - l * p.layer_cols;
+          uint8_t* bj = bt + j * p.b_chunk;
+          tma_load_2d(bj, &tm_b.m[l], &full[stage], col, c * p.chunk_rows, pol_x);
+          if (p.hilo)
+            tma_load_2d(bj + p.chunk_rows * 128, &tm_b.m[l], &full[stage], col,
+                        p.n_tok + c * p.chunk_rows, pol_x);
+        }
         ++issued;
         if (++stage == static_cast<uint32_t>(p.n_stages)) {
           stage = 0;
@@ -293,16 +354,19 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
       const uint32_t idesc = umma_idesc_bf16(128, p.mma_n);
       uint32_t stage = 0, phase = 0;
       bool first = true;
-      for (int kt = kt0; kt < kt1; ++kt) {
+      for (int kt = kt0; kt < kt1; kt += p.kb) {
         if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) break;
         tc_fence_after();
+        const int nck = min(p.kb, kt1 - kt);
         const uint32_t a_addr = base + stage * p.stage_bytes;
-        const uint64_t adesc = umma_sdesc_sw128(a_addr);
-        const uint64_t bdesc = umma_sdesc_sw128(a_addr + kATile);
+        for (int j = 0; j < nck; ++j) {
+          const uint64_t adesc = umma_sdesc_sw128(a_addr + j * kATile);
+          const uint64_t bdesc = umma_sdesc_sw128(a_addr + p.kb * kATile + j * p.b_chunk);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          umma_bf16(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, idesc, first ? 0u : 1u);
-          first = false;
+          for (int kk = 0; kk < 4; ++kk) {
+            umma_bf16(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, idesc, first ? 0u : 1u);
+            first = false;
+          }
         }
         umma_commit(&empty[stage]);
         if (++stage == static_cast<uint32_t>(p.n_stages)) {
@@ -324,7 +388,9 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
       tc_fence_after();
       const int f = o * 128 + q * 32 + lane;
       const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-      float* dst = p.part + static_cast<size_t>(s) * p.n_tok * p.ld_out + f;
+      // split-K reduction by fire-and-forget atomic adds at L2: the finisher then
+      // needs one round trip instead of one per split
+      float* dst = p.acc + f;
       for (int c0 = 0; c0 < p.chunk_rows; c0 += 16) {
         uint32_t v[16], w[16];
         tmem_ld_32x32b_x16(tmem_base + lane_base + c0, v);
@@ -335,7 +401,7 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
           const int tok = c * p.chunk_rows + c0 + j;
           float val = __uint_as_float(v[j]);
           if (p.hilo) val += __uint_as_float(w[j]);
-          if (tok < p.n_tok) dst[static_cast<size_t>(tok) * p.ld_out] = val;
+          if (tok < p.n_tok) atomicAdd(dst + static_cast<size_t>(tok) * p.ld_out, val);
         }
       }
       tc_fence_before();
@@ -369,7 +435,12 @@ int gemm_smem(int stage_bytes, int n_stages) {
 }
 
 int setup_gemm(GemmParams& g, int b_rows_per_stage) {
-  g.stage_bytes = kATile + ((b_rows_per_stage * 128 + 1023) / 1024) * 1024;
+  g.b_chunk = ((b_rows_per_stage * 128 + 1023) / 1024) * 1024;
+  // as many 64-column chunks per stage as still leave three stages
+  g.kb = kGemmChunksPerStage;
+  while (g.kb > 1 && (kGemmSmemBudget - 1024 - 24) / (g.kb * (kATile + g.b_chunk) + 16) < 3)
+    g.kb >>= 1;
+  g.stage_bytes = g.kb * (kATile + g.b_chunk);
   g.n_stages = (kGemmSmemBudget - 1024 - 24) / (g.stage_bytes + 16);
   if (g.n_stages > kMaxGemmStages) g.n_stages = kMaxGemmStages;
   if (g.n_stages < 2) {
@@ -454,7 +525,7 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
     g.hilo = 0;
     g.ld_out = H;
     g.mma_n = g.chunk_rows;
-    g.part = part_fc;
+    g.acc = part_fc;
     g.tickets = tickets;
     const int smem = setup_gemm(g, g.chunk_rows);
     CUtensorMap ta;
@@ -487,7 +558,7 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
     g.hilo = 1;
     g.ld_out = 2 * kvd;
     g.mma_n = 2 * g.chunk_rows;
-    g.part = part_kv;
+    g.acc = part_kv;
     g.tickets = tickets + plan.fc_out_tiles * plan.fc_tok_chunks;
     const int smem = setup_gemm(g, 2 * g.chunk_rows);
     CUtensorMap tk, tv;

@@ -37,9 +37,13 @@ constexpr int kUnitRows = 8;             // balancing granule = one 8-row TMA bo
 constexpr int kSmemBudget = 224 * 1024;
 constexpr int kMaxStages = 12;
 #ifndef DFLASH_LM_CHUNKS_PER_STAGE
-#define DFLASH_LM_CHUNKS_PER_STAGE 2
+#define DFLASH_LM_CHUNKS_PER_STAGE 4
 #endif
 constexpr int kLmChunksPerStage = DFLASH_LM_CHUNKS_PER_STAGE;  // power of two
+#ifndef DFLASH_LM_MIN_STAGES
+#define DFLASH_LM_MIN_STAGES 2
+#endif
+constexpr int kLmMinStages = DFLASH_LM_MIN_STAGES;
 
 struct LmParams {
   int vocab, hidden, ntok;
@@ -354,10 +358,10 @@ extern "C" int dflash_verify_accept(const dflash_dims* dims, const void* hidden,
   p.n_units = (p.vocab + kUnitRows - 1) / kUnitRows;
   p.x_chunk = ((p.n_xbox * p.ntok_box * 128) + 1023) / 1024 * 1024;
   const int fixed = 1024 /*alignment slack*/ + 8 * 5 + 16 + 8 * p.ntok + 64;
-  // as many 64-column chunks per stage as divide K and still leave three stages
+  // as many 64-column chunks per stage as divide K and still leave enough stages
   p.kb = kLmChunksPerStage;
   while (p.kb > 1 && ((p.hidden / 64) % p.kb ||
-                      (kSmemBudget - fixed) / (p.kb * (kATileBytes + p.x_chunk) + 16) < 3))
+                      (kSmemBudget - fixed) / (p.kb * (kATileBytes + p.x_chunk) + 16) < kLmMinStages))
     p.kb >>= 1;
   p.stage_bytes = p.kb * (kATileBytes + p.x_chunk);
   p.n_stages = (kSmemBudget - fixed) / (p.stage_bytes + 16);
@@ -473,7 +477,7 @@ extern "C" int dflash_verify_accept_noalloc(const dflash_dims* dims, const void*
   const int fixed = 1024 + 8 * 5 + 16 + 8 * p.ntok + 64;
   p.kb = kLmChunksPerStage;
   while (p.kb > 1 && ((p.hidden / 64) % p.kb ||
-                      (kSmemBudget - fixed) / (p.kb * (kATileBytes + p.x_chunk) + 16) < 3))
+                      (kSmemBudget - fixed) / (p.kb * (kATileBytes + p.x_chunk) + 16) < kLmMinStages))
     p.kb >>= 1;
   p.stage_bytes = p.kb * (kATileBytes + p.x_chunk);
   p.n_stages = (kSmemBudget - fixed) / (p.stage_bytes + 16);

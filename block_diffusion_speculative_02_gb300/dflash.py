@@ -16,7 +16,9 @@ from typing import Optional, Sequence
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libdflash.so")
+# DFLASH_LIBRARY may name another build of the same library (e.g. one compiled
+# with different tile parameters); the default is the in-tree build.
+LIB_PATH = os.environ.get("DFLASH_LIBRARY") or os.path.join(_PKG, "libdflash.so")
 
 DFLASH_OK = 0
 STATUS_BITS = {

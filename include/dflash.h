@@ -90,9 +90,10 @@ typedef struct {
   float rms_eps;         /* RMSNorm epsilon (1e-6)                          */
 } dflash_dims;
 
-/* A KV cache as the kernels see it.
- *  contiguous (page_table == NULL): k, v are bf16 [B, capacity, Hkv, D].
- *  paged      (page_table != NULL): k, v are bf16 [n_pages, page_size, Hkv, D];
+/* A KV cache as the kernels see it.  Both layouts are head-major, so that the
+ * rows of one KV head are contiguous (what one attention CTA streams):
+ *  contiguous (page_table == NULL): k, v are bf16 [B, Hkv, capacity, D].
+ *  paged      (page_table != NULL): k, v are bf16 [n_pages, Hkv, page_size, D];
  *             page_table is int32 [B, max_pages] (-1 = unmapped); the free
  *             pages are free_list[0 .. *free_count) (int32, device).
  *  seq_len is int32 [B] on the device: the number of valid rows.

@@ -309,6 +309,20 @@ def scatter_paged(layout: PagedLayout, per_seq: list, row_shape) -> np.ndarray:
     return pool
 
 
+def scatter_paged_heads(layout: PagedLayout, per_seq: list, n_heads: int,
+                        head_dim: int) -> np.ndarray:
+    """Head-major page pool [n_pages, Hkv, page, D] from per-sequence rows [L_b, Hkv, D]."""
+    pool = scatter_paged(layout, per_seq, (n_heads, head_dim))
+    return np.ascontiguousarray(pool.transpose(0, 2, 1, 3))
+
+
+def pack_contiguous_heads(per_seq: list, capacity: int, n_heads: int,
+                          head_dim: int) -> np.ndarray:
+    """Head-major contiguous cache [B, Hkv, capacity, D] from rows [L_b, Hkv, D]."""
+    out = pack_contiguous(per_seq, capacity, (n_heads, head_dim))
+    return np.ascontiguousarray(out.transpose(0, 2, 1, 3))
+
+
 def pack_contiguous(per_seq: list, capacity: int, row_shape) -> np.ndarray:
     """Pack per-sequence rows [L_b, ...] into a contiguous cache [B, capacity, ...] (bits)."""
     B = len(per_seq)

@@ -9,7 +9,7 @@ import torch
 
 from oracle.dflash_oracle import block_attention as ref_attention
 from synthetic import (CONFIG_BY_NAME, make_cycle_inputs, make_paged_layout, normal_bf16,
-                       pack_contiguous, scatter_paged)
+                       pack_contiguous_heads, scatter_paged_heads)
 from tests.gpu_helpers import assert_close_bf16, dev_bf16, dev_i32, host_f64
 
 pytestmark = pytest.mark.gpu
@@ -31,25 +31,25 @@ def run_attention(q, k, v, ctx_k, ctx_v, lens, Hq, Hkv, D, theta, paged=False, c
     ws = dfl.alloc_workspace(dims)
     if paged:
         lay = make_paged_layout(rng, lens, reserve_tokens=16)
-        kp = scatter_paged(lay, ctx_k, (Hkv, D))
-        vp = scatter_paged(lay, ctx_v, (Hkv, D))
+        kp = scatter_paged_heads(lay, ctx_k, Hkv, D)      # [pages, Hkv, 16, D]
+        vp = scatter_paged_heads(lay, ctx_v, Hkv, D)
         if garbage:                       # NaN bit patterns in every unused row
             for b, L in enumerate(lens):
                 pg = lay.page_table[b, int(L) // 16] if L % 16 else -1
                 if pg >= 0:
-                    kp[pg, L % 16:] = 0x7FC1
-                    vp[pg, L % 16:] = 0x7FC1
+                    kp[pg, :, L % 16:] = 0x7FC1
+                    vp[pg, :, L % 16:] = 0x7FC1
         view = dfl.KVView(dev_bf16(kp), dev_bf16(vp), dev_i32(lens), capacity=lay.max_pages * 16,
                           page_table=dev_i32(lay.page_table), free_list=dev_i32(lay.free_list),
                           free_count=dev_i32([lay.free_count]), page_size=16)
     else:
         cap = capacity or int(max(lens)) + 16
-        kc = pack_contiguous(ctx_k, cap, (Hkv, D))
-        vc = pack_contiguous(ctx_v, cap, (Hkv, D))
+        kc = pack_contiguous_heads(ctx_k, cap, Hkv, D)       # [B, Hkv, cap, D]
+        vc = pack_contiguous_heads(ctx_v, cap, Hkv, D)
         if garbage:
             for b, L in enumerate(lens):
-                kc[b, L:] = 0x7FC1
-                vc[b, L:] = 0xFF80
+                kc[b, :, L:] = 0x7FC1
+                vc[b, :, L:] = 0xFF80
         view = dfl.KVView(dev_bf16(kc), dev_bf16(vc), dev_i32(lens), capacity=cap)
     out = torch.full((B, 16, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
     dfl.dflash_block_attention(dims, dev_bf16(q), dev_bf16(k), dev_bf16(v), view,

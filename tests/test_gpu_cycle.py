@@ -13,7 +13,7 @@ from oracle.dflash_oracle import ctx_project as ref_project
 from oracle.dflash_oracle import bf16_to_f64, kv_crop_lengths, near_tie_mask
 from oracle.dflash_oracle import verify_accept as ref_verify
 from synthetic import (draw_accept_lengths, make_block_ids, make_paged_layout, normal_bf16,
-                       pack_contiguous, scatter_paged, unit_rms_rows_bf16)
+                       pack_contiguous_heads, scatter_paged_heads, unit_rms_rows_bf16)
 from tests.gpu_helpers import assert_close_bf16, check_verify, dev_bf16, dev_i32, host_f64
 
 pytestmark = pytest.mark.gpu
@@ -41,13 +41,13 @@ def test_three_cycles_carry_state(paged):
     ws = dfl.alloc_workspace(dims)
     if paged:
         lay = make_paged_layout(rng, L0, reserve_tokens=64, max_len=cap)
-        draft = dfl.KVView(dev_bf16(scatter_paged(lay, ctx_k, (Hkv, D))),
-                           dev_bf16(scatter_paged(lay, ctx_v, (Hkv, D))), dev_i32(L0),
+        draft = dfl.KVView(dev_bf16(scatter_paged_heads(lay, ctx_k, Hkv, D)),
+                           dev_bf16(scatter_paged_heads(lay, ctx_v, Hkv, D)), dev_i32(L0),
                            capacity=lay.max_pages * 16, page_table=dev_i32(lay.page_table),
                            free_list=dev_i32(lay.free_list), free_count=dev_i32([lay.free_count]))
     else:
-        draft = dfl.KVView(dev_bf16(pack_contiguous(ctx_k, cap, (Hkv, D))),
-                           dev_bf16(pack_contiguous(ctx_v, cap, (Hkv, D))), dev_i32(L0),
+        draft = dfl.KVView(dev_bf16(pack_contiguous_heads(ctx_k, cap, Hkv, D)),
+                           dev_bf16(pack_contiguous_heads(ctx_v, cap, Hkv, D)), dev_i32(L0),
                            capacity=cap)
     target = dfl.KVView(None, None, dev_i32(L0 + 16), capacity=cap)
     w = CycleWeights(dev_bf16(w_lm), dev_bf16(w_fc), dev_bf16(gh), dev_bf16(wk), dev_bf16(wv),
@@ -113,9 +113,9 @@ def test_three_cycles_carry_state(paged):
                 r = int(L[b]) + t
                 if paged:
                     pg = draft.page_table.cpu().numpy()[b, r // 16]
-                    row = kk[pg, r % 16]
+                    row = kk[pg, :, r % 16]
                 else:
-                    row = kk[b, r]
+                    row = kk[b, :, r]
                 np.testing.assert_allclose(row, ref_k[b][r], atol=2e-2)
         L = newL
         ref_k = [ref_k[b][:L[b]] for b in range(B)]

@@ -45,7 +45,7 @@ def run_project(layers, w_fc, gh, wk, wv, gk, write_pos, Hq, Hkv, D, theta, page
     lay = None
     if paged:
         lay = make_paged_layout(rng, write_pos, reserve_tokens=16, slack_pages=pool_slack)
-        kc = torch.full((lay.n_pages, 16, Hkv, D), 1.0, dtype=torch.bfloat16, device="cuda")
+        kc = torch.full((lay.n_pages, Hkv, 16, D), 1.0, dtype=torch.bfloat16, device="cuda")
         vc = kc.clone()
         view = dfl.KVView(kc, vc, dev_i32(write_pos if alias else np.zeros(B, np.int32)),
                           capacity=lay.max_pages * 16, page_table=dev_i32(lay.page_table),
@@ -53,7 +53,7 @@ def run_project(layers, w_fc, gh, wk, wv, gk, write_pos, Hq, Hkv, D, theta, page
                           page_size=16)
     else:
         cap = capacity or max_ctx + 3
-        kc = torch.full((B, cap, Hkv, D), 1.0, dtype=torch.bfloat16, device="cuda")
+        kc = torch.full((B, Hkv, cap, D), 1.0, dtype=torch.bfloat16, device="cuda")
         vc = kc.clone()
         view = dfl.KVView(kc, vc, dev_i32(write_pos if alias else np.zeros(B, np.int32)),
                           capacity=cap)
@@ -76,11 +76,11 @@ def gather_rows(view, lay, write_pos, Hkv, D):
             r = int(pos) + t
             if table is not None:
                 pg = table[b, r // 16]
-                ks.append(k[pg, r % 16])
-                vs.append(v[pg, r % 16])
+                ks.append(k[pg, :, r % 16])
+                vs.append(v[pg, :, r % 16])
             else:
-                ks.append(k[b, r])
-                vs.append(v[b, r])
+                ks.append(k[b, :, r])
+                vs.append(v[b, :, r])
     return np.stack(ks), np.stack(vs)
 
 
@@ -107,7 +107,7 @@ def test_project_tiny(norms):
     view, _, ek, ev = check_project(layers, w_fc, gh, wk, wv, gk, [128], 4, 2, 64)
     # rows outside the block keep their old contents
     kb = host_bits(view.k)
-    assert np.all(kb[0, :128] == SENTINEL) and np.all(kb[0, 144:] == SENTINEL)
+    assert np.all(kb[0, :, :128] == SENTINEL) and np.all(kb[0, :, 144:] == SENTINEL)
     print(ek, ev)
 
 
@@ -166,7 +166,7 @@ def test_project_flags_an_exhausted_page_pool():
     table = np.full((B, 4), -1, np.int32)
     table[0, 0], table[1, 0] = 0, 1          # each sequence owns one page, needs a second
     free = np.array([2, -1, -1, -1], np.int32)
-    kc = torch.full((4, 16, Hkv, D), 1.0, dtype=torch.bfloat16, device="cuda")
+    kc = torch.full((4, Hkv, 16, D), 1.0, dtype=torch.bfloat16, device="cuda")
     view = dfl.KVView(kc, kc.clone(), dev_i32([0, 0]), capacity=64, page_table=dev_i32(table),
                       free_list=dev_i32(free), free_count=dev_i32([1]), page_size=16)
     dfl.dflash_ctx_project(dims, [dev_bf16(x) for x in layers], dev_bf16(w_fc), dev_bf16(gh),
