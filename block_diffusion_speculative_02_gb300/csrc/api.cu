@@ -19,10 +19,6 @@ namespace {
 #define DFLASH_ATT_CTAS_PER_SM 2
 #endif
 constexpr int kAttCtasPerSm = DFLASH_ATT_CTAS_PER_SM;
-#ifndef DFLASH_GEMM_CTAS_PER_SM
-#define DFLASH_GEMM_CTAS_PER_SM 1
-#endif
-constexpr int kGemmCtasPerSm = DFLASH_GEMM_CTAS_PER_SM;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

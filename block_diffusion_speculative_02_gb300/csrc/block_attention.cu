@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
       const float x1 = bf16_bits_to_float(p.k_blk[src + d]);
       const float x2 = bf16_bits_to_float(p.k_blk[src + d + D / 2]);
       float sn, cs;
-      sincosf(rope_angle(L + j, p.rope.hi[d], p.rope.lo[d]), &sn, &cs);
+      rope_sincos(L + j, p.rope.hi[d], p.rope.lo[d], &sn, &cs);
       uint16_t* kd = reinterpret_cast<uint16_t*>(blk_k);
       uint16_t* vd = reinterpret_cast<uint16_t*>(blk_v);
       const int e1 = d, e2 = d + D / 2;
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
         for (int r = 0; r < 2; ++r) {
           const int pos = Lc + (r ? rb : ra);
           float sn, cs;
-          sincosf(rope_angle(pos, p.rope.hi[d], p.rope.lo[d]), &sn, &cs);
+          rope_sincos(pos, p.rope.hi[d], p.rope.lo[d], &sn, &cs);
           const float x1 = qv[kk][r][e], x2 = qv[kk + D / 32][r][e];
           qv[kk][r][e] = x1 * cs - x2 * sn;
           qv[kk + D / 32][r][e] = x2 * cs + x1 * sn;
@@ -473,6 +473,7 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
 // four partial rows are added in shared memory -- two dependent global rounds.
 constexpr int kMaxSplits = 64;
 
+template <int D>
 __global__ void __launch_bounds__(128) attn_combine_kernel(const CombineParams p) {
   griddep_wait();
   griddep_launch_dependents();
@@ -498,8 +499,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const CombineParams p
   __syncthreads();
   float M = -INFINITY;
   for (int s = 0; s < p.splits; ++s) M = fmaxf(M, s_m[s]);
-  const int D = p.head_dim;
-  const int per = D / 32;  // 2 or 4 elements per lane
+  constexpr int per = D / 32;  // 2 or 4 elements per lane
   const float* base = p.part_o + (unit0 * p.rows + rr) * D + lane * per;
   const size_t stride = static_cast<size_t>(p.rows) * D;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const CombineParams p
     const float ms = s_m[s];
     const float ws = ms == -INFINITY ? 0.f : exp2f(ms - M);
     lsum += ws * s_l[s];
-    if (per == 4) {
+    if constexpr (per == 4) {
       const float4 v = *reinterpret_cast<const float4*>(base + s * stride);
       acc[0] += ws * v.x; acc[1] += ws * v.y; acc[2] += ws * v.z; acc[3] += ws * v.w;
     } else {
@@ -517,18 +517,20 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(const CombineParams p
       acc[0] += ws * v.x; acc[1] += ws * v.y;
     }
   }
+#pragma unroll
   for (int e = 0; e < per; ++e) s_acc[warp][lane * per + e] = acc[e];
   if (lane == 0) s_lsum[warp] = lsum;
   __syncthreads();
   if (warp == 0) {
     const float inv = 1.f / (s_lsum[0] + s_lsum[1] + s_lsum[2] + s_lsum[3]);
     float o[4];
+#pragma unroll
     for (int e = 0; e < per; ++e) {
       const int d = lane * per + e;
       o[e] = (s_acc[0][d] + s_acc[1][d] + s_acc[2][d] + s_acc[3][d]) * inv;
     }
     uint16_t* dst = p.out + static_cast<size_t>(row) * D + lane * per;
-    if (per == 4) {
+    if constexpr (per == 4) {
       uint2 v;
       v.x = pack_bf16(o[0], o[1]);
       v.y = pack_bf16(o[2], o[3]);
@@ -581,7 +583,7 @@ int launch_attention(const dflash_dims& dims, const Plan& plan, const dflash_kv_
               dim3(32 * (p.group + 1)), smem, stream, tm_k, tm_v, tm_k64, tm_v64, p);
   if (rc) return rc;
   const int rows_out = dims.batch * kBlock * dims.n_q_heads;
-  return launch(attn_combine_kernel, dim3(rows_out), dim3(128), 0, stream, cp);
+  return launch(attn_combine_kernel<D>, dim3(rows_out), dim3(128), 0, stream, cp);
 }
 
 }  // namespace

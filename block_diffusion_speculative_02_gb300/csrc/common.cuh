@@ -94,6 +94,15 @@ __device__ __forceinline__ float rope_angle(int pos, float f_hi, float f_lo) {
   return r + a_lo;
 }
 
+// sin and cos of the rotation angle pos * inv_freq.  The angle is first reduced
+// to about [-pi, pi] (above), where the hardware approximations __sinf/__cosf
+// are accurate to ~4e-7 absolute; they are single instructions, which keeps
+// the code of the (cold) RoPE paths small.
+__device__ __forceinline__ void rope_sincos(int pos, float f_hi, float f_lo, float* sn,
+                                            float* cs) {
+  __sincosf(rope_angle(pos, f_hi, f_lo), sn, cs);
+}
+
 // ----------------------------------------------------------------------------
 // mbarrier
 // ----------------------------------------------------------------------------

@@ -33,10 +33,9 @@ namespace {
 
 constexpr int kGemmThreads = 192;
 constexpr int kATile = 128 * 128;  // 128 rows x 64 bf16
-constexpr int kGemmSmemBudget = 110 * 1024;  // two CTAs per SM
-constexpr int kMaxGemmStages = 8;
+constexpr int kMaxGemmStages = 12;
 #ifndef DFLASH_GEMM_CHUNKS_PER_STAGE
-#define DFLASH_GEMM_CHUNKS_PER_STAGE 2
+#define DFLASH_GEMM_CHUNKS_PER_STAGE 4
 #endif
 constexpr int kGemmChunksPerStage = DFLASH_GEMM_CHUNKS_PER_STAGE;
 
@@ -234,7 +233,7 @@ __device__ void finish_kv(const GemmParams& p, int o, int c, float* smem_f) {
         const int b = tok / kBlock;
         const int pos = (j < n ? p.pos_snapshot[b] : 0) + (tok - b * kBlock);
         float sn, cs;
-        sincosf(rope_angle(pos, p.rope.hi[fi], p.rope.lo[fi]), &sn, &cs);
+        rope_sincos(pos, p.rope.hi[fi], p.rope.lo[fi], &sn, &cs);
         const float partner = d < half ? kbuf[j * 128 + et + half] : kbuf[j * 128 + et - half];
         val[j] = d < half ? val[j] * cs - partner * sn : val[j] * cs + partner * sn;
       }

@@ -18,6 +18,13 @@ constexpr int kMaxCtxLayers = 8;
 constexpr int kMaxTokens = 512;     // batch * 16
 constexpr int kMaxViews = 4;
 
+// Projection GEMM CTAs resident per SM; their shared-memory budget follows.
+#ifndef DFLASH_GEMM_CTAS_PER_SM
+#define DFLASH_GEMM_CTAS_PER_SM 1
+#endif
+constexpr int kGemmCtasPerSm = DFLASH_GEMM_CTAS_PER_SM;
+constexpr int kGemmSmemBudget = (kGemmCtasPerSm == 1 ? 220 : 110) * 1024;
+
 // Split-K / split-KV plan for one set of shapes on one device.  The workspace
 // layout and every launch derive from the same plan, so they always agree.
 struct Plan {
