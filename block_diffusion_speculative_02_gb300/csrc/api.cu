@@ -95,7 +95,7 @@ int make_plan(const dflash_dims& d, Plan* p) {
     const int by_len = (d.max_ctx + 4095) / 4096;
     if (s < by_len) s = by_len;
     if (s > pages) s = pages;
-    if (s > 64) s = 64;  // the split merge keeps one split per lane, two per lane at most
+    if (s > kMaxAttSplits) s = kMaxAttSplits;  // the split merge stages at most 64 splits
     if (s < 1) s = 1;
     q.att_splits = s;
   }

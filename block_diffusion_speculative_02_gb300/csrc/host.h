@@ -17,6 +17,7 @@ constexpr int kBlock = 16;          // staged token + 15 mask positions
 constexpr int kMaxCtxLayers = 8;
 constexpr int kMaxTokens = 512;     // batch * 16
 constexpr int kMaxViews = 4;
+constexpr int kMaxAttSplits = 64;
 
 // Projection GEMM CTAs resident per SM; their shared-memory budget follows.
 #ifndef DFLASH_GEMM_CTAS_PER_SM
