@@ -49,6 +49,9 @@ def parse_args(argv=None):
                     help="extra steps after the timed region with events around every call")
     ap.add_argument("--sets", type=int, default=0,
                     help="rotating input sets (0: enough to exceed twice the L2 size)")
+    ap.add_argument("--serial", action="store_true",
+                    help="queue verify and the projection on one stream instead of running "
+                         "them side by side on disjoint SM budgets")
     return ap.parse_args(argv)
 
 
@@ -395,28 +398,49 @@ def main(argv=None):
     __graft_entry__.build()
     world, rank = init_dist("nccl")
     import block_diffusion_speculative_02_gb300 as dfl
-    from block_diffusion_speculative_02_gb300.cycle import run_cycle
+    from block_diffusion_speculative_02_gb300.cycle import run_cycle, side_stream
 
     kv_bytes_per_set = 2 * cfg.n_kv_heads * cfg.head_dim * 2 * (
         cfg.batch * (cfg.ctx_len or cfg.ctx_len_range[1]) + 32)
     n_sets = args.sets or max(1, min(16, math.ceil(2 * L2_BYTES / max(1, kv_bytes_per_set))))
     dims, w, states, accepts, ws, lens = build_workload(cfg, n_sets)
     stream = torch.cuda.current_stream()
+    concurrent = not args.serial
+    if concurrent:
+        # verify on this stream, the projection on a side stream, each on its
+        # own share of the SMs; joined before the crop
+        verify_sms, project_sms = dfl.dflash_cycle_sm_split(dims)
+        side = side_stream(stream.device)
+        fork, join = torch.cuda.Event(), torch.cuda.Event()
+    else:
+        verify_sms = project_sms = 0
+        side = stream
+    dims_v = dfl.with_sm_budget(dims, verify_sms)
+    dims_p = dfl.with_sm_budget(dims, project_sms)
 
     def step(i, ev=None):
         st = states[i % n_sets]
+        if concurrent:
+            fork.record(stream)
+            side.wait_event(fork)
         if ev is not None:
             ev[0].record(stream)
-        dfl.dflash_verify_accept(dims, st.verify_hidden, w.w_lm, st.block_ids, st.len_before,
+        dfl.dflash_verify_accept(dims_v, st.verify_hidden, w.w_lm, st.block_ids, st.len_before,
                                  st.posterior, st.accept_len, st.next_staged, st.commit_len,
-                                 st.out_tokens, ws)
+                                 st.out_tokens, ws, stream)
         if ev is not None:
             ev[1].record(stream)
-        dfl.dflash_ctx_project(dims, st.layer_hidden, w.w_fc, w.hidden_norm_w, w.w_k, w.w_v,
-                               w.k_norm_w, st.write_pos, st.draft_cache, ws)
-        dfl.dflash_kv_crop([st.target_view, st.draft_cache], st.commit_len, dims.batch, ws)
+        dfl.dflash_ctx_project(dims_p, st.layer_hidden, w.w_fc, w.hidden_norm_w, w.w_k, w.w_v,
+                               w.k_norm_w, st.write_pos, st.draft_cache, ws, side)
+        if concurrent:
+            join.record(side)
+            stream.wait_event(join)
+        if ev is not None:
+            ev[2].record(stream)
+        dfl.dflash_kv_crop([st.target_view, st.draft_cache], st.commit_len, dims.batch, ws,
+                           stream)
         dfl.dflash_block_attention(dims, st.q_blk, st.k_blk, st.v_blk, st.draft_cache,
-                                   1.0 / math.sqrt(cfg.head_dim), st.attn_out, ws)
+                                   1.0 / math.sqrt(cfg.head_dim), st.attn_out, ws, stream)
 
     for i in range(args.warmup):
         step(i)
@@ -429,7 +453,7 @@ def main(argv=None):
     if rank == 0:
         sampler.start()
         time.sleep(0.3)
-    lm_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    lm_events = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
                  for _ in range(args.steps)]
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -444,7 +468,8 @@ def main(argv=None):
     clocks = sampler.stop() if rank == 0 else None
     elapsed_s = e0.elapsed_time(e1) / 1e3
     max_s = max_over_ranks(elapsed_s, device="cuda")
-    lm_ms = statistics.mean(a.elapsed_time(b) for a, b in lm_events)
+    lm_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in lm_events)
+    phase_ms = statistics.mean(a.elapsed_time(c) for a, _, c in lm_events)
     status = dfl.dflash_read_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {status:#x} after the timed region")
@@ -488,7 +513,7 @@ def main(argv=None):
         torch.cuda.synchronize()
         breakdown = {n: 1e3 * statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
                      for j, n in enumerate(names)}
-        breakdown["unit"] = "us per call (events between calls)"
+        breakdown["unit"] = "us per call (one stream, events between calls)"
 
     # ---- end to end: host buffers in, results out, every step ----
     e2e = None
@@ -510,7 +535,7 @@ def main(argv=None):
         for _ in range(args.e2e_steps):
             for d_, h_ in zip(ins, host_in):
                 d_.copy_(h_, non_blocking=True)
-            run_cycle(dims, w, st0, ws, 1.0 / math.sqrt(cfg.head_dim))
+            run_cycle(dims, w, st0, ws, 1.0 / math.sqrt(cfg.head_dim), concurrent=concurrent)
             for h_, d_ in zip(host_out, outs):
                 h_.copy_(d_, non_blocking=True)
             torch.cuda.current_stream().synchronize()
@@ -535,12 +560,18 @@ def main(argv=None):
             "config": {"workload": cfg.name, "batch": cfg.batch, "block": 16,
                        "hidden": cfg.hidden, "vocab": cfg.vocab, "context": int(lens.max()),
                        "ctx_layers": cfg.n_ctx_layers, "drafter_layers": 1,
-                       "l2": f"{n_sets} rotating input sets (> L2)", "graph": False},
+                       "l2": f"{n_sets} rotating input sets (> L2)", "graph": False,
+                       "verify_project": ("side by side, SM budgets %d + %d"
+                                          % (verify_sms, project_sms)) if concurrent
+                       else "one stream"},
             "committed_tokens_per_s": value * cfg.batch * (1 + acc_mean),
             "tokens_per_cycle": cfg.batch * (1 + acc_mean),
             "acceptance_rate": acc_mean / 15.0,
             "cycle_gbs": cycle_gbs, "cycle_roofline_frac": cycle_gbs / peak,
             "algorithmic_bytes_per_cycle": bytes_,
+            "verify_project_phase": {
+                "us": 1e3 * phase_ms,
+                "gbs": (bytes_["lm_head"] + bytes_["ctx_project"]) / (phase_ms / 1e3) / 1e9},
             "roofline": {"bound": "hbm", "kernel": "lmhead_argmax_accept", "achieved": lm_gbs,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": lm_gbs / peak, "traffic": traffic,

@@ -7,6 +7,6 @@ bench call.
 """
 from . import dflash  # noqa: F401
 from .dflash import (DFlashError, Dims, KVView, alloc_workspace, dflash_block_attention,  # noqa
-                     dflash_ctx_project, dflash_kv_crop, dflash_read_status,
-                     dflash_verify_accept, dflash_workspace_bytes, dflash_workspace_init,
-                     load_library, make_dims)
+                     dflash_ctx_project, dflash_cycle_sm_split, dflash_kv_crop,
+                     dflash_read_status, dflash_verify_accept, dflash_workspace_bytes,
+                     dflash_workspace_init, load_library, make_dims, with_sm_budget)

@@ -51,7 +51,7 @@ int check_dims(const dflash_dims* d) {
   if ((d->n_kv_heads * d->head_dim) % 128) return DFLASH_E_UNSUPPORTED;
   if (d->vocab < 1) return DFLASH_E_ARG;
   if (d->n_ctx_layers < 1 || d->n_ctx_layers > kMaxCtxLayers) return DFLASH_E_UNSUPPORTED;
-  if (d->max_ctx < 0) return DFLASH_E_ARG;
+  if (d->max_ctx < 0 || d->sm_budget < 0) return DFLASH_E_ARG;
   if (!(d->rms_eps >= 0.0f) || !(d->rope_theta > 0.0f)) return DFLASH_E_ARG;
   return DFLASH_OK;
 }
@@ -63,29 +63,20 @@ int current_num_sms() {
   return n;
 }
 
-static int pick_splits(int units, int k_tiles, int slots) {
-  int s = slots / (units > 0 ? units : 1);
-  if (s < 1) s = 1;
-  if (s > k_tiles) s = k_tiles;
-  return s;
-}
-
 int make_plan(const dflash_dims& d, Plan* p) {
   int rc = check_dims(&d);
   if (rc) return rc;
   Plan q = {};
   q.num_sms = current_num_sms();
   if (q.num_sms <= 0) return DFLASH_E_CUDA;
+  q.budget_sms = d.sm_budget > 0 && d.sm_budget < q.num_sms ? d.sm_budget : q.num_sms;
   q.ntok = d.batch * kBlock;
-  const int slots = kGemmCtasPerSm * q.num_sms;
   q.fc_out_tiles = d.hidden / 128;
   q.fc_k_tiles = d.n_ctx_layers * d.hidden / 64;
   q.fc_tok_chunks = (q.ntok + 255) / 256;
-  q.fc_splits = pick_splits(q.fc_out_tiles * q.fc_tok_chunks, q.fc_k_tiles, slots);
   q.kv_out_tiles = 2 * d.n_kv_heads * d.head_dim / 128;
   q.kv_k_tiles = d.hidden / 64;
   q.kv_tok_chunks = (q.ntok + 127) / 128;
-  q.kv_splits = pick_splits(q.kv_out_tiles * q.kv_tok_chunks, q.kv_k_tiles, slots);
   q.att_rows = (d.n_q_heads / d.n_kv_heads) * kBlock;
   {
     // enough (sequence, KV head, split) CTAs for two per SM, and no split
@@ -174,6 +165,25 @@ extern "C" size_t dflash_workspace_bytes(const dflash_dims* dims) {
   return p.total;
 }
 
+extern "C" int dflash_cycle_sm_split(const dflash_dims* dims, int32_t* verify_sms,
+                                     int32_t* project_sms) {
+  if (!verify_sms || !project_sms) return DFLASH_E_ARG;
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  const int nsm = current_num_sms();
+  if (nsm < 2) return DFLASH_E_CUDA;
+  const double h = dims->hidden;
+  const double lm = static_cast<double>(dims->vocab) * h;
+  const double proj = dims->n_ctx_layers * h * h +
+                      2.0 * dims->n_kv_heads * dims->head_dim * h;
+  int p = static_cast<int>(std::lround(nsm * proj / (proj + lm)));
+  if (p < 1) p = 1;
+  if (p > nsm - 1) p = nsm - 1;
+  *project_sms = p;
+  *verify_sms = nsm - p;
+  return DFLASH_OK;
+}
+
 extern "C" int dflash_workspace_init(void* ws, size_t ws_bytes, dflash_stream_t stream) {
   if (!ws || ws_bytes < 256) return DFLASH_E_WORKSPACE;
   return cuda_err(cudaMemsetAsync(ws, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream)));
@@ -201,4 +211,4 @@ extern "C" const char* dflash_status_string(int code) {
   }
 }
 
-extern "C" int dflash_version(void) { return 100; }
+extern "C" int dflash_version(void) { return 101; }

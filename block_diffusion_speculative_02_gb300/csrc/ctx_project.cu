@@ -6,14 +6,19 @@
 // projected from them.  "dflash-mlx" (dpshk.com) 块扩散草稿 step 3: the
 // drafter reads the target's multi-layer hidden states.
 //
-// Two kernels on one stream, both "swap-AB" split-K GEMMs on the
+// Two kernels on one stream, both "swap-AB" stream-K GEMMs on the
 // 5th-generation tensor cores (128 output features are the MMA's M, the token
 // rows its N, fp32 accumulators in TMEM, the weight stream staged by a TMA
-// pipeline; memory-bound at small batch, so K is split until every SM streams
-// weights).  Each split CTA adds its partial tile into an fp32 accumulator in
-// the workspace with fire-and-forget atomic adds; the last split CTA of each
-// output tile (atomic ticket, no waiting) reads the finished sums in one round
-// trip, clears them for the next call and finishes the tile:
+// pipeline).  At small batch the GEMMs are bound by the weight stream, so the
+// work is cut into units of (output tile, k-stage) and every CTA of the grid
+// (one per SM of the budget) streams one equal contiguous range of units:
+// all SMs move weights, whatever the tile count.  A CTA's range crosses tile
+// boundaries; each piece ("segment") accumulates in one of two TMEM slots
+// (the epilogue drains one while the MMAs fill the other) and is added into
+// an fp32 accumulator in the workspace with fire-and-forget atomic adds.  The
+// CTA that completes a tile's count of contributions (atomic ticket, no
+// waiting) reads the finished sums in one round trip, clears them for the
+// next call and finishes the tile once its own pipeline has drained:
 //  1. fc GEMM   Y = X W_fc^T.  X is never materialised: the k-loop reads
 //     layer floor(k / H) through its own tensor map, which is the
 //     concatenation.  Finisher: g_h * Y stored as a bf16 pair hi + lo
@@ -23,7 +28,7 @@
 //  2. K/V GEMM  [K;V] = [hi;lo] W_{k|v}^T.  Finisher: the RMSNorm scale of Y
 //     (one factor per token row, so it commutes with the GEMM), per-head
 //     RMSNorm and RoPE for K, bf16 store into the cache rows.
-// The order of the fp32 additions across splits is not fixed, so results can
+// The order of the fp32 additions across CTAs is not fixed, so results can
 // differ between runs by fp32 rounding (well inside the bf16 outputs' ulp).
 #include "common.cuh"
 #include "host.h"
@@ -34,6 +39,7 @@ namespace {
 constexpr int kGemmThreads = 192;
 constexpr int kATile = 128 * 128;  // 128 rows x 64 bf16
 constexpr int kMaxGemmStages = 12;
+constexpr int kMaxSegments = 32;   // tiles one CTA may touch
 #ifndef DFLASH_GEMM_CHUNKS_PER_STAGE
 #define DFLASH_GEMM_CHUNKS_PER_STAGE 4
 #endif
@@ -46,7 +52,8 @@ struct LayerMaps {
 struct GemmParams {
   int mode;          // kModeFc or kModeKv (selects the finisher)
   int k_tiles;       // K / 64
-  int splits;
+  int k_stages;      // ceil(k_tiles / kb): work units per tile
+  int n_units;       // out_tiles * n_chunks * k_stages
   int out_tiles;     // output features / 128
   int a_split;       // tiles >= a_split read the second weight map
   int layer_cols;    // columns per B map (fc: H); k-tile kt reads map (kt*64)/layer_cols
@@ -59,8 +66,8 @@ struct GemmParams {
   int n_stages, stage_bytes, tmem_cols;
   int kb;            // 64-column K chunks per pipeline stage
   int b_chunk;       // bytes of the token tile of one chunk (1024-aligned)
-  float* acc;        // [n_tok][ld_out] split-K accumulator, zero between calls
-  uint32_t* tickets; // [out_tiles * n_chunks], zero between calls
+  float* acc;        // [n_tok][ld_out] fp32 accumulator, zero between calls
+  uint32_t* tickets; // [n_chunks * out_tiles] contributions so far, zero between calls
   uint32_t* status;
   // shared by both finishers
   int hidden, fc_out_tiles;
@@ -266,40 +273,64 @@ __device__ void finish_kv(const GemmParams& p, int o, int c, float* smem_f) {
   }
 }
 
+// Unit u = (tile T, k-stage ks) with u = T * k_stages + ks; tile T covers
+// output features (T % out_tiles) * 128 .. +127 for token chunk T / out_tiles.
+// CTA i of G streams units [U*i/G, U*(i+1)/G): every CTA moves the same
+// number of weight bytes whatever the tile count.
+__device__ __forceinline__ int unit_begin(const GemmParams& p, int i) {
+  return static_cast<int>(static_cast<long long>(p.n_units) * i / gridDim.x);
+}
+
+// The CTA whose unit range holds unit u.
+__device__ __forceinline__ int unit_owner(const GemmParams& p, int u) {
+  return static_cast<int>((static_cast<long long>(gridDim.x) * (u + 1) - 1) / p.n_units);
+}
+
+// Number of CTAs that add partial sums into tile T.
+__device__ __forceinline__ uint32_t tile_contributors(const GemmParams& p, int T) {
+  const int first = T * p.k_stages;
+  const int last = min(p.n_units, first + p.k_stages) - 1;
+  return static_cast<uint32_t>(unit_owner(p, last) - unit_owner(p, first) + 1);
+}
+
 __global__ void __launch_bounds__(kGemmThreads)
-splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
-                   const __grid_constant__ CUtensorMap tm_a1,
-                   const __grid_constant__ LayerMaps tm_b, const GemmParams p) {
+streamk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
+                    const __grid_constant__ CUtensorMap tm_a1,
+                    const __grid_constant__ LayerMaps tm_b, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.n_stages * p.stage_bytes);
   uint64_t* empty = full + p.n_stages;
-  uint64_t* tfull = empty + p.n_stages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull + 1);
+  uint64_t* tfull = empty + p.n_stages;   // [2] accumulator slot ready
+  uint64_t* tempty = tfull + 2;           // [2] accumulator slot drained
+  uint64_t* mdrain = tempty + 2;          // every MMA issued has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdrain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  volatile int* seg_ok = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  volatile int* n_fin = reinterpret_cast<volatile int*>(tmem_slot + 3);
+  int* fin_tiles = reinterpret_cast<int*>(tmem_slot + 4);  // [kMaxSegments]
 
-  int unit = blockIdx.x;
-  const int o = unit % p.out_tiles;
-  unit /= p.out_tiles;
-  const int s = unit % p.splits;
-  const int c = unit / p.splits;
-  const int kt0 = static_cast<int>(static_cast<long long>(s) * p.k_tiles / p.splits);
-  const int kt1 = static_cast<int>(static_cast<long long>(s + 1) * p.k_tiles / p.splits);
+  const int u0 = unit_begin(p, blockIdx.x);
+  const int u1 = unit_begin(p, blockIdx.x + 1);
+  const int KS = p.k_stages;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.n_stages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(tfull, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 128);
+    }
+    mbar_init(mdrain, 1);
     *abort_flag = 0;
-    *last_flag = 0;
+    *n_fin = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, p.tmem_cols);
+    tmem_alloc(tmem_slot, 2 * p.tmem_cols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -312,17 +343,19 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
     if (lane == 0) {
       const uint64_t pol_w = l2_policy_evict_first();
       const uint64_t pol_x = l2_policy_evict_last();
-      const CUtensorMap* ma = o < p.a_split ? &tm_a0 : &tm_a1;
-      const int arow = (o < p.a_split ? o : o - p.a_split) * 128;
-      const uint32_t bytes = kATile + (1 + p.hilo) * p.chunk_rows * 128;
+      const uint32_t bbytes = (1 + p.hilo) * p.chunk_rows * 128;
       uint32_t stage = 0, phase = 0;
       int issued = 0;
-      for (int kt = kt0; kt < kt1; kt += p.kb) {
+      for (int u = u0; u < u1; ++u) {
+        const int T = u / KS, kt = (u - T * KS) * p.kb;
+        const int o = T % p.out_tiles, c = T / p.out_tiles;
+        const CUtensorMap* ma = o < p.a_split ? &tm_a0 : &tm_a1;
+        const int arow = (o < p.a_split ? o : o - p.a_split) * 128;
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) break;
-        const int nck = min(p.kb, kt1 - kt);
+        const int nck = min(p.kb, p.k_tiles - kt);
         uint8_t* a = smem + stage * p.stage_bytes;
         uint8_t* bt = a + p.kb * kATile;
-        mbar_arrive_expect_tx(&full[stage], nck * bytes);
+        mbar_arrive_expect_tx(&full[stage], nck * (kATile + bbytes));
         // the chunks of a stage go out back to back: each weight row is
         // requested as nck * 128 contiguous bytes
         for (int j = 0; j < nck; ++j) {
@@ -342,6 +375,7 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
           phase ^= 1;
         }
       }
+      // no copy may still be landing when the stages are reused by the finisher
       for (int st = 0; st < p.n_stages && st < issued; ++st) {
         const int last = st + ((issued - 1 - st) / p.n_stages) * p.n_stages;
         mbar_wait_drain(&full[st], static_cast<uint32_t>((last / p.n_stages) & 1), p.status);
@@ -352,48 +386,75 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
       const uint32_t base = smem_u32(smem);
       const uint32_t idesc = umma_idesc_bf16(128, p.mma_n);
       uint32_t stage = 0, phase = 0;
+      int seg = 0;
+      uint32_t acc = 0;
       bool first = true;
-      for (int kt = kt0; kt < kt1; kt += p.kb) {
+      for (int u = u0; u < u1; ++u) {
+        const int ks = u % KS;
+        if (u == u0 || ks == 0) {  // a segment (this CTA's part of one tile) starts
+          const int slot = seg & 1;
+          if (seg >= 2 &&
+              !mbar_wait(&tempty[slot], static_cast<uint32_t>(((seg >> 1) - 1) & 1), abort_flag,
+                         p.status))
+            break;
+          tc_fence_after();
+          acc = tmem_base + slot * p.tmem_cols;
+          first = true;
+        }
         if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) break;
         tc_fence_after();
-        const int nck = min(p.kb, kt1 - kt);
+        const int nck = min(p.kb, p.k_tiles - ks * p.kb);
         const uint32_t a_addr = base + stage * p.stage_bytes;
         for (int j = 0; j < nck; ++j) {
           const uint64_t adesc = umma_sdesc_sw128(a_addr + j * kATile);
           const uint64_t bdesc = umma_sdesc_sw128(a_addr + p.kb * kATile + j * p.b_chunk);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            umma_bf16(tmem_base, adesc + 2 * kk, bdesc + 2 * kk, idesc, first ? 0u : 1u);
+            umma_bf16(acc, adesc + 2 * kk, bdesc + 2 * kk, idesc, first ? 0u : 1u);
             first = false;
           }
         }
         umma_commit(&empty[stage]);
+        if (u == u1 - 1 || ks == KS - 1) {  // the segment ends: hand the slot over
+          umma_commit(&tfull[seg & 1]);
+          ++seg;
+        }
         if (++stage == static_cast<uint32_t>(p.n_stages)) {
           stage = 0;
           phase ^= 1;
         }
       }
-      umma_commit(tfull);  // also the drain point for the MMAs
-      mbar_wait_drain(tfull, 0, p.status);
+      umma_commit(mdrain);
+      mbar_wait_drain(mdrain, 0, p.status);
     }
   } else {
+    const int et = threadIdx.x - 64;
     if (p.mode == kModeFc && blockIdx.x == 0) {
-      for (int b = threadIdx.x - 64; b < p.batch; b += 128) reserve_block_rows(p, b);
+      for (int b = et; b < p.batch; b += 128) reserve_block_rows(p, b);
     }
     // epilogue: TMEM lane = output feature, column = token (hi, then lo)
     const int q = warp & 3;
-    const bool ok = mbar_wait(tfull, 0, abort_flag, p.status);
-    if (__all_sync(0xffffffffu, ok) && kt1 > kt0) {
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    int seg = 0;
+    for (int u = u0; u < u1; ++seg) {
+      const int T = u / KS;
+      const int o = T % p.out_tiles, c = T / p.out_tiles;
+      const int slot = seg & 1;
+      const bool ok = mbar_wait(&tfull[slot], static_cast<uint32_t>((seg >> 1) & 1), abort_flag,
+                                p.status);
+      named_bar_sync(1, 128);
+      if (et == 0) *seg_ok = ok && !*abort_flag;
+      named_bar_sync(1, 128);
+      if (!*seg_ok) break;  // uniform over the four warps
       tc_fence_after();
-      const int f = o * 128 + q * 32 + lane;
-      const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-      // split-K reduction by fire-and-forget atomic adds at L2: the finisher then
-      // needs one round trip instead of one per split
-      float* dst = p.acc + f;
+      const uint32_t tacc = tmem_base + slot * p.tmem_cols + lane_base;
+      // partial sums go to the fp32 accumulator by fire-and-forget atomic adds
+      // at L2; the tile's finisher then needs one round trip
+      float* dst = p.acc + o * 128 + q * 32 + lane;
       for (int c0 = 0; c0 < p.chunk_rows; c0 += 16) {
         uint32_t v[16], w[16];
-        tmem_ld_32x32b_x16(tmem_base + lane_base + c0, v);
-        if (p.hilo) tmem_ld_32x32b_x16(tmem_base + lane_base + p.chunk_rows + c0, w);
+        tmem_ld_32x32b_x16(tacc + c0, v);
+        if (p.hilo) tmem_ld_32x32b_x16(tacc + p.chunk_rows + c0, w);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -404,51 +465,75 @@ splitk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
         }
       }
       tc_fence_before();
+      mbar_arrive(&tempty[slot]);
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (et == 0 && atomicAdd(p.tickets + T, 1u) == tile_contributors(p, T) - 1u)
+        fin_tiles[(*n_fin)++] = T;  // this CTA completed the tile's sum
+      u = min(u1, (T + 1) * KS);
     }
   }
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, p.tmem_cols);
+    tmem_dealloc(tmem_base, 2 * p.tmem_cols);
   }
-  if (warp >= 2) {
-    // the last split CTA of (output tile, token chunk) reduces and finishes it
+  if (warp >= 2 && *n_fin > 0) {
+    // finish the tiles this CTA completed; the pipeline is drained, so its
+    // shared memory is free for the finisher
     __threadfence();
-    named_bar_sync(1, 128);
-    uint32_t* ticket = p.tickets + o * p.n_chunks + c;
-    if (threadIdx.x == 64) *last_flag = (atomicAdd(ticket, 1u) == static_cast<uint32_t>(p.splits - 1));
-    named_bar_sync(1, 128);
-    if (*last_flag) {
-      __threadfence();
-      // the pipeline is drained: its shared memory is free for the finisher
-      float* scratch = reinterpret_cast<float*>(smem);
+    float* scratch = reinterpret_cast<float*>(smem);
+    const int nf = *n_fin;
+    for (int i = 0; i < nf; ++i) {
+      const int T = fin_tiles[i];
+      const int o = T % p.out_tiles, c = T / p.out_tiles;
       if (p.mode == kModeFc) finish_fc(p, o, c, scratch); else finish_kv(p, o, c, scratch);
-      if (threadIdx.x == 64) *ticket = 0u;
+      named_bar_sync(1, 128);  // scratch is reused by the next tile
+      if (threadIdx.x == 64) p.tickets[T] = 0u;
     }
   }
   griddep_launch_dependents();
 }
 
+// Dynamic shared memory: 1 KB alignment slack, the stages with their full and
+// empty barriers, then tfull[2], tempty[2], mdrain, four words and the
+// finisher list.
+constexpr int kGemmTail = 5 * 8 + 4 * 4 + kMaxSegments * 4;
+
 int gemm_smem(int stage_bytes, int n_stages) {
-  return 1024 + n_stages * (stage_bytes + 16) + 8 + 16;
+  return 1024 + n_stages * (stage_bytes + 16) + kGemmTail;
 }
 
 int setup_gemm(GemmParams& g, int b_rows_per_stage) {
   g.b_chunk = ((b_rows_per_stage * 128 + 1023) / 1024) * 1024;
   // as many 64-column chunks per stage as still leave three stages
   g.kb = kGemmChunksPerStage;
-  while (g.kb > 1 && (kGemmSmemBudget - 1024 - 24) / (g.kb * (kATile + g.b_chunk) + 16) < 3)
+  while (g.kb > 1 &&
+         (kGemmSmemBudget - 1024 - kGemmTail) / (g.kb * (kATile + g.b_chunk) + 16) < 3)
     g.kb >>= 1;
   g.stage_bytes = g.kb * (kATile + g.b_chunk);
-  g.n_stages = (kGemmSmemBudget - 1024 - 24) / (g.stage_bytes + 16);
+  g.n_stages = (kGemmSmemBudget - 1024 - kGemmTail) / (g.stage_bytes + 16);
   if (g.n_stages > kMaxGemmStages) g.n_stages = kMaxGemmStages;
-  if (g.n_stages < 2) {
-    g.n_stages = 2;  // large token chunks: one CTA per SM
-  }
+  if (g.n_stages < 2) g.n_stages = 2;
   int cols = 32;
   while (cols < g.mma_n) cols *= 2;
-  g.tmem_cols = cols;
+  g.tmem_cols = cols;  // two slots of this width are allocated
+  g.k_stages = (g.k_tiles + g.kb - 1) / g.kb;
+  g.n_units = g.out_tiles * g.n_chunks * g.k_stages;
   return gemm_smem(g.stage_bytes, g.n_stages);
+}
+
+// CTAs of a stream-K launch: at most `ctas` (one per SM of the budget), at
+// most one per unit, and enough that no CTA touches more than kMaxSegments
+// tiles.
+int streamk_grid(const GemmParams& g, int ctas) {
+  int grid = ctas < g.n_units ? ctas : g.n_units;
+  while (grid < g.n_units) {
+    const int per = (g.n_units + grid - 1) / grid;
+    if ((per + g.k_stages - 1) / g.k_stages + 1 <= kMaxSegments) break;
+    ++grid;
+  }
+  return grid;
 }
 
 }  // namespace
@@ -514,7 +599,6 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
     GemmParams g = common;
     g.mode = kModeFc;
     g.k_tiles = plan.fc_k_tiles;
-    g.splits = plan.fc_splits;
     g.out_tiles = plan.fc_out_tiles;
     g.a_split = plan.fc_out_tiles;
     g.layer_cols = H;
@@ -537,9 +621,9 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
                                   static_cast<uint64_t>(H) * 2, 64, g.chunk_rows)))
         return rc;
     for (int l = nL; l < kMaxCtxLayers; ++l) lm.m[l] = lm.m[0];
-    if ((rc = set_smem_limit(reinterpret_cast<const void*>(splitk_gemm_kernel), smem))) return rc;
-    const int grid = g.out_tiles * g.splits * g.n_chunks;
-    if ((rc = launch(splitk_gemm_kernel, dim3(grid), dim3(kGemmThreads), smem, st, ta, ta, lm, g)))
+    if ((rc = set_smem_limit(reinterpret_cast<const void*>(streamk_gemm_kernel), smem))) return rc;
+    const int grid = streamk_grid(g, plan.budget_sms);
+    if ((rc = launch(streamk_gemm_kernel, dim3(grid), dim3(kGemmThreads), smem, st, ta, ta, lm, g)))
       return rc;
   }
   // ---- 2. K/V GEMM on [hi; lo]; its finisher scales, normalises, rotates, stores ----
@@ -547,7 +631,6 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
     GemmParams g = common;
     g.mode = kModeKv;
     g.k_tiles = plan.kv_k_tiles;
-    g.splits = plan.kv_splits;
     g.out_tiles = plan.kv_out_tiles;
     g.a_split = plan.kv_out_tiles / 2;
     g.layer_cols = H;
@@ -570,9 +653,9 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
                                 static_cast<uint64_t>(H) * 2, 64, g.chunk_rows)))
       return rc;
     for (int l = 1; l < kMaxCtxLayers; ++l) lm.m[l] = lm.m[0];
-    if ((rc = set_smem_limit(reinterpret_cast<const void*>(splitk_gemm_kernel), smem))) return rc;
-    const int grid = g.out_tiles * g.splits * g.n_chunks;
-    if ((rc = launch(splitk_gemm_kernel, dim3(grid), dim3(kGemmThreads), smem, st, tk, tv, lm, g)))
+    if ((rc = set_smem_limit(reinterpret_cast<const void*>(streamk_gemm_kernel), smem))) return rc;
+    const int grid = streamk_grid(g, plan.budget_sms);
+    if ((rc = launch(streamk_gemm_kernel, dim3(grid), dim3(kGemmThreads), smem, st, tk, tv, lm, g)))
       return rc;
   }
   return DFLASH_OK;

@@ -19,27 +19,23 @@ constexpr int kMaxTokens = 512;     // batch * 16
 constexpr int kMaxViews = 4;
 constexpr int kMaxAttSplits = 64;
 
-// Projection GEMM CTAs resident per SM; their shared-memory budget follows.
-#ifndef DFLASH_GEMM_CTAS_PER_SM
-#define DFLASH_GEMM_CTAS_PER_SM 1
-#endif
-constexpr int kGemmCtasPerSm = DFLASH_GEMM_CTAS_PER_SM;
-constexpr int kGemmSmemBudget = (kGemmCtasPerSm == 1 ? 220 : 110) * 1024;
+// Shared memory of one projection GEMM CTA (one CTA per SM).
+constexpr int kGemmSmemBudget = 220 * 1024;
 
-// Split-K / split-KV plan for one set of shapes on one device.  The workspace
-// layout and every launch derive from the same plan, so they always agree.
+// Launch plan for one set of shapes on one device.  The workspace layout and
+// every launch derive from the same plan, so they always agree; the layout
+// depends on the device only, never on dflash_dims::sm_budget.
 struct Plan {
-  int num_sms;
+  int num_sms;          // SMs of the device
+  int budget_sms;       // SMs the LM head / projection grids may occupy
   int ntok;             // batch * 16
   // context projection
   int fc_out_tiles;     // hidden / 128
   int fc_k_tiles;       // nL * hidden / 64
   int fc_tok_chunks;    // ceil(ntok / 256)
-  int fc_splits;
   int kv_out_tiles;     // 2 * Hkv * D / 128
   int kv_k_tiles;       // hidden / 64
   int kv_tok_chunks;    // ceil(ntok / 128)  (hi + lo columns per chunk)
-  int kv_splits;
   // block attention
   int att_rows;         // (Hq / Hkv) * 16 query rows per KV head
   int att_splits;

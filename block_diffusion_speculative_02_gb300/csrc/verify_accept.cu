@@ -396,7 +396,7 @@ extern "C" int dflash_verify_accept(const dflash_dims* dims, const void* hidden,
   const int smem = p.n_stages * (p.stage_bytes + 16) + fixed;
   if ((rc = set_smem_limit(reinterpret_cast<const void*>(lmhead_argmax_accept_kernel), smem)))
     return rc;
-  const int grid = plan.num_sms < p.n_units ? plan.num_sms : p.n_units;
+  const int grid = plan.budget_sms < p.n_units ? plan.budget_sms : p.n_units;
   return launch(lmhead_argmax_accept_kernel, dim3(grid), dim3(kThreads), smem,
                 reinterpret_cast<cudaStream_t>(stream), tm_w, tm_w8, tm_x, p);
 }
@@ -515,7 +515,7 @@ extern "C" int dflash_verify_accept_noalloc(const dflash_dims* dims, const void*
   const int smem = p.n_stages * (p.stage_bytes + 16) + fixed;
   if ((rc = set_smem_limit(reinterpret_cast<const void*>(lmhead_argmax_accept_kernel), smem)))
     return rc;
-  const int grid = plan.num_sms < p.n_units ? plan.num_sms : p.n_units;
+  const int grid = plan.budget_sms < p.n_units ? plan.budget_sms : p.n_units;
   return launch(lmhead_argmax_accept_kernel, dim3(grid), dim3(kThreads), smem, st, tm_w, tm_w8,
                 tm_x, p);
 }

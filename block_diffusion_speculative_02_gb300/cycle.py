@@ -7,6 +7,12 @@ drafter's context K/V, crop the target and drafter caches to the committed
 length, then run the drafter's dual-source block attention for the next
 block.  This module only holds device buffers and issues the calls; every
 step runs in the CUDA library.
+
+Verification and the projection do not depend on each other (the projection
+reads the target's hidden states and the drafter's write position, not the
+acceptance), so by default they run side by side: verify on the caller's
+stream, the projection on a side stream, each on its own share of the SMs
+(``dflash_cycle_sm_split``), joined before the crop.
 """
 from __future__ import annotations
 
@@ -16,8 +22,20 @@ from typing import List, Optional
 
 import torch
 
-from .dflash import (Dims, KVView, dflash_block_attention, dflash_ctx_project, dflash_kv_crop,
-                     dflash_verify_accept)
+from .dflash import (Dims, KVView, dflash_block_attention, dflash_ctx_project,
+                     dflash_cycle_sm_split, dflash_kv_crop, dflash_verify_accept, with_sm_budget)
+
+_side_streams = {}
+
+
+def side_stream(device) -> torch.cuda.Stream:
+    """The side stream (one per device) that carries the projection."""
+    idx = torch.device(device).index
+    if idx is None:
+        idx = torch.cuda.current_device()
+    if idx not in _side_streams:
+        _side_streams[idx] = torch.cuda.Stream(device=idx)
+    return _side_streams[idx]
 
 
 @dataclass
@@ -52,15 +70,35 @@ class CycleState:
 
 
 def run_cycle(dims: Dims, w: CycleWeights, st: CycleState, ws: torch.Tensor,
-              scale: Optional[float] = None, stream=None):
-    """Issue one cycle on the current (or given) stream."""
+              scale: Optional[float] = None, stream=None, concurrent: bool = True):
+    """Issue one cycle on the current (or given) stream.
+
+    With ``concurrent`` the verification and the projection run on disjoint
+    SM budgets on two streams; otherwise all four calls queue on one stream.
+    """
     if scale is None:
         scale = 1.0 / math.sqrt(dims.head_dim)
-    dflash_verify_accept(dims, st.verify_hidden, w.w_lm, st.block_ids, st.len_before,
+    main = torch.cuda.current_stream() if stream is None else stream
+    if concurrent:
+        verify_sms, project_sms = dflash_cycle_sm_split(dims)
+        dims_v = with_sm_budget(dims, verify_sms)
+        dims_p = with_sm_budget(dims, project_sms)
+        side = side_stream(st.verify_hidden.device)
+        fork = torch.cuda.Event()
+        fork.record(main)
+        side.wait_event(fork)
+    else:
+        dims_v = dims_p = dims
+        side = main
+    dflash_verify_accept(dims_v, st.verify_hidden, w.w_lm, st.block_ids, st.len_before,
                          st.posterior, st.accept_len, st.next_staged, st.commit_len,
-                         st.out_tokens, ws, stream)
-    dflash_ctx_project(dims, st.layer_hidden, w.w_fc, w.hidden_norm_w, w.w_k, w.w_v, w.k_norm_w,
-                       st.write_pos, st.draft_cache, ws, stream)
-    dflash_kv_crop([st.target_view, st.draft_cache], st.commit_len, dims.batch, ws, stream)
+                         st.out_tokens, ws, main)
+    dflash_ctx_project(dims_p, st.layer_hidden, w.w_fc, w.hidden_norm_w, w.w_k, w.w_v,
+                       w.k_norm_w, st.write_pos, st.draft_cache, ws, side)
+    if concurrent:
+        join = torch.cuda.Event()
+        join.record(side)
+        main.wait_event(join)
+    dflash_kv_crop([st.target_view, st.draft_cache], st.commit_len, dims.batch, ws, main)
     dflash_block_attention(dims, st.q_blk, st.k_blk, st.v_blk, st.draft_cache, scale,
-                           st.attn_out, ws, stream)
+                           st.attn_out, ws, main)

@@ -34,7 +34,7 @@ STATUS_BITS = {
 EXPORTED = ["dflash_workspace_bytes", "dflash_workspace_init", "dflash_ctx_project",
             "dflash_block_attention", "dflash_verify_accept", "dflash_kv_crop",
             "dflash_read_status", "dflash_status_string", "dflash_version",
-            "dflash_verify_accept_noalloc"]
+            "dflash_verify_accept_noalloc", "dflash_cycle_sm_split"]
 
 
 class DFlashError(RuntimeError):
@@ -49,7 +49,7 @@ class Dims(ctypes.Structure):
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("vocab", ctypes.c_int32), ("n_ctx_layers", ctypes.c_int32),
                 ("max_ctx", ctypes.c_int32), ("rope_theta", ctypes.c_float),
-                ("rms_eps", ctypes.c_float)]
+                ("rms_eps", ctypes.c_float), ("sm_budget", ctypes.c_int32)]
 
 
 class KVViewC(ctypes.Structure):
@@ -98,6 +98,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_status_string.argtypes = [ctypes.c_int]
     lib.dflash_version.restype = ctypes.c_int
     lib.dflash_version.argtypes = []
+    lib.dflash_cycle_sm_split.restype = ctypes.c_int
+    lib.dflash_cycle_sm_split.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(i32),
+                                          ctypes.POINTER(i32)]
     _lib = lib
     return lib
 
@@ -129,9 +132,24 @@ def _dev(t: Optional[torch.Tensor], dtype=None, name="tensor") -> Optional[int]:
 
 
 def make_dims(batch, hidden, n_q_heads, n_kv_heads, head_dim, vocab, n_ctx_layers, max_ctx,
-              rope_theta=1.0e6, rms_eps=1.0e-6, block=16) -> Dims:
+              rope_theta=1.0e6, rms_eps=1.0e-6, block=16, sm_budget=0) -> Dims:
     return Dims(batch, block, hidden, n_q_heads, n_kv_heads, head_dim, vocab, n_ctx_layers,
-                max_ctx, rope_theta, rms_eps)
+                max_ctx, rope_theta, rms_eps, sm_budget)
+
+
+def with_sm_budget(dims: Dims, sm_budget: int) -> Dims:
+    """A copy of ``dims`` whose LM-head / projection grids use at most ``sm_budget`` SMs."""
+    d = Dims.from_buffer_copy(dims)
+    d.sm_budget = int(sm_budget)
+    return d
+
+
+def dflash_cycle_sm_split(dims: Dims):
+    """(verify_sms, project_sms): SM budgets for running verify and the projection concurrently."""
+    v, p = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(load_library().dflash_cycle_sm_split(ctypes.byref(dims), ctypes.byref(v),
+                                                ctypes.byref(p)), "dflash_cycle_sm_split")
+    return int(v.value), int(p.value)
 
 
 @dataclass

@@ -88,6 +88,13 @@ typedef struct {
                             attention split-K scratch                       */
   float rope_theta;      /* RoPE base (Qwen3: 1e6)                          */
   float rms_eps;         /* RMSNorm epsilon (1e-6)                          */
+  int32_t sm_budget;     /* SMs that dflash_verify_accept and
+                            dflash_ctx_project may occupy; 0 = all.  Two
+                            calls given disjoint budgets (summing to at
+                            most the SM count, see dflash_cycle_sm_split)
+                            run side by side on two streams instead of
+                            queueing for SMs.  The other calls ignore it,
+                            and it does not change the workspace size.     */
 } dflash_dims;
 
 /* A KV cache as the kernels see it.  Both layouts are head-major, so that the
@@ -117,6 +124,14 @@ DFLASH_API size_t dflash_workspace_bytes(const dflash_dims* dims);
 
 /* Zero a workspace (cudaMemsetAsync on `stream`). */
 DFLASH_API int dflash_workspace_init(void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/* Budgets (dflash_dims::sm_budget) for running dflash_verify_accept and
+ * dflash_ctx_project side by side on two streams.  Both are bound by the
+ * weights they stream (W_lm; W_fc, W_k, W_v), so the device's SMs are split
+ * in proportion to those bytes, each side getting at least one SM.  Writes
+ * the two budgets (summing to the SM count of the current device). */
+DFLASH_API int dflash_cycle_sm_split(const dflash_dims* dims, int32_t* verify_sms,
+                                     int32_t* project_sms);
 
 /*
  * a1 — context projection ([P1] §4 and §2; [P2] 块扩散草稿 step 3).
@@ -231,7 +246,7 @@ DFLASH_API int dflash_read_status(void* ws, uint32_t* host_status, int clear, df
 /* Text for a return code. */
 DFLASH_API const char* dflash_status_string(int code);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor): 101. */
 DFLASH_API int dflash_version(void);
 
 #ifdef __cplusplus

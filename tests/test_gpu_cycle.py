@@ -19,8 +19,9 @@ from tests.gpu_helpers import assert_close_bf16, check_verify, dev_bf16, dev_i32
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("concurrent", [True, False])
 @pytest.mark.parametrize("paged", [False, True])
-def test_three_cycles_carry_state(paged):
+def test_three_cycles_carry_state(paged, concurrent):
     import block_diffusion_speculative_02_gb300 as dfl
     from block_diffusion_speculative_02_gb300.cycle import CycleState, CycleWeights, run_cycle
 
@@ -95,7 +96,7 @@ def test_three_cycles_carry_state(paged):
             next_staged=torch.zeros(B, dtype=torch.int32, device="cuda"), commit_len=commit,
             out_tokens=out_tokens,
             attn_out=torch.zeros((B, 16, Hq, D), dtype=torch.bfloat16, device="cuda"))
-        run_cycle(dims, w, st, ws)
+        run_cycle(dims, w, st, ws, concurrent=concurrent)
         torch.cuda.synchronize()
         assert dfl.dflash_read_status(ws) == 0
         got = {"posterior": st.posterior.cpu().numpy(), "accept": st.accept_len.cpu().numpy(),

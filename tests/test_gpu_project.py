@@ -32,7 +32,7 @@ def make_inputs(seed, B, H, nL, Hkv, D):
 
 
 def run_project(layers, w_fc, gh, wk, wv, gk, write_pos, Hq, Hkv, D, theta, paged=False,
-                capacity=None, alias=False, seed=0, pool_slack=8):
+                capacity=None, alias=False, seed=0, pool_slack=8, sm_budget=0):
     dfl = _dfl()
     B = len(write_pos)
     H = w_fc.shape[0]
@@ -41,6 +41,7 @@ def run_project(layers, w_fc, gh, wk, wv, gk, write_pos, Hq, Hkv, D, theta, page
     max_ctx = int(write_pos.max()) + 16
     dims = dfl.make_dims(B, H, Hq, Hkv, D, 1000, nL, max_ctx, rope_theta=theta)
     ws = dfl.alloc_workspace(dims)
+    dims.sm_budget = sm_budget          # grid size only: the workspace does not depend on it
     rng = np.random.default_rng(seed)
     lay = None
     if paged:
@@ -85,12 +86,12 @@ def gather_rows(view, lay, write_pos, Hkv, D):
 
 
 def check_project(layers, w_fc, gh, wk, wv, gk, write_pos, Hq, Hkv, D, theta=1e6, paged=False,
-                  alias=False):
+                  alias=False, sm_budget=0):
     B = len(write_pos)
     pos = np.repeat(np.asarray(write_pos), 16) + np.tile(np.arange(16), B)
     ref = ref_project(layers, w_fc, gh, wk, wv, gk, pos, Hkv, D, theta, 1e-6)
     view, lay, status = run_project(layers, w_fc, gh, wk, wv, gk, write_pos, Hq, Hkv, D, theta,
-                                    paged=paged, alias=alias)
+                                    paged=paged, alias=alias, sm_budget=sm_budget)
     assert status == 0, status
     k, v = gather_rows(view, lay, write_pos, Hkv, D)
     ek = assert_close_bf16(k, ref["k"])
@@ -119,6 +120,31 @@ def test_project_tiny(norms):
 def test_project_contiguous(B, H, nL, Hkv, D, pos):
     layers, w_fc, gh, wk, wv, gk = make_inputs(B + H, B, H, nL, Hkv, D)
     check_project(layers, w_fc, gh, wk, wv, gk, pos, 4 * Hkv, Hkv, D)
+
+
+@pytest.mark.parametrize("sm_budget", [1, 3, 20])
+@pytest.mark.parametrize("B,H,nL,Hkv,D,pos", [
+    (17, 256, 2, 2, 64, list(range(0, 17 * 5, 5))),    # two 256-row token chunks
+    (2, 1024, 5, 8, 128, [2048, 7]),
+])
+def test_project_small_sm_budget(sm_budget, B, H, nL, Hkv, D, pos):
+    """Few CTAs: each streams a long run of (tile, k-stage) units crossing many
+    tile boundaries, so several CTAs add into every tile."""
+    layers, w_fc, gh, wk, wv, gk = make_inputs(B + H + sm_budget, B, H, nL, Hkv, D)
+    check_project(layers, w_fc, gh, wk, wv, gk, pos, 4 * Hkv, Hkv, D, sm_budget=sm_budget)
+
+
+def test_cycle_sm_split():
+    dfl = _dfl()
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    cfg = CONFIG_BY_NAME["qwen3_8b_b1"]
+    dims = dfl.make_dims(1, cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.vocab,
+                         cfg.n_ctx_layers, 8192)
+    v, p = dfl.dflash_cycle_sm_split(dims)
+    assert v + p == nsm and p >= 1 and v >= 1
+    proj = cfg.n_ctx_layers * cfg.hidden ** 2 + 2 * cfg.n_kv_heads * cfg.head_dim * cfg.hidden
+    share = proj / (proj + cfg.vocab * cfg.hidden)
+    assert abs(p - nsm * share) <= 0.5 + 1e-9
 
 
 def test_project_paged_reserves_pages():
