@@ -19,6 +19,8 @@
 // queries/keys is applied in registers at positions L + i.  The split that
 // owns the tail also folds in the 16 block keys.  Partial (O, max, sum) go to
 // the workspace and a second kernel merges the splits by log-sum-exp.
+#include <type_traits>
+
 #include "common.cuh"
 #include "host.h"
 
@@ -88,10 +90,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // Byte address of (row, 16-byte chunk) in a tile stored as 64-column halves of
-// `half_rows` rows x 128 B with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t swz(uint32_t base, int half_rows, int row, int chunk) {
-  return base + static_cast<uint32_t>((chunk >> 3) * half_rows * 128 + row * 128 +
+// kChunk rows x 128 B with the 128-byte swizzle.  The row stride of a half is
+// a compile-time constant, so the addresses of a fully unrolled chunk fold to
+// a per-lane base plus immediates.
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
+  return base + static_cast<uint32_t>((chunk >> 3) * kChunk * 128 + row * 128 +
                                       (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+// 2^x on the special-function unit (one instruction; -inf gives +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 template <int D>
@@ -99,15 +110,20 @@ struct Cfg {
   static constexpr int kHalves = D / 64;
   static constexpr int kTile = kHalves * kChunk * 128;   // K or V of one 64-key chunk
   static constexpr int kStage = 2 * kTile;
-  static constexpr int kBlkTile = kHalves * kPage * 128;  // K or V of the 16 block rows
+  // the 16 block rows of K and V share one tile with the same half stride as a
+  // chunk: K in rows 0..15 of each half, V in rows 16..31
+  static constexpr int kBlkTile = (kHalves - 1) * kChunk * 128 + 2 * kPage * 128;
+  static constexpr int kBlkV = kPage * 128;              // V offset inside that tile
 };
 
-// One chunk of keys for one warp: S = Q K^T, online softmax, O += P V.
+// One chunk of keys for one warp: S = Q K^T, online softmax, O += P V.  The
+// running max m is kept in the scaled log2 domain, so each probability is one
+// FFMA and one ex2.
 template <int D>
 __device__ __forceinline__ void attend_chunk(const uint32_t (&qf)[D / 16][4], uint32_t kbase,
-                                             uint32_t vbase, int half_rows, int n_valid,
-                                             float scale_log2, float (&o)[D / 8][4], float& m_a,
-                                             float& m_b, float& l_a, float& l_b) {
+                                             uint32_t vbase, int n_valid, float scale_log2,
+                                             float (&o)[D / 8][4], float& m_a, float& m_b,
+                                             float& l_a, float& l_b) {
   const int lane = threadIdx.x & 31;
   const int t = lane & 3;
   const int n16 = (n_valid + 15) >> 4;
@@ -122,38 +138,41 @@ __device__ __forceinline__ void attend_chunk(const uint32_t (&qf)[D / 16][4], ui
         const int key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
         const int chunk = 2 * kk + ((lane >> 3) & 1);
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(swz(kbase, half_rows, key, chunk), b0, b1, b2, b3);
+        ldsm_x4(swz(kbase, key, chunk), b0, b1, b2, b3);
         mma_16816(s[2 * np], qf[kk], b0, b1);
         mma_16816(s[2 * np + 1], qf[kk], b2, b3);
       }
     }
   }
+  if (n_valid < kChunk) {
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (nt * 8 + 2 * t + (e & 1) >= n_valid) s[nt][e] = -INFINITY;
+    }
+  }
   float mx_a = -INFINITY, mx_b = -INFINITY;
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int key = nt * 8 + 2 * t + (e & 1);
-      const float v = key < n_valid ? s[nt][e] * scale_log2 : -INFINITY;
-      s[nt][e] = v;
-      if (e < 2) mx_a = fmaxf(mx_a, v); else mx_b = fmaxf(mx_b, v);
-    }
+    mx_a = fmaxf(mx_a, fmaxf(s[nt][0], s[nt][1]));
+    mx_b = fmaxf(mx_b, fmaxf(s[nt][2], s[nt][3]));
   }
   mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
   mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
   mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
   mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-  const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-  const float al_a = exp2f(m_a - mn_a), al_b = exp2f(m_b - mn_b);
+  const float mn_a = fmaxf(m_a, mx_a * scale_log2), mn_b = fmaxf(m_b, mx_b * scale_log2);
+  const float al_a = fast_exp2(m_a - mn_a), al_b = fast_exp2(m_b - mn_b);
   m_a = mn_a;
   m_b = mn_b;
   float sum_a = 0.f, sum_b = 0.f;
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
-    s[nt][0] = exp2f(s[nt][0] - mn_a);
-    s[nt][1] = exp2f(s[nt][1] - mn_a);
-    s[nt][2] = exp2f(s[nt][2] - mn_b);
-    s[nt][3] = exp2f(s[nt][3] - mn_b);
+    s[nt][0] = fast_exp2(fmaf(s[nt][0], scale_log2, -mn_a));
+    s[nt][1] = fast_exp2(fmaf(s[nt][1], scale_log2, -mn_a));
+    s[nt][2] = fast_exp2(fmaf(s[nt][2], scale_log2, -mn_b));
+    s[nt][3] = fast_exp2(fmaf(s[nt][3], scale_log2, -mn_b));
     sum_a += s[nt][0] + s[nt][1];
     sum_b += s[nt][2] + s[nt][3];
   }
@@ -179,7 +198,7 @@ __device__ __forceinline__ void attend_chunk(const uint32_t (&qf)[D / 16][4], ui
         const int key = 16 * j + (lane & 7) + (((lane >> 3) & 1) << 3);
         const int chunk = 2 * dp + (lane >> 4);
         uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(swz(vbase, half_rows, key, chunk), b0, b1, b2, b3);
+        ldsm_x4_t(swz(vbase, key, chunk), b0, b1, b2, b3);
         mma_16816(o[2 * dp], a, b0, b1);
         mma_16816(o[2 * dp + 1], a, b2, b3);
       }
@@ -195,9 +214,10 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
-  uint8_t* blk_k = smem + kStages * C::kStage;
-  uint8_t* blk_v = blk_k + C::kBlkTile;
-  uint64_t* full = reinterpret_cast<uint64_t*>(blk_v + C::kBlkTile);
+  uint8_t* blk = smem + kStages * C::kStage;  // block K (rows 0..15) and V (rows 16..31)
+  float* rope_hi = reinterpret_cast<float*>(blk + C::kBlkTile);  // inv_freq as hi + lo
+  float* rope_lo = rope_hi + D / 2;
+  uint64_t* full = reinterpret_cast<uint64_t*>(rope_lo + D / 2);
   uint64_t* empty = full + kStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
 
@@ -213,6 +233,12 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
     }
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  // the rotary table goes to shared memory once: lanes then read it by index
+  // without serialising on the parameter bank
+  for (int i = threadIdx.x; i < D / 2; i += blockDim.x) {
+    rope_hi[i] = p.rope.hi[i];
+    rope_lo[i] = p.rope.lo[i];
   }
   if (warp == G && lane == 0) {
     tma_prefetch_desc(&tm_k);
@@ -324,26 +350,45 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
   const int t = lane & 3;
   const int ra = lane >> 2, rb = ra + 8;  // block rows owned by this thread
 
-  // block keys/values (RoPE'd) into shared memory, by the split that owns them
+  // block keys/values (RoPE'd) into shared memory, by the split that owns them.
+  // One item = 8 consecutive dims d0..d0+7 of block row j and their rotary
+  // partners d0+D/2..: four 16-byte loads, all issued before any arithmetic.
   if (has_block) {
-    const int nthreads = 32 * G;
-    for (int idx = threadIdx.x; idx < kPage * (D / 2); idx += nthreads) {
-      const int j = idx / (D / 2);
-      const int d = idx - j * (D / 2);
-      const size_t src = (static_cast<size_t>(b * kBlock + j) * p.n_kv_heads + g) * D;
-      const float x1 = bf16_bits_to_float(p.k_blk[src + d]);
-      const float x2 = bf16_bits_to_float(p.k_blk[src + d + D / 2]);
-      float sn, cs;
-      rope_sincos(L + j, p.rope.hi[d], p.rope.lo[d], &sn, &cs);
-      uint16_t* kd = reinterpret_cast<uint16_t*>(blk_k);
-      uint16_t* vd = reinterpret_cast<uint16_t*>(blk_v);
-      const int e1 = d, e2 = d + D / 2;
-      const int a1 = (e1 >> 6) * kPage * 64 + j * 64 + ((((e1 & 63) >> 3) ^ (j & 7)) << 3) + (e1 & 7);
-      const int a2 = (e2 >> 6) * kPage * 64 + j * 64 + ((((e2 & 63) >> 3) ^ (j & 7)) << 3) + (e2 & 7);
-      kd[a1] = float_to_bf16_bits(x1 * cs - x2 * sn);
-      kd[a2] = float_to_bf16_bits(x2 * cs + x1 * sn);
-      vd[a1] = p.v_blk[src + e1];
-      vd[a2] = p.v_blk[src + e2];
+    constexpr int kItems = kPage * (D / 16);
+    for (int it = threadIdx.x; it < kItems; it += 32 * G) {
+      const int j = it / (D / 16);
+      const int d0 = (it - j * (D / 16)) * 8;
+      const size_t src = (static_cast<size_t>(b * kBlock + j) * p.n_kv_heads + g) * D + d0;
+      const uint4 k1 = *reinterpret_cast<const uint4*>(p.k_blk + src);
+      const uint4 k2 = *reinterpret_cast<const uint4*>(p.k_blk + src + D / 2);
+      const uint4 v1 = *reinterpret_cast<const uint4*>(p.v_blk + src);
+      const uint4 v2 = *reinterpret_cast<const uint4*>(p.v_blk + src + D / 2);
+      const uint32_t kw1[4] = {k1.x, k1.y, k1.z, k1.w}, kw2[4] = {k2.x, k2.y, k2.z, k2.w};
+      uint32_t r1[4], r2[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float o1[2], o2[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int d = d0 + 2 * q + e;
+          const float x1 = __uint_as_float(e ? (kw1[q] & 0xFFFF0000u) : (kw1[q] << 16));
+          const float x2 = __uint_as_float(e ? (kw2[q] & 0xFFFF0000u) : (kw2[q] << 16));
+          float sn, cs;
+          rope_sincos(L + j, rope_hi[d], rope_lo[d], &sn, &cs);
+          o1[e] = x1 * cs - x2 * sn;
+          o2[e] = x2 * cs + x1 * sn;
+        }
+        r1[q] = pack_bf16(o1[0], o1[1]);
+        r2[q] = pack_bf16(o2[0], o2[1]);
+      }
+      // swizzled 16-byte chunks: dims d0.. sit in half d0 >> 6, chunk (d0 & 63) >> 3
+      const int e2 = d0 + D / 2;
+      const int off1 = (d0 >> 6) * kChunk * 128 + j * 128 + ((((d0 & 63) >> 3) ^ (j & 7)) << 4);
+      const int off2 = (e2 >> 6) * kChunk * 128 + j * 128 + ((((e2 & 63) >> 3) ^ (j & 7)) << 4);
+      *reinterpret_cast<uint4*>(blk + off1) = make_uint4(r1[0], r1[1], r1[2], r1[3]);
+      *reinterpret_cast<uint4*>(blk + off2) = make_uint4(r2[0], r2[1], r2[2], r2[3]);
+      *reinterpret_cast<uint4*>(blk + C::kBlkV + off1) = v1;
+      *reinterpret_cast<uint4*>(blk + C::kBlkV + off2) = v2;
     }
     named_bar_sync(1, 32 * G);
   }
@@ -377,7 +422,7 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
         for (int r = 0; r < 2; ++r) {
           const int pos = Lc + (r ? rb : ra);
           float sn, cs;
-          rope_sincos(pos, p.rope.hi[d], p.rope.lo[d], &sn, &cs);
+          rope_sincos(pos, rope_hi[d], rope_lo[d], &sn, &cs);
           const float x1 = qv[kk][r][e], x2 = qv[kk + D / 32][r][e];
           qv[kk][r][e] = x1 * cs - x2 * sn;
           qv[kk + D / 32][r][e] = x2 * cs + x1 * sn;
@@ -404,12 +449,11 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
   uint32_t stage = 0, phase = 0;
   for (int c = has_block ? -1 : 0; c < n_chunks; ++c) {
     uint32_t kb, vb;
-    int half_rows, n_valid;
+    int n_valid;
     uint8_t* vst = nullptr;
     if (c < 0) {
-      kb = smem_u32(blk_k);
-      vb = smem_u32(blk_v);
-      half_rows = kPage;
+      kb = smem_u32(blk);
+      vb = kb + C::kBlkV;
       n_valid = kPage;
     } else {
       const bool ok = mbar_wait(&full[stage], phase, abort_flag, p.status);
@@ -418,7 +462,6 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
       vst = kst + C::kTile;
       kb = smem_u32(kst);
       vb = smem_u32(vst);
-      half_rows = kChunk;
       n_valid = min(kChunk, key_end - (key_begin + c * kChunk));
       const int n_fill = ((n_valid + 15) >> 4) << 4;
       if (n_valid < n_fill) {
@@ -434,7 +477,7 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
         __syncwarp();
       }
     }
-    attend_chunk<D>(qf, kb, vb, half_rows, n_valid, p.scale_log2, o, m_a, m_b, l_a, l_b);
+    attend_chunk<D>(qf, kb, vb, n_valid, p.scale_log2, o, m_a, m_b, l_a, l_b);
     if (c >= 0) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
@@ -467,77 +510,90 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
   }
 }
 
-// Merge the split partials by log-sum-exp.  One CTA of four warps per output
-// row (b, i, h): all (max, sum) pairs are fetched at once, then each warp sums
-// a quarter of the splits with all of its loads in flight together, and the
-// four partial rows are added in shared memory -- two dependent global rounds.
+// Merge the split partials by log-sum-exp.  One warp per output row (b, i, h),
+// four rows per CTA.  A lane holds the (max, sum) pairs of splits lane and
+// lane + 32 and D/32 output elements; the partial rows are read in batches of
+// kBatch splits whose loads are all in flight together, and the first batch
+// is requested before the maxima are known, so a row costs about one global
+// round trip per batch.
 constexpr int kMaxSplits = 64;
+constexpr int kCombineRows = 4;
 
 template <int D>
-__global__ void __launch_bounds__(128) attn_combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(32 * kCombineRows) attn_combine_kernel(const CombineParams p) {
   griddep_wait();
   griddep_launch_dependents();
-  __shared__ float s_m[kMaxSplits], s_l[kMaxSplits];
-  __shared__ float s_acc[4][128];
-  __shared__ float s_lsum[4];
+  constexpr int per = D / 32;  // 2 or 4 elements per lane
+  constexpr int kBatch = 16;
+  using Vec = typename std::conditional<per == 4, float4, float2>::type;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x;
+  const int row = blockIdx.x * kCombineRows + warp;
+  const int rows_out = p.batch * kBlock * p.n_q_heads;
+  if (row >= rows_out) return;
   const int b = row / (kBlock * p.n_q_heads);
   const int rem = row - b * kBlock * p.n_q_heads;
   const int i = rem / p.n_q_heads;
   const int h = rem - i * p.n_q_heads;
-  const int L = p.seq_len[b];
-  if (L < 0 || L > p.limit) return;
   const int g = h / p.group, w = h - g * p.group;
   const int rr = w * kBlock + i;
   const size_t unit0 = (static_cast<size_t>(b) * p.n_kv_heads + g) * p.splits;
-  for (int s = threadIdx.x; s < p.splits; s += 128) {
-    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + ((unit0 + s) * p.rows + rr) * 2);
-    s_m[s] = ml.x;
-    s_l[s] = ml.y;
+  const int L = p.seq_len[b];
+  float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+  if (lane < p.splits) {
+    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + ((unit0 + lane) * p.rows + rr) * 2);
+    m0 = ml.x;
+    l0 = ml.y;
   }
-  __syncthreads();
-  float M = -INFINITY;
-  for (int s = 0; s < p.splits; ++s) M = fmaxf(M, s_m[s]);
-  constexpr int per = D / 32;  // 2 or 4 elements per lane
+  if (lane + 32 < p.splits) {
+    const float2 ml =
+        *reinterpret_cast<const float2*>(p.part_ml + ((unit0 + lane + 32) * p.rows + rr) * 2);
+    m1 = ml.x;
+    l1 = ml.y;
+  }
   const float* base = p.part_o + (unit0 * p.rows + rr) * D + lane * per;
   const size_t stride = static_cast<size_t>(p.rows) * D;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float lsum = 0.f;
-#pragma unroll 16
-  for (int s = warp; s < p.splits; s += 4) {
-    const float ms = s_m[s];
-    const float ws = ms == -INFINITY ? 0.f : exp2f(ms - M);
-    lsum += ws * s_l[s];
-    if constexpr (per == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(base + s * stride);
-      acc[0] += ws * v.x; acc[1] += ws * v.y; acc[2] += ws * v.z; acc[3] += ws * v.w;
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(base + s * stride);
-      acc[0] += ws * v.x; acc[1] += ws * v.y;
+  Vec v[kBatch];
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k)
+    if (k < p.splits) v[k] = *reinterpret_cast<const Vec*>(base + k * stride);
+  if (L < 0 || L > p.limit) return;
+  float M = fmaxf(m0, m1);
+#pragma unroll
+  for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const float w0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
+  const float w1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
+  float lsum = w0 * l0 + w1 * l1;
+#pragma unroll
+  for (int off = 16; off; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+  float acc[per];
+#pragma unroll
+  for (int e = 0; e < per; ++e) acc[e] = 0.f;
+  for (int s0 = 0; s0 < p.splits; s0 += kBatch) {
+    if (s0 > 0) {
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+        if (s0 + k < p.splits) v[k] = *reinterpret_cast<const Vec*>(base + (s0 + k) * stride);
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int sp = s0 + k;
+      const float wk = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
+      if (sp < p.splits) {
+        const float* f = reinterpret_cast<const float*>(&v[k]);
+#pragma unroll
+        for (int e = 0; e < per; ++e) acc[e] = fmaf(wk, f[e], acc[e]);
+      }
     }
   }
-#pragma unroll
-  for (int e = 0; e < per; ++e) s_acc[warp][lane * per + e] = acc[e];
-  if (lane == 0) s_lsum[warp] = lsum;
-  __syncthreads();
-  if (warp == 0) {
-    const float inv = 1.f / (s_lsum[0] + s_lsum[1] + s_lsum[2] + s_lsum[3]);
-    float o[4];
-#pragma unroll
-    for (int e = 0; e < per; ++e) {
-      const int d = lane * per + e;
-      o[e] = (s_acc[0][d] + s_acc[1][d] + s_acc[2][d] + s_acc[3][d]) * inv;
-    }
-    uint16_t* dst = p.out + static_cast<size_t>(row) * D + lane * per;
-    if constexpr (per == 4) {
-      uint2 v;
-      v.x = pack_bf16(o[0], o[1]);
-      v.y = pack_bf16(o[2], o[3]);
-      *reinterpret_cast<uint2*>(dst) = v;
-    } else {
-      *reinterpret_cast<uint32_t*>(dst) = pack_bf16(o[0], o[1]);
-    }
+  const float inv = 1.f / lsum;
+  uint16_t* dst = p.out + static_cast<size_t>(row) * D + lane * per;
+  if constexpr (per == 4) {
+    uint2 o;
+    o.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    o.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = o;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
   }
 }
 
@@ -576,14 +632,15 @@ int launch_attention(const dflash_dims& dims, const Plan& plan, const dflash_kv_
                                 kChunk, 1)))
       return rc;
   }
-  const int smem = 1024 + kStages * C::kStage + 2 * C::kBlkTile + 2 * kStages * 8 + 16;
+  const int smem = 1024 + kStages * C::kStage + C::kBlkTile + D * 4 + 2 * kStages * 8 + 16;
   if ((rc = set_smem_limit(reinterpret_cast<const void*>(block_attention_kernel<D>), smem)))
     return rc;
   rc = launch(block_attention_kernel<D>, dim3(plan.att_splits, dims.n_kv_heads, dims.batch),
               dim3(32 * (p.group + 1)), smem, stream, tm_k, tm_v, tm_k64, tm_v64, p);
   if (rc) return rc;
   const int rows_out = dims.batch * kBlock * dims.n_q_heads;
-  return launch(attn_combine_kernel<D>, dim3(rows_out), dim3(128), 0, stream, cp);
+  return launch(attn_combine_kernel<D>, dim3((rows_out + kCombineRows - 1) / kCombineRows),
+                dim3(32 * kCombineRows), 0, stream, cp);
 }
 
 }  // namespace
