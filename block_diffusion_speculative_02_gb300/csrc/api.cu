@@ -15,11 +15,6 @@ namespace {
 #define DFLASH_TMAP_L2_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_256B
 #endif
 
-#ifndef DFLASH_ATT_CTAS_PER_SM
-#define DFLASH_ATT_CTAS_PER_SM 2
-#endif
-constexpr int kAttCtasPerSm = DFLASH_ATT_CTAS_PER_SM;
-
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -79,10 +74,11 @@ int make_plan(const dflash_dims& d, Plan* p) {
   q.kv_tok_chunks = (q.ntok + 127) / 128;
   q.att_rows = (d.n_q_heads / d.n_kv_heads) * kBlock;
   {
-    // enough (sequence, KV head, split) CTAs for two per SM, and no split
-    // longer than 4096 keys so that ragged batches balance
+    // enough (sequence, KV head, split) CTAs to fill every SM once (one
+    // attention CTA per SM), and no split longer than 4096 keys so that
+    // ragged batches balance
     const int pages = (d.max_ctx + 15) / 16;
-    int s = (kAttCtasPerSm * q.num_sms) / (d.batch * d.n_kv_heads);
+    int s = q.num_sms / (d.batch * d.n_kv_heads);
     const int by_len = (d.max_ctx + 4095) / 4096;
     if (s < by_len) s = by_len;
     if (s > pages) s = pages;

@@ -6,19 +6,29 @@
 // block.  "dflash-mlx" (dpshk.com) 块扩散草稿: the staged token and 15 masks
 // are denoised in one parallel forward that reads the target's hidden states.
 //
-// Design (GB300): decode-style attention is bound by the context KV read
-// (64 flop per byte with GQA packing).  Grid = (split, KV head, sequence): each
-// CTA owns one KV head of one sequence and a page-aligned slice of its
-// context, so the G = Hq/Hkv query heads that share the KV head (G*16 query
-// rows) read every KV byte once.  One producer warp streams 64-key chunks of
-// K and V through a 3-stage TMA pipeline (one 16-row box per page and 64-wide
-// half of the head dim, 128-byte swizzle; contiguous and paged caches differ
-// only in the row coordinate of each box).  G consumer warps (one per query
-// head, 16 rows each) run QK^T and PV on mma.sync bf16 tensor cores with an
-// fp32 online softmax (quad shuffles for row max/sum).  RoPE of the block
-// queries/keys is applied in registers at positions L + i.  The split that
-// owns the tail also folds in the 16 block keys.  Partial (O, max, sum) go to
-// the workspace and a second kernel merges the splits by log-sum-exp.
+// Design (GB300): grid = (split, KV head, sequence).  Each CTA owns one KV
+// head of one sequence and a page-aligned slice of its context, so the
+// G = Hq/Hkv query heads sharing the KV head (R = 16 G query rows) read every
+// KV byte once.  The two products run on the 5th-generation tensor cores with
+// the query rows as the MMA's M (128 rows; R/4 real rows per 32-lane TMEM
+// quadrant, so all four warps of the softmax work):
+//   S = Q K^T   (M = 128, N = keys of the chunk, K = D)   -> TMEM, two buffers
+//   O += P V    (M = 128, N = D, K = keys; V is read MN-major) -> TMEM
+// One warp streams 64-key chunks of K and V with TMA (one 16-row box per
+// page and 64-wide half of the head dim, or one 64-row box for a whole
+// contiguous chunk; 128-byte swizzle), one thread issues the MMAs, and one
+// thread pair per query row runs the online softmax straight from TMEM (for
+// R <= 64 every query row is staged twice, at lanes i and i + 16 of its
+// quadrant, and the pair splits the chunk's keys): row max, exp2, row sum,
+// bf16 P into shared memory for the next MMA.  The running
+// max only moves (and O in TMEM is rescaled) when a chunk raises it by more
+// than 2^8, so P stays below 256 and rescales are rare.  The S MMA of chunk
+// j + 1 overlaps the softmax of chunk j.  RoPE of the block queries and keys
+// is applied while they are staged into shared memory, at positions L + i,
+// from a sin/cos table of the 16 block positions built once per CTA.
+// The split that owns the tail also folds in the 16 block keys (a 16-key
+// chunk).  Partial (O, max, sum) go to the workspace and a second kernel
+// merges the splits by log-sum-exp.
 #include <type_traits>
 
 #include "common.cuh"
@@ -27,15 +37,17 @@
 namespace dflash {
 namespace {
 
-constexpr int kChunk = 64;   // keys per pipeline stage
-constexpr int kPage = 16;    // rows per TMA box
-#ifndef DFLASH_ATT_STAGES
-#define DFLASH_ATT_STAGES 3
-#endif
-constexpr int kStages = DFLASH_ATT_STAGES;
+constexpr int kChunk = 64;     // keys per pipeline stage
+constexpr int kPage = 16;      // rows per TMA box
+constexpr int kAttThreads = 320;  // TMA, MMA, two softmax warpgroups
+// TMEM columns: S buffers at 0 and 64, O of the even-chunk group at 128, O of
+// the odd-chunk group at 128 + D
+template <int D>
+__host__ __device__ constexpr int tmem_cols() { return 128 + 2 * D <= 256 ? 256 : 512; }
+constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnParams {
-  int batch, n_q_heads, n_kv_heads, group, splits, rows;  // rows = group * 16
+  int batch, n_q_heads, n_kv_heads, group, splits, rows;  // rows R = group * 16
   int paged, capacity, max_pages;
   const int32_t* seq_len;
   const int32_t* page_table;
@@ -46,6 +58,8 @@ struct AttnParams {
   float* part_o;
   float* part_ml;
   uint32_t* status;
+  // shared-memory plan (byte offsets from the 1024-aligned base)
+  int n_stages, off_q, off_st, off_blk, off_sc, off_ml, off_rope, off_bar;
   RopeTable rope;
 };
 
@@ -57,29 +71,6 @@ struct CombineParams {
   uint16_t* out;
 };
 
-__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                          uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return static_cast<uint32_t>(float_to_bf16_bits(lo)) |
          (static_cast<uint32_t>(float_to_bf16_bits(hi)) << 16);
@@ -87,15 +78,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Byte address of (row, 16-byte chunk) in a tile stored as 64-column halves of
-// kChunk rows x 128 B with the 128-byte swizzle.  The row stride of a half is
-// a compile-time constant, so the addresses of a fully unrolled chunk fold to
-// a per-lane base plus immediates.
-__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int chunk) {
-  return base + static_cast<uint32_t>((chunk >> 3) * kChunk * 128 + row * 128 +
-                                      (((chunk & 7) ^ (row & 7)) << 4));
 }
 
 // 2^x on the special-function unit (one instruction; -inf gives +0).
@@ -108,145 +90,116 @@ __device__ __forceinline__ float fast_exp2(float x) {
 template <int D>
 struct Cfg {
   static constexpr int kHalves = D / 64;
-  static constexpr int kTile = kHalves * kChunk * 128;   // K or V of one 64-key chunk
+  static constexpr int kHalf = kChunk * 128;              // one 64-col half of a chunk
+  static constexpr int kTile = kHalves * kHalf;           // K or V of one 64-key chunk
   static constexpr int kStage = 2 * kTile;
-  // the 16 block rows of K and V share one tile with the same half stride as a
+  // the 16 block rows of K and V share one tile with the half stride of a
   // chunk: K in rows 0..15 of each half, V in rows 16..31
-  static constexpr int kBlkTile = (kHalves - 1) * kChunk * 128 + 2 * kPage * 128;
-  static constexpr int kBlkV = kPage * 128;              // V offset inside that tile
+  static constexpr int kBlkTile = (kHalves - 1) * kHalf + 2 * kPage * 128;
+  static constexpr int kBlkV = kPage * 128;
 };
 
-// One chunk of keys for one warp: S = Q K^T, online softmax, O += P V.  The
-// running max m is kept in the scaled log2 domain, so each probability is one
-// FFMA and one ex2.
-template <int D>
-__device__ __forceinline__ void attend_chunk(const uint32_t (&qf)[D / 16][4], uint32_t kbase,
-                                             uint32_t vbase, int n_valid, float scale_log2,
-                                             float (&o)[D / 8][4], float& m_a, float& m_b,
-                                             float& l_a, float& l_b) {
-  const int lane = threadIdx.x & 31;
-  const int t = lane & 3;
-  const int n16 = (n_valid + 15) >> 4;
-  float s[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-    for (int np = 0; np < 4; ++np) {
-      if (np < n16) {
-        const int key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-        const int chunk = 2 * kk + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(swz(kbase, key, chunk), b0, b1, b2, b3);
-        mma_16816(s[2 * np], qf[kk], b0, b1);
-        mma_16816(s[2 * np + 1], qf[kk], b2, b3);
-      }
-    }
-  }
-  if (n_valid < kChunk) {
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (nt * 8 + 2 * t + (e & 1) >= n_valid) s[nt][e] = -INFINITY;
-    }
-  }
-  float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    mx_a = fmaxf(mx_a, fmaxf(s[nt][0], s[nt][1]));
-    mx_b = fmaxf(mx_b, fmaxf(s[nt][2], s[nt][3]));
-  }
-  mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-  mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-  mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-  mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-  const float mn_a = fmaxf(m_a, mx_a * scale_log2), mn_b = fmaxf(m_b, mx_b * scale_log2);
-  const float al_a = fast_exp2(m_a - mn_a), al_b = fast_exp2(m_b - mn_b);
-  m_a = mn_a;
-  m_b = mn_b;
-  float sum_a = 0.f, sum_b = 0.f;
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    s[nt][0] = fast_exp2(fmaf(s[nt][0], scale_log2, -mn_a));
-    s[nt][1] = fast_exp2(fmaf(s[nt][1], scale_log2, -mn_a));
-    s[nt][2] = fast_exp2(fmaf(s[nt][2], scale_log2, -mn_b));
-    s[nt][3] = fast_exp2(fmaf(s[nt][3], scale_log2, -mn_b));
-    sum_a += s[nt][0] + s[nt][1];
-    sum_b += s[nt][2] + s[nt][3];
-  }
-  l_a = l_a * al_a + sum_a;
-  l_b = l_b * al_b + sum_b;
-#pragma unroll
-  for (int dt = 0; dt < D / 8; ++dt) {
-    o[dt][0] *= al_a;
-    o[dt][1] *= al_a;
-    o[dt][2] *= al_b;
-    o[dt][3] *= al_b;
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (j < n16) {
-      uint32_t a[4];
-      a[0] = pack_bf16(s[2 * j][0], s[2 * j][1]);
-      a[1] = pack_bf16(s[2 * j][2], s[2 * j][3]);
-      a[2] = pack_bf16(s[2 * j + 1][0], s[2 * j + 1][1]);
-      a[3] = pack_bf16(s[2 * j + 1][2], s[2 * j + 1][3]);
-#pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {
-        const int key = 16 * j + (lane & 7) + (((lane >> 3) & 1) << 3);
-        const int chunk = 2 * dp + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(swz(vbase, key, chunk), b0, b1, b2, b3);
-        mma_16816(o[2 * dp], a, b0, b1);
-        mma_16816(o[2 * dp + 1], a, b2, b3);
-      }
-    }
-  }
+// Byte offset of (row, 16-byte chunk `c` of the 128-byte row) in a tile of
+// rows x 128 B with the 128-byte swizzle (row stride 128 B).
+__device__ __forceinline__ int swz_off(int row, int c) {
+  return row * 128 + (((c & 7) ^ (row & 7)) << 4);
 }
 
-template <int D>
-__global__ void __launch_bounds__(288) block_attention_kernel(
+// Rotate 8 consecutive dims (x1: d0..d0+7) against their partners (x2:
+// d0+D/2..) with the (cos, sin) pairs sc[d0..d0+7] of one position; bf16 in,
+// bf16 out.
+__device__ __forceinline__ void rope8(const uint4& x1, const uint4& x2, const float2* sc, int d0,
+                                      uint4& y1, uint4& y2) {
+  const uint32_t w1[4] = {x1.x, x1.y, x1.z, x1.w}, w2[4] = {x2.x, x2.y, x2.z, x2.w};
+  uint32_t r1[4], r2[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    float o1[2], o2[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float2 cs = sc[d0 + 2 * q + e];
+      const float a = __uint_as_float(e ? (w1[q] & 0xFFFF0000u) : (w1[q] << 16));
+      const float c = __uint_as_float(e ? (w2[q] & 0xFFFF0000u) : (w2[q] << 16));
+      o1[e] = a * cs.x - c * cs.y;
+      o2[e] = c * cs.x + a * cs.y;
+    }
+    r1[q] = pack_bf16(o1[0], o1[1]);
+    r2[q] = pack_bf16(o2[0], o2[1]);
+  }
+  y1 = make_uint4(r1[0], r1[1], r1[2], r1[3]);
+  y2 = make_uint4(r2[0], r2[1], r2[2], r2[3]);
+}
+
+template <int D, bool DUP>
+__global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const __grid_constant__ CUtensorMap tm_k64, const __grid_constant__ CUtensorMap tm_v64,
     const AttnParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
-  uint8_t* blk = smem + kStages * C::kStage;  // block K (rows 0..15) and V (rows 16..31)
-  float* rope_hi = reinterpret_cast<float*>(blk + C::kBlkTile);  // inv_freq as hi + lo
+  const int R = p.rows;
+  const int NS = p.n_stages;
+  const int rq = R / 4;                        // real query rows per TMEM quadrant
+  constexpr bool dup = DUP;                    // rows staged twice (lanes i, i + 16): R <= 64
+  constexpr int kPBytes = 128 * 128;           // one P buffer: 128 rows x 64 keys bf16
+  constexpr int kQHalf = 128 * 128;            // one 64-dim half of Q: 128 rows
+  uint8_t* qs = smem + p.off_q;                // Q: [half][128 rows][128 B]
+  uint8_t* stg = smem + p.off_st;
+  uint8_t* blk = smem + p.off_blk;
+  float2* sct = reinterpret_cast<float2*>(smem + p.off_sc);  // [16 positions][D/2] (cos, sin)
+  float2* ml_odd = reinterpret_cast<float2*>(smem + p.off_ml);  // [128] odd group's (max, sum)
+  float* rope_hi = reinterpret_cast<float*>(smem + p.off_rope);
   float* rope_lo = rope_hi + D / 2;
-  uint64_t* full = reinterpret_cast<uint64_t*>(rope_lo + D / 2);
-  uint64_t* empty = full + kStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+  uint64_t* empty = full + NS;
+  uint64_t* s_full = empty + NS;   // [2] S(j) in TMEM buffer j & 1
+  uint64_t* p_full = s_full + 2;   // [2] P(j) in shared buffer j & 1 (and O rescaled)
+  uint64_t* pv_done = p_full + 2;  // [2] O += P(j) V(j) completed
+  uint64_t* q_ready = pv_done + 2; // Q and the block tile staged (256 arrivals)
+  uint64_t* o_done = q_ready + 1;
+  uint64_t* mdrain = o_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdrain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
   const int s_idx = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], G);
+      mbar_init(&empty[i], 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(q_ready, 256);
+    mbar_init(o_done, 1);
+    mbar_init(mdrain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // the rotary table goes to shared memory once: lanes then read it by index
-  // without serialising on the parameter bank
   for (int i = threadIdx.x; i < D / 2; i += blockDim.x) {
     rope_hi[i] = p.rope.hi[i];
     rope_lo[i] = p.rope.lo[i];
   }
-  if (warp == G && lane == 0) {
+  if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_k64);
     tma_prefetch_desc(&tm_v64);
   }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, tmem_cols<D>());
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
   griddep_wait();
 
   const int L = p.seq_len[b];
@@ -263,28 +216,33 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
   const int key_end = min(pg_end * kPage, Lc);
   const int n_keys = key_end > key_begin ? key_end - key_begin : 0;
   const int n_chunks = (n_keys + kChunk - 1) / kChunk;
-  const bool has_block = valid_len && (s_idx == p.splits - 1);
+  const int has_block = (valid_len && s_idx == p.splits - 1) ? 1 : 0;
+  const int n_total = n_chunks + has_block;    // chunk 0 is the block when has_block
+  auto chunk_keys = [&](int j) {               // valid keys of chunk j
+    if (has_block && j == 0) return kPage;
+    return min(kChunk, key_end - (key_begin + (j - has_block) * kChunk));
+  };
 
-  if (warp == G) {
+  if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
       uint32_t stage = 0, phase = 0;
+      int issued = 0;
       for (int c = 0; c < n_chunks; ++c) {
         if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) break;
-        uint8_t* kst = smem + stage * C::kStage;
+        uint8_t* kst = stg + stage * C::kStage;
         uint8_t* vst = kst + C::kTile;
         const int k0 = key_begin + c * kChunk;
         const int npg = min(kChunk / kPage, (key_end - k0 + kPage - 1) / kPage);
         // head-major caches: a page (16 rows) of one head is 16 * D contiguous
         // elements, a contiguous cache holds each head's rows back to back
-        const int slab = b * p.n_kv_heads + g;  // contiguous: (sequence, head) slab
+        const int slab = b * p.n_kv_heads + g;
         if (!p.paged && npg == kChunk / kPage) {
-          // whole chunk of a contiguous cache: one 64-row box per half
           mbar_arrive_expect_tx(&full[stage], 2u * C::kHalves * kChunk * 128);
           for (int h = 0; h < C::kHalves; ++h) {
-            tma_load_3d(kst + h * kChunk * 128, &tm_k64, &full[stage], h * 64, k0, slab, pol);
-            tma_load_3d(vst + h * kChunk * 128, &tm_v64, &full[stage], h * 64, k0, slab, pol);
+            tma_load_3d(kst + h * C::kHalf, &tm_k64, &full[stage], h * 64, k0, slab, pol);
+            tma_load_3d(vst + h * C::kHalf, &tm_v64, &full[stage], h * 64, k0, slab, pol);
           }
         } else {
           int zc[kChunk / kPage];  // third coordinate of each page's box, -1 = unmapped
@@ -307,8 +265,8 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
             if (zc[j] >= 0) continue;
             set_status(p.status, DFLASH_ST_PAGE_MISSING);
             for (int h = 0; h < C::kHalves; ++h) {
-              uint4* kz = reinterpret_cast<uint4*>(kst + h * kChunk * 128 + j * kPage * 128);
-              uint4* vz = reinterpret_cast<uint4*>(vst + h * kChunk * 128 + j * kPage * 128);
+              uint4* kz = reinterpret_cast<uint4*>(kst + h * C::kHalf + j * kPage * 128);
+              uint4* vz = reinterpret_cast<uint4*>(vst + h * C::kHalf + j * kPage * 128);
               for (int i = 0; i < kPage * 128 / 16; ++i) kz[i] = vz[i] = make_uint4(0, 0, 0, 0);
             }
             zeroed = true;
@@ -320,9 +278,9 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
               if (zc[j] < 0) continue;
               const int row = p.paged ? 0 : k0 + j * kPage;
               for (int h = 0; h < C::kHalves; ++h) {
-                tma_load_3d(kst + h * kChunk * 128 + j * kPage * 128, &tm_k, &full[stage], h * 64,
+                tma_load_3d(kst + h * C::kHalf + j * kPage * 128, &tm_k, &full[stage], h * 64,
                             row, zc[j], pol);
-                tma_load_3d(vst + h * kChunk * 128 + j * kPage * 128, &tm_v, &full[stage], h * 64,
+                tma_load_3d(vst + h * C::kHalf + j * kPage * 128, &tm_v, &full[stage], h * 64,
                             row, zc[j], pol);
               }
             }
@@ -330,183 +288,325 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
             mbar_arrive(&full[stage]);
           }
         }
-        if (++stage == kStages) {
+        ++issued;
+        if (++stage == static_cast<uint32_t>(NS)) {
           stage = 0;
           phase ^= 1;
         }
       }
-      // drain copies still in flight (only matters after an abort)
-      const int issued = n_chunks;
-      for (int st = 0; st < kStages && st < issued; ++st) {
-        const int last = st + ((issued - 1 - st) / kStages) * kStages;
-        mbar_wait_drain(&full[st], static_cast<uint32_t>((last / kStages) & 1), p.status);
+      // no copy may still be landing when the CTA exits
+      for (int st = 0; st < NS && st < issued; ++st) {
+        const int last = st + ((issued - 1 - st) / NS) * NS;
+        mbar_wait_drain(&full[st], static_cast<uint32_t>((last / NS) & 1), p.status);
       }
     }
-    return;
-  }
-
-  // ---------------- consumers: warp w = query head g*G + w ----------------
-  const int h = g * G + warp;
-  const int t = lane & 3;
-  const int ra = lane >> 2, rb = ra + 8;  // block rows owned by this thread
-
-  // block keys/values (RoPE'd) into shared memory, by the split that owns them.
-  // One item = 8 consecutive dims d0..d0+7 of block row j and their rotary
-  // partners d0+D/2..: four 16-byte loads, all issued before any arithmetic.
-  if (has_block) {
-    constexpr int kItems = kPage * (D / 16);
-    for (int it = threadIdx.x; it < kItems; it += 32 * G) {
-      const int j = it / (D / 16);
-      const int d0 = (it - j * (D / 16)) * 8;
-      const size_t src = (static_cast<size_t>(b * kBlock + j) * p.n_kv_heads + g) * D + d0;
-      const uint4 k1 = *reinterpret_cast<const uint4*>(p.k_blk + src);
-      const uint4 k2 = *reinterpret_cast<const uint4*>(p.k_blk + src + D / 2);
-      const uint4 v1 = *reinterpret_cast<const uint4*>(p.v_blk + src);
-      const uint4 v2 = *reinterpret_cast<const uint4*>(p.v_blk + src + D / 2);
-      const uint32_t kw1[4] = {k1.x, k1.y, k1.z, k1.w}, kw2[4] = {k2.x, k2.y, k2.z, k2.w};
-      uint32_t r1[4], r2[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float o1[2], o2[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int d = d0 + 2 * q + e;
-          const float x1 = __uint_as_float(e ? (kw1[q] & 0xFFFF0000u) : (kw1[q] << 16));
-          const float x2 = __uint_as_float(e ? (kw2[q] & 0xFFFF0000u) : (kw2[q] << 16));
-          float sn, cs;
-          rope_sincos(L + j, rope_hi[d], rope_lo[d], &sn, &cs);
-          o1[e] = x1 * cs - x2 * sn;
-          o2[e] = x2 * cs + x1 * sn;
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0 && n_total > 0) {
+      const uint32_t q_addr = smem_u32(qs);
+      const uint32_t blk_addr = smem_u32(blk);
+      const uint32_t st_addr = smem_u32(stg);
+      const uint32_t p_addr = smem_u32(smem);    // P buffers at offsets 0 and kPBytes
+      const uint32_t o_tmem = tmem_base + 128;
+      const uint32_t idesc_pv = umma_idesc_bf16(128, D) | (1u << 16);  // B (= V) MN-major
+      bool ok = mbar_wait(q_ready, 0, abort_flag, p.status);
+      tc_fence_after();
+      // S(j) = Q K_j^T into TMEM buffer j & 1
+      auto issue_s = [&](int j) -> bool {
+        const int nk = chunk_keys(j);
+        const int ncol = (nk + 15) & ~15;
+        uint32_t kb;
+        if (has_block && j == 0) {
+          kb = blk_addr;
+        } else {
+          const int c = j - has_block;
+          if (!mbar_wait(&full[c % NS], static_cast<uint32_t>((c / NS) & 1), abort_flag, p.status))
+            return false;
+          tc_fence_after();
+          kb = st_addr + (c % NS) * C::kStage;
         }
-        r1[q] = pack_bf16(o1[0], o1[1]);
-        r2[q] = pack_bf16(o2[0], o2[1]);
+        const uint32_t idesc = umma_idesc_bf16(128, ncol);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = umma_sdesc_sw128(q_addr + (kk >> 2) * kQHalf + (kk & 3) * 32);
+          const uint64_t bd = umma_sdesc_sw128(kb + (kk >> 2) * C::kHalf + (kk & 3) * 32);
+          umma_bf16(tmem_base + (j & 1) * 64, a, bd, idesc, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[j & 1]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      if (ok && n_total > 1) ok = issue_s(1);
+      for (int j = 0; ok && j < n_total; ++j) {
+        if (!mbar_wait(&p_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), abort_flag, p.status))
+          break;
+        tc_fence_after();
+        const bool is_blk = has_block && j == 0;
+        const int c = j - has_block;
+        const uint32_t vb = is_blk ? blk_addr + C::kBlkV : st_addr + (c % NS) * C::kStage + C::kTile;
+        const int ksteps = (chunk_keys(j) + 15) >> 4;
+        for (int ks = 0; ks < ksteps; ++ks) {
+          const uint64_t a = umma_sdesc_sw128(p_addr + (j & 1) * kPBytes + ks * 32);
+          const uint64_t bd = umma_sdesc_sw128_mn(vb + ks * 2048, C::kHalf, 1024);
+          umma_bf16(o_tmem + (j & 1) * D, a, bd, idesc_pv, (j >= 2 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(&pv_done[j & 1]);
+        if (!is_blk) umma_commit(&empty[c % NS]);
+        if (j + 2 < n_total && !issue_s(j + 2)) break;
       }
-      // swizzled 16-byte chunks: dims d0.. sit in half d0 >> 6, chunk (d0 & 63) >> 3
-      const int e2 = d0 + D / 2;
-      const int off1 = (d0 >> 6) * kChunk * 128 + j * 128 + ((((d0 & 63) >> 3) ^ (j & 7)) << 4);
-      const int off2 = (e2 >> 6) * kChunk * 128 + j * 128 + ((((e2 & 63) >> 3) ^ (j & 7)) << 4);
-      *reinterpret_cast<uint4*>(blk + off1) = make_uint4(r1[0], r1[1], r1[2], r1[3]);
-      *reinterpret_cast<uint4*>(blk + off2) = make_uint4(r2[0], r2[1], r2[2], r2[3]);
-      *reinterpret_cast<uint4*>(blk + C::kBlkV + off1) = v1;
-      *reinterpret_cast<uint4*>(blk + C::kBlkV + off2) = v2;
+      umma_commit(o_done);
+      umma_commit(mdrain);
+      mbar_wait_drain(mdrain, 0, p.status);
     }
-    named_bar_sync(1, 32 * G);
-  }
-
-  // query fragments (A operand of m16n8k16), rotated in registers: element d
-  // and its RoPE partner d + D/2 sit in the same thread, D/32 k-steps apart.
-  uint32_t qf[D / 16][4];
-  {
-    float qv[D / 16][2][4];  // [k-step][row a/b][k offsets 2t, 2t+1, 2t+8, 2t+9]
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int row = r ? rb : ra;
-        const uint16_t* src =
-            p.q_blk + (static_cast<size_t>(b * kBlock + row) * p.n_q_heads + h) * D + kk * 16 + 2 * t;
-        const uint32_t lo = *reinterpret_cast<const uint32_t*>(src);
-        const uint32_t hi = *reinterpret_cast<const uint32_t*>(src + 8);
-        qv[kk][r][0] = __uint_as_float(lo << 16);
-        qv[kk][r][1] = __uint_as_float(lo & 0xFFFF0000u);
-        qv[kk][r][2] = __uint_as_float(hi << 16);
-        qv[kk][r][3] = __uint_as_float(hi & 0xFFFF0000u);
-      }
+  } else {
+    // ---------------- staging, then softmax (warps 2..9) ----------------
+    const int tid = threadIdx.x - 64;            // 0 .. 255
+    // (cos, sin) of the 16 block positions L + i, i < 16, for every frequency
+    for (int k = tid; k < kPage * (D / 2); k += 256) {
+      const int i = k / (D / 2), d = k - i * (D / 2);
+      float sn, cs;
+      rope_sincos(Lc + i, rope_hi[d], rope_lo[d], &sn, &cs);
+      sct[k] = make_float2(cs, sn);
     }
+    named_bar_sync(1, 256);
+    // Q rows (rr = w * 16 + i for query head g * G + w) rotated at L + i, and
+    // the block's K (rotated at L + j) and V, into the swizzled K-major tiles.
+    // Q row rr goes to MMA row 32 (rr / rq) + rr % rq, and again 16 rows
+    // further when rows are doubled.  Items of 8 dims with their rotary
+    // partners; loads issued before math.
+    {
+      constexpr int kPer = D / 16;               // items per row
+      const int q_items = R * kPer;
+      for (int base = 0; base < q_items; base += 2 * 256) {
+        uint4 x1[2], x2[2];
 #pragma unroll
-    for (int kk = 0; kk < D / 32; ++kk) {
+        for (int u = 0; u < 2; ++u) {
+          const int it = base + u * 256 + tid;
+          if (it < q_items) {
+            const int rr = it / kPer, d0 = (it - rr * kPer) * 8;
+            const int w = rr >> 4, i = rr & 15;
+            const size_t src =
+                (static_cast<size_t>(b * kBlock + i) * p.n_q_heads + g * G + w) * D + d0;
+            x1[u] = *reinterpret_cast<const uint4*>(p.q_blk + src);
+            x2[u] = *reinterpret_cast<const uint4*>(p.q_blk + src + D / 2);
+          }
+        }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int d = kk * 16 + 2 * t + (e & 1) + ((e >> 1) << 3);
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int pos = Lc + (r ? rb : ra);
-          float sn, cs;
-          rope_sincos(pos, rope_hi[d], rope_lo[d], &sn, &cs);
-          const float x1 = qv[kk][r][e], x2 = qv[kk + D / 32][r][e];
-          qv[kk][r][e] = x1 * cs - x2 * sn;
-          qv[kk + D / 32][r][e] = x2 * cs + x1 * sn;
+        for (int u = 0; u < 2; ++u) {
+          const int it = base + u * 256 + tid;
+          if (it < q_items) {
+            const int rr = it / kPer, d0 = (it - rr * kPer) * 8;
+            uint4 y1, y2;
+            rope8(x1[u], x2[u], sct + (rr & 15) * (D / 2), d0, y1, y2);
+            const int e2 = d0 + D / 2;
+            const int m = 32 * (rr / rq) + rr % rq;
+            *reinterpret_cast<uint4*>(qs + (d0 >> 6) * kQHalf + swz_off(m, (d0 & 63) >> 3)) = y1;
+            *reinterpret_cast<uint4*>(qs + (e2 >> 6) * kQHalf + swz_off(m, (e2 & 63) >> 3)) = y2;
+            if (dup) {
+              *reinterpret_cast<uint4*>(qs + (d0 >> 6) * kQHalf + swz_off(m + 16, (d0 & 63) >> 3)) = y1;
+              *reinterpret_cast<uint4*>(qs + (e2 >> 6) * kQHalf + swz_off(m + 16, (e2 & 63) >> 3)) = y2;
+            }
+          }
         }
       }
+      if (has_block) {
+        for (int it = tid; it < kPage * kPer; it += 256) {
+          const int j = it / kPer, d0 = (it - j * kPer) * 8;
+          const size_t src = (static_cast<size_t>(b * kBlock + j) * p.n_kv_heads + g) * D + d0;
+          const uint4 k1 = *reinterpret_cast<const uint4*>(p.k_blk + src);
+          const uint4 k2 = *reinterpret_cast<const uint4*>(p.k_blk + src + D / 2);
+          const uint4 v1 = *reinterpret_cast<const uint4*>(p.v_blk + src);
+          const uint4 v2 = *reinterpret_cast<const uint4*>(p.v_blk + src + D / 2);
+          uint4 y1, y2;
+          rope8(k1, k2, sct + j * (D / 2), d0, y1, y2);
+          const int e2 = d0 + D / 2;
+          const int off1 = (d0 >> 6) * C::kHalf + swz_off(j, (d0 & 63) >> 3);
+          const int off2 = (e2 >> 6) * C::kHalf + swz_off(j, (e2 & 63) >> 3);
+          *reinterpret_cast<uint4*>(blk + off1) = y1;
+          *reinterpret_cast<uint4*>(blk + off2) = y2;
+          *reinterpret_cast<uint4*>(blk + C::kBlkV + off1) = v1;
+          *reinterpret_cast<uint4*>(blk + C::kBlkV + off2) = v2;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(q_ready);
     }
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      qf[kk][0] = pack_bf16(qv[kk][0][0], qv[kk][0][1]);
-      qf[kk][1] = pack_bf16(qv[kk][1][0], qv[kk][1][1]);
-      qf[kk][2] = pack_bf16(qv[kk][0][2], qv[kk][0][3]);
-      qf[kk][3] = pack_bf16(qv[kk][1][2], qv[kk][1][3]);
-    }
-  }
 
-  float o[D / 8][4];
+    const int q4 = warp & 3;                    // TMEM lane quadrant of this warp
+    const int grp = (warp - 2) >> 2;            // 0: even chunks, 1: odd chunks
+    // this thread's query row: lane i of the quadrant (i < rq real); with
+    // doubled rows lanes i and i + 16 hold the same row and split its keys
+    const int i_row = dup ? (lane & 15) : lane;
+    const int khalf = dup ? (lane >> 4) : 0;    // which 32 keys of a chunk (doubled rows)
+    const bool real = i_row < rq;
+    const int rr = q4 * rq + i_row;             // row in the partial outputs
+    const int m = q4 * 32 + i_row;              // MMA row that carries P of this query row
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16);
+    const uint32_t o_col = 128 + grp * D;       // this group's O accumulator
+    constexpr int kMine = dup ? 32 : 64;        // keys of a chunk per thread
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = grp; j < n_total; j += 2) {
+      const int nk = chunk_keys(j);
+      ok = mbar_wait(&s_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[4][16];
 #pragma unroll
-  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-
-  // iteration -1 is the 16 block keys (only in the split that owns them), then
-  // the context chunks; one copy of the chunk code keeps the loop in the
-  // instruction cache
-  uint32_t stage = 0, phase = 0;
-  for (int c = has_block ? -1 : 0; c < n_chunks; ++c) {
-    uint32_t kb, vb;
-    int n_valid;
-    uint8_t* vst = nullptr;
-    if (c < 0) {
-      kb = smem_u32(blk);
-      vb = kb + C::kBlkV;
-      n_valid = kPage;
-    } else {
-      const bool ok = mbar_wait(&full[stage], phase, abort_flag, p.status);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      uint8_t* kst = smem + stage * C::kStage;
-      vst = kst + C::kTile;
-      kb = smem_u32(kst);
-      vb = smem_u32(vst);
-      n_valid = min(kChunk, key_end - (key_begin + c * kChunk));
-      const int n_fill = ((n_valid + 15) >> 4) << 4;
-      if (n_valid < n_fill) {
-        // rows past the length inside the last 16-key group: zero V so that
-        // 0-probability keys cannot inject NaN/Inf from stale memory
-        for (int i = lane; i < (n_fill - n_valid) * C::kHalves * 8; i += 32) {
-          const int row = n_valid + i / (C::kHalves * 8);
+      for (int c16 = 0; c16 < 4; ++c16)
+        if (c16 * 16 < nk) tmem_ld_32x32b_x16(lane_addr + (j & 1) * 64 + c16 * 16, sv[c16]);
+      tmem_ld_wait();
+      // this thread's keys kbase .. kbase + kMine - 1, masked past nk
+      const int kbase = 32 * khalf;
+      float x[kMine];
+#pragma unroll
+      for (int e = 0; e < kMine; ++e) {
+        uint32_t v;
+        if (dup) v = khalf ? sv[2 + (e >> 4)][e & 15] : sv[e >> 4][e & 15];
+        else v = sv[e >> 4][e & 15];
+        x[e] = kbase + e < nk ? __uint_as_float(v) : -INFINITY;
+      }
+      float mx4[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+      for (int e = 4; e < kMine; e += 4) {
+        mx4[0] = fmaxf(mx4[0], x[e]);
+        mx4[1] = fmaxf(mx4[1], x[e + 1]);
+        mx4[2] = fmaxf(mx4[2], x[e + 2]);
+        mx4[3] = fmaxf(mx4[3], x[e + 3]);
+      }
+      float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      if (dup) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mx_s = mx * p.scale_log2;
+      float alpha = 1.f;
+      if (m_run == -INFINITY) {
+        m_run = mx_s;                         // first chunk of this group: O and l empty
+      } else if (mx_s > m_run + kRescaleLog2) {
+        alpha = fast_exp2(m_run - mx_s);
+        m_run = mx_s;
+      }
+      // the group's previous P V (chunk j - 2) must be done before its P buffer
+      // is rewritten or its O rescaled
+      if (j >= 2) {
+        ok = mbar_wait(&pv_done[j & 1], static_cast<uint32_t>(((j - 2) >> 1) & 1), abort_flag,
+                       p.status);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+      }
+      if (__any_sync(0xffffffffu, real && alpha != 1.f)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c16 = 0; c16 < D / 16; ++c16) {
+          uint32_t ov[16];
+          tmem_ld_32x32b_x16(lane_addr + o_col + c16 * 16, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st_32x32b_x16(lane_addr + o_col + c16 * 16, ov);
+        }
+        tmem_st_wait();
+      }
+      l_run *= alpha;
+      if (q4 == 0 && (nk & 15) && !(has_block && j == 0)) {
+        // rows past the length inside the last 16-key group came with their
+        // page: zero their V so that 0-probability keys cannot inject
+        // NaN/Inf from stale memory into O
+        uint8_t* vst = stg + ((j - has_block) % NS) * C::kStage + C::kTile;
+        const int n_fill = (nk + 15) & ~15;
+        for (int i = lane; i < (n_fill - nk) * C::kHalves * 8; i += 32) {
+          const int r = nk + i / (C::kHalves * 8);
           const int ch = i % (C::kHalves * 8);
-          *reinterpret_cast<uint4*>(vst + (ch >> 3) * kChunk * 128 + row * 128 +
-                                    (((ch & 7) ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vst + (ch >> 3) * C::kHalf + swz_off(r, ch & 7)) =
+              make_uint4(0, 0, 0, 0);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
       }
+      uint8_t* prow = smem + (j & 1) * kPBytes;
+      const int ncol = (nk + 15) & ~15;         // keys the P V MMA reads (p = 0 past nk)
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c8 = 0; c8 < kMine / 8; ++c8) {  // 8 keys = one 16-byte chunk of the P row
+        const int key0 = kbase + 8 * c8;
+        if (key0 < ncol) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const float p0 = fast_exp2(fmaf(x[8 * c8 + e], p.scale_log2, -m_run));
+            const float p1 = fast_exp2(fmaf(x[8 * c8 + e + 1], p.scale_log2, -m_run));
+            sum4[e >> 1] += p0 + p1;
+            pk[e >> 1] = pack_bf16(p0, p1);
+          }
+          if (real)
+            *reinterpret_cast<uint4*>(prow + swz_off(m, key0 >> 3)) =
+                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full[j & 1]);
     }
-    attend_chunk<D>(qf, kb, vb, n_valid, p.scale_log2, o, m_a, m_b, l_a, l_b);
-    if (c >= 0) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      if (++stage == kStages) {
-        stage = 0;
-        phase ^= 1;
+    if (dup) l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
+    // epilogue: the odd group hands its (max, sum) to the even group, which
+    // merges the two O accumulators into this split's partial (O, max, sum)
+    const bool writer = real && khalf == 0;
+    const bool odd_used = n_total > 1;
+    if (grp == 1 && writer) ml_odd[m] = make_float2(ok ? m_run : -INFINITY, ok ? l_run : 0.f);
+    named_bar_sync(2, 256);
+    if (grp == 0) {
+      const size_t unit = (static_cast<size_t>(b) * p.n_kv_heads + g) * p.splits + s_idx;
+      float* po = p.part_o + (unit * R + rr) * D;
+      float* pml = p.part_ml + (unit * R + rr) * 2;
+      bool have_o = ok && n_total > 0;
+      if (have_o) {
+        const bool done = mbar_wait(o_done, 0, abort_flag, p.status);
+        have_o = __all_sync(0xffffffffu, done);
       }
+      float M = m_run, wa = 1.f, wb = 0.f, l_tot = l_run;
+      if (have_o && odd_used) {
+        const float2 ob = ml_odd[m];
+        M = fmaxf(m_run, ob.x);
+        wa = fast_exp2(m_run - M);
+        wb = ob.x == -INFINITY ? 0.f : fast_exp2(ob.x - M);
+        l_tot = wa * l_run + wb * ob.y;
+      }
+      if (have_o) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c16 = 0; c16 < D / 16; ++c16) {
+          uint32_t oa[16], ob[16];
+          tmem_ld_32x32b_x16(lane_addr + 128 + c16 * 16, oa);
+          if (odd_used) tmem_ld_32x32b_x16(lane_addr + 128 + D + c16 * 16, ob);
+          tmem_ld_wait();
+          if (writer) {
+            float o[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              o[e] = odd_used ? wa * __uint_as_float(oa[e]) + wb * __uint_as_float(ob[e])
+                              : __uint_as_float(oa[e]);
+#pragma unroll
+            for (int e = 0; e < 16; e += 4)
+              *reinterpret_cast<float4*>(po + c16 * 16 + e) =
+                  make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+          }
+        }
+      } else if (writer) {
+        for (int e = 0; e < D; e += 4) *reinterpret_cast<float4*>(po + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+        M = -INFINITY;
+        l_tot = 0.f;
+      }
+      if (writer) *reinterpret_cast<float2*>(pml) = make_float2(M, l_tot);
     }
   }
   griddep_launch_dependents();
-
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
-  l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
-  l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
-
-  const size_t unit = (static_cast<size_t>(b) * p.n_kv_heads + g) * p.splits + s_idx;
-  float* po = p.part_o + unit * p.rows * D;
-  float* pml = p.part_ml + unit * p.rows * 2;
-  const int rra = warp * kBlock + ra, rrb = warp * kBlock + rb;
-#pragma unroll
-  for (int dt = 0; dt < D / 8; ++dt) {
-    const int d = dt * 8 + 2 * t;
-    *reinterpret_cast<float2*>(po + static_cast<size_t>(rra) * D + d) = make_float2(o[dt][0], o[dt][1]);
-    *reinterpret_cast<float2*>(po + static_cast<size_t>(rrb) * D + d) = make_float2(o[dt][2], o[dt][3]);
-  }
-  if (t == 0) {
-    *reinterpret_cast<float2*>(pml + rra * 2) = make_float2(m_a, l_a);
-    *reinterpret_cast<float2*>(pml + rrb * 2) = make_float2(m_b, l_b);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tmem_cols<D>());
   }
 }
 
@@ -516,7 +616,6 @@ __global__ void __launch_bounds__(288) block_attention_kernel(
 // kBatch splits whose loads are all in flight together, and the first batch
 // is requested before the maxima are known, so a row costs about one global
 // round trip per batch.
-constexpr int kMaxSplits = 64;
 constexpr int kCombineRows = 4;
 
 template <int D>
@@ -597,6 +696,35 @@ __global__ void __launch_bounds__(32 * kCombineRows) attn_combine_kernel(const C
   }
 }
 
+// Shared-memory plan of the attention kernel: two P buffers (128 rows x 64
+// keys each), Q ([half][128 rows][128 B]), the K/V stages, the block tile,
+// the sin/cos table, the odd group's (max, sum), the rotary table and the
+// barriers.  One CTA per SM, with as many stages (up to 6) as fit.
+constexpr int kSmemPerCta = 232448;  // opt-in maximum of one CTA
+
+template <int D>
+int attention_smem_for(AttnParams& p, int n_stages) {
+  using C = Cfg<D>;
+  p.n_stages = n_stages;
+  p.off_q = 2 * 128 * 128;                              // after the two P buffers
+  p.off_st = p.off_q + C::kHalves * 128 * 128;
+  p.off_blk = p.off_st + n_stages * C::kStage;
+  p.off_sc = p.off_blk + C::kBlkTile;                   // [16][D/2] float2
+  p.off_ml = p.off_sc + kPage * (D / 2) * 8;            // [128] float2
+  p.off_rope = p.off_ml + 128 * 8;
+  p.off_bar = p.off_rope + D * 4;
+  return 1024 + p.off_bar + (2 * n_stages + 9) * 8 + 8;
+}
+
+template <int D>
+int plan_attention_smem(AttnParams& p) {
+  for (int ns = 6; ns >= 2; --ns) {
+    const int smem = attention_smem_for<D>(p, ns);
+    if (smem <= kSmemPerCta) return smem;
+  }
+  return attention_smem_for<D>(p, 2);
+}
+
 template <int D>
 int launch_attention(const dflash_dims& dims, const Plan& plan, const dflash_kv_view& cache,
                      AttnParams& p, CombineParams& cp, cudaStream_t stream) {
@@ -632,11 +760,12 @@ int launch_attention(const dflash_dims& dims, const Plan& plan, const dflash_kv_
                                 kChunk, 1)))
       return rc;
   }
-  const int smem = 1024 + kStages * C::kStage + C::kBlkTile + D * 4 + 2 * kStages * 8 + 16;
-  if ((rc = set_smem_limit(reinterpret_cast<const void*>(block_attention_kernel<D>), smem)))
-    return rc;
-  rc = launch(block_attention_kernel<D>, dim3(plan.att_splits, dims.n_kv_heads, dims.batch),
-              dim3(32 * (p.group + 1)), smem, stream, tm_k, tm_v, tm_k64, tm_v64, p);
+  const int smem = plan_attention_smem<D>(p);
+  // query rows are doubled across the TMEM lanes when they fill at most half
+  auto kernel = p.rows <= 64 ? block_attention_kernel<D, true> : block_attention_kernel<D, false>;
+  if ((rc = set_smem_limit(reinterpret_cast<const void*>(kernel), smem))) return rc;
+  rc = launch(kernel, dim3(plan.att_splits, dims.n_kv_heads, dims.batch), dim3(kAttThreads), smem,
+              stream, tm_k, tm_v, tm_k64, tm_v64, p);
   if (rc) return rc;
   const int rows_out = dims.batch * kBlock * dims.n_q_heads;
   return launch(attn_combine_kernel<D>, dim3((rows_out + kCombineRows - 1) / kCombineRows),
