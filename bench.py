@@ -398,7 +398,7 @@ def main(argv=None):
     __graft_entry__.build()
     world, rank = init_dist("nccl")
     import block_diffusion_speculative_02_gb300 as dfl
-    from block_diffusion_speculative_02_gb300.cycle import run_cycle, side_stream
+    from block_diffusion_speculative_02_gb300.cycle import run_cycle, side_stream, tune_sm_split
 
     kv_bytes_per_set = 2 * cfg.n_kv_heads * cfg.head_dim * 2 * (
         cfg.batch * (cfg.ctx_len or cfg.ctx_len_range[1]) + 32)
@@ -408,8 +408,9 @@ def main(argv=None):
     concurrent = not args.serial
     if concurrent:
         # verify on this stream, the projection on a side stream, each on its
-        # own share of the SMs; joined before the crop
-        verify_sms, project_sms = dfl.dflash_cycle_sm_split(dims)
+        # own share of the SMs (measured once around the proportional split,
+        # before the warm-up); joined before the crop
+        verify_sms, project_sms = tune_sm_split(dims, w, states, ws)
         side = side_stream(stream.device)
         fork, join = torch.cuda.Event(), torch.cuda.Event()
     else:
@@ -535,7 +536,8 @@ def main(argv=None):
         for _ in range(args.e2e_steps):
             for d_, h_ in zip(ins, host_in):
                 d_.copy_(h_, non_blocking=True)
-            run_cycle(dims, w, st0, ws, 1.0 / math.sqrt(cfg.head_dim), concurrent=concurrent)
+            run_cycle(dims, w, st0, ws, 1.0 / math.sqrt(cfg.head_dim), concurrent=concurrent,
+                      sm_split=(verify_sms, project_sms) if concurrent else None)
             for h_, d_ in zip(host_out, outs):
                 h_.copy_(d_, non_blocking=True)
             torch.cuda.current_stream().synchronize()

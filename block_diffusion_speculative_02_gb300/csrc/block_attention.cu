@@ -361,51 +361,50 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
   } else {
     // ---------------- staging, then softmax (warps 2..9) ----------------
     const int tid = threadIdx.x - 64;            // 0 .. 255
-    // (cos, sin) of the 16 block positions L + i, i < 16, for every frequency
-    for (int k = tid; k < kPage * (D / 2); k += 256) {
-      const int i = k / (D / 2), d = k - i * (D / 2);
-      float sn, cs;
-      rope_sincos(Lc + i, rope_hi[d], rope_lo[d], &sn, &cs);
-      sct[k] = make_float2(cs, sn);
-    }
-    named_bar_sync(1, 256);
     // Q rows (rr = w * 16 + i for query head g * G + w) rotated at L + i, and
     // the block's K (rotated at L + j) and V, into the swizzled K-major tiles.
     // Q row rr goes to MMA row 32 (rr / rq) + rr % rq, and again 16 rows
     // further when rows are doubled.  Items of 8 dims with their rotary
-    // partners; loads issued before math.
+    // partners; this thread's loads go out before the sin/cos table is built.
     {
       constexpr int kPer = D / 16;               // items per row
+      constexpr int kMaxItems = 128 * kPer / 256;  // items per thread at R = 128
       const int q_items = R * kPer;
-      for (int base = 0; base < q_items; base += 2 * 256) {
-        uint4 x1[2], x2[2];
+      uint4 x1[kMaxItems], x2[kMaxItems];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int it = base + u * 256 + tid;
-          if (it < q_items) {
-            const int rr = it / kPer, d0 = (it - rr * kPer) * 8;
-            const int w = rr >> 4, i = rr & 15;
-            const size_t src =
-                (static_cast<size_t>(b * kBlock + i) * p.n_q_heads + g * G + w) * D + d0;
-            x1[u] = *reinterpret_cast<const uint4*>(p.q_blk + src);
-            x2[u] = *reinterpret_cast<const uint4*>(p.q_blk + src + D / 2);
-          }
+      for (int u = 0; u < kMaxItems; ++u) {
+        const int it = u * 256 + tid;
+        if (it < q_items) {
+          const int rr = it / kPer, d0 = (it - rr * kPer) * 8;
+          const int w = rr >> 4, i = rr & 15;
+          const size_t src =
+              (static_cast<size_t>(b * kBlock + i) * p.n_q_heads + g * G + w) * D + d0;
+          x1[u] = *reinterpret_cast<const uint4*>(p.q_blk + src);
+          x2[u] = *reinterpret_cast<const uint4*>(p.q_blk + src + D / 2);
         }
+      }
+      // (cos, sin) of the 16 block positions L + i, i < 16, for every frequency
+      for (int k = tid; k < kPage * (D / 2); k += 256) {
+        const int i = k / (D / 2), d = k - i * (D / 2);
+        float sn, cs;
+        rope_sincos(Lc + i, rope_hi[d], rope_lo[d], &sn, &cs);
+        sct[k] = make_float2(cs, sn);
+      }
+      named_bar_sync(1, 256);
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int it = base + u * 256 + tid;
-          if (it < q_items) {
-            const int rr = it / kPer, d0 = (it - rr * kPer) * 8;
-            uint4 y1, y2;
-            rope8(x1[u], x2[u], sct + (rr & 15) * (D / 2), d0, y1, y2);
-            const int e2 = d0 + D / 2;
-            const int m = 32 * (rr / rq) + rr % rq;
-            *reinterpret_cast<uint4*>(qs + (d0 >> 6) * kQHalf + swz_off(m, (d0 & 63) >> 3)) = y1;
-            *reinterpret_cast<uint4*>(qs + (e2 >> 6) * kQHalf + swz_off(m, (e2 & 63) >> 3)) = y2;
-            if (dup) {
-              *reinterpret_cast<uint4*>(qs + (d0 >> 6) * kQHalf + swz_off(m + 16, (d0 & 63) >> 3)) = y1;
-              *reinterpret_cast<uint4*>(qs + (e2 >> 6) * kQHalf + swz_off(m + 16, (e2 & 63) >> 3)) = y2;
-            }
+      for (int u = 0; u < kMaxItems; ++u) {
+        const int it = u * 256 + tid;
+        if (it < q_items) {
+          const int rr = it / kPer, d0 = (it - rr * kPer) * 8;
+          uint4 y1, y2;
+          rope8(x1[u], x2[u], sct + (rr & 15) * (D / 2), d0, y1, y2);
+          const int e2 = d0 + D / 2;
+          const int m = 32 * (rr / rq) + rr % rq;
+          *reinterpret_cast<uint4*>(qs + (d0 >> 6) * kQHalf + swz_off(m, (d0 & 63) >> 3)) = y1;
+          *reinterpret_cast<uint4*>(qs + (e2 >> 6) * kQHalf + swz_off(m, (e2 & 63) >> 3)) = y2;
+          if (dup) {
+            *reinterpret_cast<uint4*>(qs + (d0 >> 6) * kQHalf + swz_off(m + 16, (d0 & 63) >> 3)) = y1;
+            *reinterpret_cast<uint4*>(qs + (e2 >> 6) * kQHalf + swz_off(m + 16, (e2 & 63) >> 3)) = y2;
           }
         }
       }
@@ -623,7 +622,7 @@ __global__ void __launch_bounds__(32 * kCombineRows) attn_combine_kernel(const C
   griddep_wait();
   griddep_launch_dependents();
   constexpr int per = D / 32;  // 2 or 4 elements per lane
-  constexpr int kBatch = 16;
+  constexpr int kBatch = 32;
   using Vec = typename std::conditional<per == 4, float4, float2>::type;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kCombineRows + warp;

@@ -22,8 +22,10 @@ struct CropViews {
 
 __global__ void kv_crop_kernel(const CropViews views, const int32_t* __restrict__ new_len,
                                int batch, uint32_t* status) {
-  griddep_wait();
+  // the next kernel may start its prologue now: whatever it reads of ours it
+  // reads after its own wait, which covers our completion
   griddep_launch_dependents();
+  griddep_wait();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= views.n * batch) return;
   const int vi = idx / batch;

@@ -18,7 +18,7 @@ from __future__ import annotations
 
 import math
 from dataclasses import dataclass
-from typing import List, Optional
+from typing import List, Optional, Tuple
 
 import torch
 
@@ -69,36 +69,81 @@ class CycleState:
     attn_out: torch.Tensor            # bf16 [B, 16, Hq, D]
 
 
-def run_cycle(dims: Dims, w: CycleWeights, st: CycleState, ws: torch.Tensor,
-              scale: Optional[float] = None, stream=None, concurrent: bool = True):
-    """Issue one cycle on the current (or given) stream.
-
-    With ``concurrent`` the verification and the projection run on disjoint
-    SM budgets on two streams; otherwise all four calls queue on one stream.
-    """
-    if scale is None:
-        scale = 1.0 / math.sqrt(dims.head_dim)
-    main = torch.cuda.current_stream() if stream is None else stream
-    if concurrent:
-        verify_sms, project_sms = dflash_cycle_sm_split(dims)
-        dims_v = with_sm_budget(dims, verify_sms)
-        dims_p = with_sm_budget(dims, project_sms)
-        side = side_stream(st.verify_hidden.device)
-        fork = torch.cuda.Event()
-        fork.record(main)
-        side.wait_event(fork)
-    else:
-        dims_v = dims_p = dims
-        side = main
+def _verify_and_project(dims_v: Dims, dims_p: Dims, w: CycleWeights, st: CycleState,
+                        ws: torch.Tensor, main, side):
+    """verify on ``main`` and the projection on ``side``, forked from and joined
+    back into ``main``."""
+    fork = torch.cuda.Event()
+    fork.record(main)
+    side.wait_event(fork)
     dflash_verify_accept(dims_v, st.verify_hidden, w.w_lm, st.block_ids, st.len_before,
                          st.posterior, st.accept_len, st.next_staged, st.commit_len,
                          st.out_tokens, ws, main)
     dflash_ctx_project(dims_p, st.layer_hidden, w.w_fc, w.hidden_norm_w, w.w_k, w.w_v,
                        w.k_norm_w, st.write_pos, st.draft_cache, ws, side)
+    join = torch.cuda.Event()
+    join.record(side)
+    main.wait_event(join)
+
+
+def tune_sm_split(dims: Dims, w: CycleWeights, states: List[CycleState], ws: torch.Tensor,
+                  spread: int = 4, reps: int = 8, rounds: int = 2) -> Tuple[int, int]:
+    """Measure the verify || projection phase for SM splits around
+    ``dflash_cycle_sm_split`` and return the fastest (verify_sms, project_sms).
+
+    The proportional split is only a first guess: the two kernels' per-SM
+    bandwidth shares and tile boundaries move the optimum by a few SMs.  Runs
+    ``rounds * (2 * spread + 1) * reps`` phases on the given states (their
+    outputs are overwritten; lengths written by the projection are restored).
+    """
+    v0, p0 = dflash_cycle_sm_split(dims)
+    nsm = v0 + p0
+    main = torch.cuda.current_stream()
+    side = side_stream(states[0].verify_hidden.device)
+    saved = [s.draft_cache.seq_len.clone() for s in states]
+    best = {}
+    for _ in range(rounds):
+        for p in range(max(1, p0 - spread), min(nsm - 1, p0 + spread) + 1):
+            dv, dp = with_sm_budget(dims, nsm - p), with_sm_budget(dims, p)
+            _verify_and_project(dv, dp, w, states[0], ws, main, side)   # warm
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(main)
+            for i in range(reps):
+                _verify_and_project(dv, dp, w, states[i % len(states)], ws, main, side)
+            e1.record(main)
+            e1.synchronize()
+            t = e0.elapsed_time(e1) / reps
+            best[p] = min(best.get(p, t), t)
+    for s, L in zip(states, saved):
+        s.draft_cache.seq_len.copy_(L)
+    torch.cuda.synchronize()
+    p = min(best, key=best.get)
+    return nsm - p, p
+
+
+def run_cycle(dims: Dims, w: CycleWeights, st: CycleState, ws: torch.Tensor,
+              scale: Optional[float] = None, stream=None, concurrent: bool = True,
+              sm_split: Optional[Tuple[int, int]] = None):
+    """Issue one cycle on the current (or given) stream.
+
+    With ``concurrent`` the verification and the projection run on disjoint
+    SM budgets on two streams (``sm_split`` = (verify_sms, project_sms), by
+    default ``dflash_cycle_sm_split``); otherwise all four calls queue on one
+    stream.
+    """
+    if scale is None:
+        scale = 1.0 / math.sqrt(dims.head_dim)
+    main = torch.cuda.current_stream() if stream is None else stream
     if concurrent:
-        join = torch.cuda.Event()
-        join.record(side)
-        main.wait_event(join)
+        verify_sms, project_sms = sm_split or dflash_cycle_sm_split(dims)
+        _verify_and_project(with_sm_budget(dims, verify_sms), with_sm_budget(dims, project_sms),
+                            w, st, ws, main, side_stream(st.verify_hidden.device))
+    else:
+        dflash_verify_accept(dims, st.verify_hidden, w.w_lm, st.block_ids, st.len_before,
+                             st.posterior, st.accept_len, st.next_staged, st.commit_len,
+                             st.out_tokens, ws, main)
+        dflash_ctx_project(dims, st.layer_hidden, w.w_fc, w.hidden_norm_w, w.w_k, w.w_v,
+                           w.k_norm_w, st.write_pos, st.draft_cache, ws, main)
     dflash_kv_crop([st.target_view, st.draft_cache], st.commit_len, dims.batch, ws, main)
     dflash_block_attention(dims, st.q_blk, st.k_blk, st.v_blk, st.draft_cache, scale,
                            st.attn_out, ws, main)
