@@ -49,6 +49,9 @@ def parse_args(argv=None):
                     help="extra steps after the timed region with events around every call")
     ap.add_argument("--sets", type=int, default=0,
                     help="rotating input sets (0: enough to exceed twice the L2 size)")
+    ap.add_argument("--sm-split", default="",
+                    help="verify_sms,project_sms for the side-by-side phase (default: measured "
+                         "around the proportional split before the warm-up)")
     ap.add_argument("--serial", action="store_true",
                     help="queue verify and the projection on one stream instead of running "
                          "them side by side on disjoint SM budgets")
@@ -410,7 +413,10 @@ def main(argv=None):
         # verify on this stream, the projection on a side stream, each on its
         # own share of the SMs (measured once around the proportional split,
         # before the warm-up); joined before the crop
-        verify_sms, project_sms = tune_sm_split(dims, w, states, ws)
+        if args.sm_split:
+            verify_sms, project_sms = (int(x) for x in args.sm_split.split(","))
+        else:
+            verify_sms, project_sms = tune_sm_split(dims, w, states, ws)
         side = side_stream(stream.device)
         fork, join = torch.cuda.Event(), torch.cuda.Event()
     else:

@@ -116,159 +116,169 @@ __device__ void reserve_block_rows(const GemmParams& p, int b) {
   v.seq_len[b] = pos + kBlock;
 }
 
-constexpr int kTokBatch = 16;  // token rows finished together (independent loads in flight)
+constexpr int kTokGroup = 4;  // token rows a warp finishes together (loads in flight)
 
-// The accumulated sums of feature f for token rows tok0 .. tok0+n-1 (all n
-// loads in flight together), cleared again for the next call.
-__device__ __forceinline__ void take_sums(const GemmParams& p, int tok0, int n, int f,
-                                          float (&y)[kTokBatch]) {
-  float* src = p.acc + static_cast<size_t>(tok0) * p.ld_out + f;
-#pragma unroll
-  for (int j = 0; j < kTokBatch; ++j) y[j] = j < n ? __ldcg(src + static_cast<size_t>(j) * p.ld_out) : 0.f;
-#pragma unroll
-  for (int j = 0; j < kTokBatch; ++j)
-    if (j < n) src[static_cast<size_t>(j) * p.ld_out] = 0.f;
+__device__ __forceinline__ uint2 pack4_bf16(float a, float b, float c, float d) {
+  return make_uint2(static_cast<uint32_t>(float_to_bf16_bits(a)) |
+                        (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16),
+                    static_cast<uint32_t>(float_to_bf16_bits(c)) |
+                        (static_cast<uint32_t>(float_to_bf16_bits(d)) << 16));
 }
 
-// fc finisher (last split CTA of an output tile): Y = the accumulated sum;
-// hi/lo bf16 pair of g_h * Y for the next GEMM; partial sums of Y^2 over this
-// tile's 128 features (the RMSNorm scale itself is applied after the K/V GEMM,
-// since it is one factor per token row).
-__device__ void finish_fc(const GemmParams& p, int o, int c, float* red) {
+__device__ __forceinline__ float4 load4_bf16(const uint16_t* src) {
+  const uint2 w = *reinterpret_cast<const uint2*>(src);
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                     __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+}
+
+// The finished sums of 4 consecutive features of token row `tok`, cleared
+// again for the next call.
+__device__ __forceinline__ float4 take4(const GemmParams& p, int tok, int f0) {
+  float4* src = reinterpret_cast<float4*>(p.acc + static_cast<size_t>(tok) * p.ld_out + f0);
+  const float4 v = __ldcg(src);
+  __stcg(src, make_float4(0.f, 0.f, 0.f, 0.f));
+  return v;
+}
+
+// fc finisher (CTA that completed an output tile): Y = the accumulated sum;
+// hi/lo bf16 pair of g_h * Y for the next GEMM; the tile's partial sums of Y^2
+// per token row (the RMSNorm scale itself is applied after the K/V GEMM,
+// since it is one factor per token row).  Warp w takes token rows w, w + 4,
+// ...; a lane owns 4 consecutive features.
+__device__ void finish_fc(const GemmParams& p, int o, int c) {
   const int et = threadIdx.x - 64, warp = et >> 5, lane = et & 31;
-  const int f = o * 128 + et;
-  const float g = p.hidden_norm_w ? bf16_bits_to_float(p.hidden_norm_w[f]) : 1.f;
+  const int f0 = o * 128 + lane * 4;
+  const float4 g = p.hidden_norm_w ? load4_bf16(p.hidden_norm_w + f0) : make_float4(1.f, 1.f, 1.f, 1.f);
   const int t0 = c * p.chunk_rows;
   const int nt = min(p.chunk_rows, p.n_tok - t0);
-  for (int j0 = 0; j0 < nt; j0 += kTokBatch) {
-    const int n = min(kTokBatch, nt - j0);
-    float y[kTokBatch];
-    take_sums(p, t0 + j0, n, f, y);
+#pragma unroll 1
+  for (int j0 = warp * kTokGroup; j0 < nt; j0 += 4 * kTokGroup) {
+    float4 y[kTokGroup];
 #pragma unroll
-    for (int j = 0; j < kTokBatch; ++j) {
-      if (j < n) {
-        const int tok = t0 + j0 + j;
-        const float gy = y[j] * g;
-        const uint16_t hi = float_to_bf16_bits(gy);
-        p.yhat[static_cast<size_t>(tok) * p.hidden + f] = hi;
-        p.yhat[(static_cast<size_t>(p.n_tok) + tok) * p.hidden + f] =
-            float_to_bf16_bits(gy - bf16_bits_to_float(hi));
+    for (int k = 0; k < kTokGroup; ++k)
+      if (j0 + k < nt) y[k] = take4(p, t0 + j0 + k, f0);
+#pragma unroll
+    for (int k = 0; k < kTokGroup; ++k) {
+      if (j0 + k >= nt) break;
+      const int tok = t0 + j0 + k;
+      const float a[4] = {y[k].x * g.x, y[k].y * g.y, y[k].z * g.z, y[k].w * g.w};
+      float hi[4], lo[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        hi[e] = bf16_bits_to_float(float_to_bf16_bits(a[e]));
+        lo[e] = a[e] - hi[e];
       }
-      float sq = y[j] * y[j];
+      *reinterpret_cast<uint2*>(p.yhat + static_cast<size_t>(tok) * p.hidden + f0) =
+          pack4_bf16(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint2*>(p.yhat + (static_cast<size_t>(p.n_tok) + tok) * p.hidden + f0) =
+          pack4_bf16(lo[0], lo[1], lo[2], lo[3]);
+      float sq = y[k].x * y[k].x + y[k].y * y[k].y + y[k].z * y[k].z + y[k].w * y[k].w;
 #pragma unroll
       for (int off = 16; off; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-      if (lane == 0 && j < n) red[warp * 256 + j0 + j] = sq;
+      if (lane == 0) p.ss[static_cast<size_t>(o) * p.n_tok + tok] = sq;
     }
   }
-  named_bar_sync(1, 128);
-  for (int j = et; j < nt; j += 128)
-    p.ss[static_cast<size_t>(o) * p.n_tok + t0 + j] =
-        red[j] + red[256 + j] + red[512 + j] + red[768 + j];
 }
 
-// kv finisher (last split CTA of an output tile): K or V rows of 128 features
-// (one or two heads) for every token of the chunk: the accumulated sum, the
-// RMSNorm scale of Y, per-head RMSNorm and RoPE for K, bf16 store into the
-// cache row write_pos + t.
-__device__ void finish_kv(const GemmParams& p, int o, int c, float* smem_f) {
+// kv finisher (CTA that completed an output tile): K or V rows of 128
+// features (one head at D = 128, two at D = 64) for every token row of the
+// chunk: the accumulated sum, the RMSNorm scale of Y, per-head RMSNorm and
+// RoPE for K, bf16 store into the cache row write_pos + t.  The per-token
+// scale and cache offsets are set up first, one thread per token row; then
+// warp w takes token rows w, w + 4, ..., a lane owning 4 consecutive features
+// (a head spans D / 4 lanes, the RoPE partner of dims d < D/2 sits D / 8
+// lanes further).
+__device__ void finish_kv(const GemmParams& p, int o, int c, uint8_t* scratch) {
   const int et = threadIdx.x - 64, warp = et >> 5, lane = et & 31;
   const int D = p.head_dim;
   const bool is_k = o < p.a_split;
-  const int feat = (is_k ? o : o - p.a_split) * 128 + et;  // within Hkv * D
-  const int head = feat / D, d = feat - head * D;
+  const int feat0 = (is_k ? o : o - p.a_split) * 128 + lane * 4;  // within Hkv * D
+  const int head = feat0 / D, d0 = feat0 - head * D;
   const int t0 = c * p.chunk_rows;
   const int nt = min(p.chunk_rows, p.n_tok - t0);
-  float* rbuf = smem_f;                   // [256] per-token RMSNorm scale of Y
-  float* red = smem_f + 256;              // [4][kTokBatch] per-warp sums
-  float* kbuf = smem_f + 256 + 4 * kTokBatch;  // [kTokBatch][128] RoPE partner exchange
-  if (p.hidden_norm_w) {
-    // the fc tiles' partial sums of Y^2 for this chunk's rows, all loads in
-    // flight at once (threads over (tile, row)), then per-row sums in tile order
-    float* ssb = kbuf;  // [fc_out_tiles][nt], free until the first batch
-    const int n_ss = p.fc_out_tiles * nt;
-    for (int i = et; i < n_ss; i += 128) {
-      const int q = i / nt, j = i - q * nt;
-      ssb[i] = p.ss[static_cast<size_t>(q) * p.n_tok + t0 + j];
-    }
-    named_bar_sync(1, 128);
-    for (int j = et; j < nt; j += 128) {
-      float tot = 0.f;
-      for (int q = 0; q < p.fc_out_tiles; ++q) tot += ssb[q * nt + j];
-      rbuf[j] = rsqrtf(tot / p.hidden + p.rms_eps);
-    }
-  } else {
-    for (int j = et; j < nt; j += 128) rbuf[j] = 1.f;
+  float* rbuf = reinterpret_cast<float*>(scratch);                  // [chunk_rows]
+  long long* dst_off = reinterpret_cast<long long*>(scratch + 1024); // [chunk_rows], -1 = skip
+  int* posb = reinterpret_cast<int*>(scratch + 1024 + 8 * 256);     // [chunk_rows]
+  float* rope_hi = reinterpret_cast<float*>(scratch + 4096);        // [D/2], read by index
+  float* rope_lo = rope_hi + 64;
+  if (et < D / 2) {
+    rope_hi[et] = p.rope.hi[et];
+    rope_lo[et] = p.rope.lo[et];
   }
-  named_bar_sync(1, 128);
-  const float gk = (is_k && p.k_norm_w) ? bf16_bits_to_float(p.k_norm_w[d]) : 1.f;
-  const int half = D / 2;
-  const int fi = d < half ? d : d - half;
   const dflash_kv_view& cv = p.cache;
   const int limit = cv.page_table ? cv.max_pages * cv.page_size : cv.capacity;
-  uint16_t* dst_base = static_cast<uint16_t*>(is_k ? cv.k : cv.v);
-  for (int j0 = 0; j0 < nt; j0 += kTokBatch) {
-    const int n = min(kTokBatch, nt - j0);
-    float val[kTokBatch];
-    take_sums(p, t0 + j0, n, o * 128 + et, val);
-#pragma unroll
-    for (int j = 0; j < kTokBatch; ++j) val[j] *= j < n ? rbuf[j0 + j] : 0.f;
-    if (is_k) {
-      if (p.k_norm_w) {
-#pragma unroll
-        for (int j = 0; j < kTokBatch; ++j) {
-          float sq = val[j] * val[j];
-#pragma unroll
-          for (int off = 16; off; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-          if (lane == 0) red[warp * kTokBatch + j] = sq;
-        }
-        named_bar_sync(1, 128);
-#pragma unroll
-        for (int j = 0; j < kTokBatch; ++j) {
-          const float tot = D == 128 ? red[j] + red[kTokBatch + j] + red[2 * kTokBatch + j] +
-                                           red[3 * kTokBatch + j]
-                                     : red[(warp >> 1) * 2 * kTokBatch + j] +
-                                           red[((warp >> 1) * 2 + 1) * kTokBatch + j];
-          val[j] = val[j] * rsqrtf(tot / D + p.rms_eps) * gk;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kTokBatch; ++j) kbuf[j * 128 + et] = val[j];
-      named_bar_sync(1, 128);
-#pragma unroll
-      for (int j = 0; j < kTokBatch; ++j) {
-        const int tok = t0 + j0 + j;
-        const int b = tok / kBlock;
-        const int pos = (j < n ? p.pos_snapshot[b] : 0) + (tok - b * kBlock);
-        float sn, cs;
-        rope_sincos(pos, p.rope.hi[fi], p.rope.lo[fi], &sn, &cs);
-        const float partner = d < half ? kbuf[j * 128 + et + half] : kbuf[j * 128 + et - half];
-        val[j] = d < half ? val[j] * cs - partner * sn : val[j] * cs + partner * sn;
-      }
-      named_bar_sync(1, 128);  // kbuf and red are reused by the next batch
-    }
-#pragma unroll
-    for (int j = 0; j < kTokBatch; ++j) {
-      if (j >= n) continue;
-      const int tok = t0 + j0 + j;
-      const int b = tok / kBlock, t = tok - b * kBlock;
-      const int pos0 = p.pos_snapshot[b];
-      if (pos0 < 0 || pos0 + kBlock > limit) continue;  // flagged by the reservation
+  // head-major caches: [B, Hkv, capacity, D] or [pages, Hkv, page_size, D]
+  const long long head_stride =
+      static_cast<long long>(cv.page_table ? cv.page_size : cv.capacity) * D;
+  for (int j = et; j < nt; j += 128) {
+    const int tok = t0 + j;
+    const int b = tok / kBlock, t = tok - b * kBlock;
+    const int pos0 = p.pos_snapshot[b];
+    long long off = -1;
+    if (pos0 >= 0 && pos0 + kBlock <= limit) {  // else flagged by the reservation
       const int pos = pos0 + t;
-      // head-major caches: [B, Hkv, capacity, D] or [pages, Hkv, page_size, D]
-      size_t off;
       if (cv.page_table) {
         const int page =
             cv.page_table[static_cast<size_t>(b) * cv.max_pages + pos / cv.page_size];
-        if (page < 0) {
-          if (et == 0) set_status(p.status, DFLASH_ST_PAGE_MISSING);
-          continue;
-        }
-        off = ((static_cast<size_t>(page) * p.n_kv_heads + head) * cv.page_size +
-               pos % cv.page_size) * D + d;
+        if (page >= 0)
+          off = (static_cast<long long>(page) * p.n_kv_heads * cv.page_size + pos % cv.page_size) * D;
+        else
+          set_status(p.status, DFLASH_ST_PAGE_MISSING);
       } else {
-        off = ((static_cast<size_t>(b) * p.n_kv_heads + head) * cv.capacity + pos) * D + d;
+        off = (static_cast<long long>(b) * p.n_kv_heads * cv.capacity + pos) * D;
       }
-      dst_base[off] = float_to_bf16_bits(val[j]);
+    }
+    dst_off[j] = off;
+    posb[j] = pos0 + t;
+    float r = 1.f;
+    if (p.hidden_norm_w) {
+      float tot = 0.f;
+      for (int q = 0; q < p.fc_out_tiles; ++q) tot += p.ss[static_cast<size_t>(q) * p.n_tok + tok];
+      r = rsqrtf(tot / p.hidden + p.rms_eps);
+    }
+    rbuf[j] = r;
+  }
+  named_bar_sync(1, 128);
+  const float4 gk = (is_k && p.k_norm_w) ? load4_bf16(p.k_norm_w + d0) : make_float4(1.f, 1.f, 1.f, 1.f);
+  const int half = D / 2;
+  const bool lower = d0 < half;
+  const int fi = lower ? d0 : d0 - half;                   // first of 4 frequencies
+  uint16_t* dst_base = static_cast<uint16_t*>(is_k ? cv.k : cv.v);
+#pragma unroll 1
+  for (int j0 = warp * kTokGroup; j0 < nt; j0 += 4 * kTokGroup) {
+    float4 v[kTokGroup];
+#pragma unroll
+    for (int k = 0; k < kTokGroup; ++k)
+      if (j0 + k < nt) v[k] = take4(p, t0 + j0 + k, o * 128 + lane * 4);
+#pragma unroll
+    for (int k = 0; k < kTokGroup; ++k) {
+      if (j0 + k >= nt) break;
+      const int j = j0 + k;
+      const float r = rbuf[j];
+      float x[4] = {v[k].x * r, v[k].y * r, v[k].z * r, v[k].w * r};
+      if (is_k) {
+        if (p.k_norm_w) {
+          float sq = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+          for (int off = D / 8; off; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+          const float rs = rsqrtf(sq / D + p.rms_eps);
+          x[0] *= rs * gk.x;
+          x[1] *= rs * gk.y;
+          x[2] *= rs * gk.z;
+          x[3] *= rs * gk.w;
+        }
+        const int pos = posb[j];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float partner = __shfl_xor_sync(0xffffffffu, x[e], D / 8);
+          float sn, cs;
+          rope_sincos(pos, rope_hi[fi + e], rope_lo[fi + e], &sn, &cs);
+          x[e] = lower ? x[e] * cs - partner * sn : x[e] * cs + partner * sn;
+        }
+      }
+      const long long off = dst_off[j];
+      if (off >= 0)
+        *reinterpret_cast<uint2*>(dst_base + off + head * head_stride + d0) =
+            pack4_bf16(x[0], x[1], x[2], x[3]);
     }
   }
 }
@@ -482,12 +492,11 @@ streamk_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0,
     // finish the tiles this CTA completed; the pipeline is drained, so its
     // shared memory is free for the finisher
     __threadfence();
-    float* scratch = reinterpret_cast<float*>(smem);
     const int nf = *n_fin;
     for (int i = 0; i < nf; ++i) {
       const int T = fin_tiles[i];
       const int o = T % p.out_tiles, c = T / p.out_tiles;
-      if (p.mode == kModeFc) finish_fc(p, o, c, scratch); else finish_kv(p, o, c, scratch);
+      if (p.mode == kModeFc) finish_fc(p, o, c); else finish_kv(p, o, c, smem);
       named_bar_sync(1, 128);  // scratch is reused by the next tile
       if (threadIdx.x == 64) p.tickets[T] = 0u;
     }
