@@ -7,7 +7,10 @@ dflash_ctx_project, dflash_kv_crop over the target and drafter views,
 dflash_block_attention) over one batch of synthetic inputs already resident
 in HBM.  Every step replays the same cycle from the same state: the block is
 written at a fixed context position, the crop trims it to the committed
-length and the attention of the next block reads that length.
+length and the attention of the next block reads that length.  Verification
+and the projection run side by side on two streams, each on its own share of
+the SMs (the split is measured once before the warm-up; --sm-split fixes it,
+--serial queues everything on one stream).
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 N > 1 runs under torchrun: every rank runs an independent replica (sequences
