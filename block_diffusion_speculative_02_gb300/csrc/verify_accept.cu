@@ -33,7 +33,17 @@ namespace {
 constexpr int kThreads = 192;
 constexpr int kTileRows = 128;           // vocabulary rows per MMA (M)
 constexpr int kATileBytes = kTileRows * 128;
-constexpr int kUnitRows = 8;             // balancing granule = one 8-row TMA box
+#ifndef DFLASH_LM_UNIT_ROWS
+#define DFLASH_LM_UNIT_ROWS 8
+#endif
+constexpr int kUnitRows = DFLASH_LM_UNIT_ROWS;  // balancing granule of the vocabulary split (8..128)
+
+// Tensor maps over W_lm with boxes of 64, 32, 16 and 8 rows: a CTA's last,
+// partial tile (its range is balanced to 8 rows) is loaded as at most four
+// boxes -- one per set bit of its row count -- instead of one per 8 rows.
+struct PartialMaps {
+  CUtensorMap m[4];
+};
 constexpr int kSmemBudget = 224 * 1024;
 constexpr int kMaxStages = 12;
 #ifndef DFLASH_LM_CHUNKS_PER_STAGE
@@ -107,7 +117,7 @@ __device__ __forceinline__ void accept_and_commit(const LmParams& p, int b) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 lmhead_argmax_accept_kernel(const __grid_constant__ CUtensorMap tm_w,
-                            const __grid_constant__ CUtensorMap tm_w8,
+                            const __grid_constant__ PartialMaps tm_part,
                             const __grid_constant__ CUtensorMap tm_x, const LmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
@@ -151,7 +161,6 @@ lmhead_argmax_accept_kernel(const __grid_constant__ CUtensorMap tm_w,
   for (int i = threadIdx.x; i < p.ntok; i += kThreads) best[i] = 0ull;
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_w);
-    tma_prefetch_desc(&tm_w8);
     tma_prefetch_desc(&tm_x);
   }
   if (warp == 1) {
@@ -179,11 +188,16 @@ lmhead_argmax_accept_kernel(const __grid_constant__ CUtensorMap tm_w,
       uint32_t stage = 0, phase = 0;
       int issued = 0;
       bool ok = true;
+      // Every CTA walks the hidden dimension starting at its own k-stage: CTAs
+      // that stream in lockstep at the same column offset of their rows hit
+      // the same DRAM channels (measured: 7 % slower); rotated starts spread
+      // the requests.  The accumulation order only changes fp32 rounding.
+      const int k_rot = blockIdx.x % k_stages;
       for (int t = 0; t < n_tiles && ok; ++t) {
         const int row0 = r0 + t * kTileRows;
         const int rows = min(kTileRows, r1 - row0);
-        const int nb8 = (rows + kUnitRows - 1) / kUnitRows;
-        const uint32_t a_bytes = rows == kTileRows ? kATileBytes : nb8 * 1024;
+        const int rows8 = (rows + 7) & ~7;    // boxes past the vocabulary are zero-filled
+        const uint32_t a_bytes = static_cast<uint32_t>(rows8) * 128;
         for (int ks = 0; ks < k_stages; ++ks) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
             ok = false;
@@ -194,15 +208,22 @@ lmhead_argmax_accept_kernel(const __grid_constant__ CUtensorMap tm_w,
           mbar_arrive_expect_tx(&full[stage], p.kb * (a_bytes + x_bytes));
           // the kb chunks of one stage are issued back to back, so every
           // vocabulary row is requested as kb*128 contiguous bytes at once
+          const int ksr = ks + k_rot < k_stages ? ks + k_rot : ks + k_rot - k_stages;
           for (int j = 0; j < p.kb; ++j) {
-            const int kcol = (ks * p.kb + j) * 64;
+            const int kcol = (ksr * p.kb + j) * 64;
             uint8_t* aj = a + j * kATileBytes;
             if (rows == kTileRows) {
               tma_load_2d(aj, &tm_w, &full[stage], kcol, row0, pol_w);
             } else {
-              for (int i = 0; i < nb8; ++i)
-                tma_load_2d(aj + 1024 * i, &tm_w8, &full[stage], kcol, row0 + kUnitRows * i,
-                            pol_w);
+              int off = 0;
+              for (int bi = 0; bi < 4; ++bi) {
+                const int br = 64 >> bi;
+                if (rows8 & br) {
+                  tma_load_2d(aj + off * 128, &tm_part.m[bi], &full[stage], kcol, row0 + off,
+                              pol_w);
+                  off += br;
+                }
+              }
             }
             for (int c = 0; c < p.n_xbox; ++c)
               tma_load_2d(b + j * p.x_chunk + c * p.ntok_box * 128, &tm_x, &full[stage], kcol,
@@ -384,12 +405,15 @@ extern "C" int dflash_verify_accept(const dflash_dims* dims, const void* hidden,
   p.out_tokens = out_tokens;
   p.out_cap = out_cap;
 
-  CUtensorMap tm_w, tm_w8, tm_x;
+  CUtensorMap tm_w, tm_x;
+  PartialMaps tm_part;
   const uint64_t pitch = static_cast<uint64_t>(dims->hidden) * 2;
   if ((rc = make_tmap_2d_bf16(&tm_w, w_lm, dims->hidden, dims->vocab, pitch, 64, kTileRows)))
     return rc;
-  if ((rc = make_tmap_2d_bf16(&tm_w8, w_lm, dims->hidden, dims->vocab, pitch, 64, kUnitRows)))
-    return rc;
+  for (int bi = 0; bi < 4; ++bi)
+    if ((rc = make_tmap_2d_bf16(&tm_part.m[bi], w_lm, dims->hidden, dims->vocab, pitch, 64,
+                                64 >> bi)))
+      return rc;
   if ((rc = make_tmap_2d_bf16(&tm_x, hidden, dims->hidden, p.ntok, pitch, 64, p.ntok_box)))
     return rc;
 
@@ -398,7 +422,7 @@ extern "C" int dflash_verify_accept(const dflash_dims* dims, const void* hidden,
     return rc;
   const int grid = plan.budget_sms < p.n_units ? plan.budget_sms : p.n_units;
   return launch(lmhead_argmax_accept_kernel, dim3(grid), dim3(kThreads), smem,
-                reinterpret_cast<cudaStream_t>(stream), tm_w, tm_w8, tm_x, p);
+                reinterpret_cast<cudaStream_t>(stream), tm_w, tm_part, tm_x, p);
 }
 
 // ---------------------------------------------------------------------------
@@ -501,12 +525,15 @@ extern "C" int dflash_verify_accept_noalloc(const dflash_dims* dims, const void*
   p.out_tokens = out_tokens;
   p.out_cap = out_cap;
 
-  CUtensorMap tm_w, tm_w8, tm_x;
+  CUtensorMap tm_w, tm_x;
+  PartialMaps tm_part;
   const uint64_t pitch = static_cast<uint64_t>(dims->hidden) * 2;
   if ((rc = make_tmap_2d_bf16(&tm_w, w_lm, dims->hidden, dims->vocab, pitch, 64, kTileRows)))
     return rc;
-  if ((rc = make_tmap_2d_bf16(&tm_w8, w_lm, dims->hidden, dims->vocab, pitch, 64, kUnitRows)))
-    return rc;
+  for (int bi = 0; bi < 4; ++bi)
+    if ((rc = make_tmap_2d_bf16(&tm_part.m[bi], w_lm, dims->hidden, dims->vocab, pitch, 64,
+                                64 >> bi)))
+      return rc;
   if ((rc = make_tmap_2d_bf16(&tm_x, hidden, dims->hidden, p.ntok, pitch, 64, p.ntok_box)))
     return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -516,6 +543,6 @@ extern "C" int dflash_verify_accept_noalloc(const dflash_dims* dims, const void*
   if ((rc = set_smem_limit(reinterpret_cast<const void*>(lmhead_argmax_accept_kernel), smem)))
     return rc;
   const int grid = plan.budget_sms < p.n_units ? plan.budget_sms : p.n_units;
-  return launch(lmhead_argmax_accept_kernel, dim3(grid), dim3(kThreads), smem, st, tm_w, tm_w8,
+  return launch(lmhead_argmax_accept_kernel, dim3(grid), dim3(kThreads), smem, st, tm_w, tm_part,
                 tm_x, p);
 }
