@@ -404,7 +404,7 @@ def main(argv=None):
     __graft_entry__.build()
     world, rank = init_dist("nccl")
     import block_diffusion_speculative_02_gb300 as dfl
-    from block_diffusion_speculative_02_gb300.cycle import run_cycle, side_stream, tune_sm_split
+    from block_diffusion_speculative_02_gb300.cycle import CycleGraph, side_stream, tune_sm_split
 
     kv_bytes_per_set = 2 * cfg.n_kv_heads * cfg.head_dim * 2 * (
         cfg.batch * (cfg.ctx_len or cfg.ctx_len_range[1]) + 32)
@@ -536,19 +536,17 @@ def main(argv=None):
         host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
         h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = sum(t.numel() * t.element_size() for t in host_out)
+        # the serving loop of a fixed-shape batch: the whole cycle, copies in
+        # and out included, as one CUDA graph launched per step
+        cg = CycleGraph(dims, w, st0, ws, list(zip(host_in, ins)), list(zip(outs, host_out)),
+                        1.0 / math.sqrt(cfg.head_dim), concurrent=concurrent,
+                        sm_split=(verify_sms, project_sms) if concurrent else None)
         for _ in range(3):
-            for d_, h_ in zip(ins, host_in):
-                d_.copy_(h_, non_blocking=True)
-            step(0)
-        torch.cuda.synchronize()
+            cg.replay()
+            torch.cuda.current_stream().synchronize()
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
-            for d_, h_ in zip(ins, host_in):
-                d_.copy_(h_, non_blocking=True)
-            run_cycle(dims, w, st0, ws, 1.0 / math.sqrt(cfg.head_dim), concurrent=concurrent,
-                      sm_split=(verify_sms, project_sms) if concurrent else None)
-            for h_, d_ in zip(host_out, outs):
-                h_.copy_(d_, non_blocking=True)
+            cg.replay()
             torch.cuda.current_stream().synchronize()
         e2e_s = time.perf_counter() - t0
         e2e_s = max_over_ranks(e2e_s, device="cuda")

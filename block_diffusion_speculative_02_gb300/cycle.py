@@ -147,3 +147,44 @@ def run_cycle(dims: Dims, w: CycleWeights, st: CycleState, ws: torch.Tensor,
     dflash_kv_crop([st.target_view, st.draft_cache], st.commit_len, dims.batch, ws, main)
     dflash_block_attention(dims, st.q_blk, st.k_blk, st.v_blk, st.draft_cache, scale,
                            st.attn_out, ws, main)
+
+
+class CycleGraph:
+    """One whole cycle -- the host-to-device copy of the step's inputs, the
+    four calls, the device-to-host copy of its results -- captured once as a
+    CUDA graph and replayed per step, so that the per-step host work is one
+    graph launch (the serving loop of a fixed-shape batch).
+
+    ``inputs``: (pinned host tensor, device tensor) pairs copied in every step;
+    ``outputs``: (device tensor, pinned host tensor) pairs copied out.  The
+    other arguments are those of :func:`run_cycle`.  Capturing runs the cycle
+    once beforehand (outside the graph) to settle every lazy setup."""
+
+    def __init__(self, dims: Dims, w: CycleWeights, st: CycleState, ws: torch.Tensor,
+                 inputs, outputs, scale: Optional[float] = None, concurrent: bool = True,
+                 sm_split: Optional[Tuple[int, int]] = None):
+        self._args = (dims, w, st, ws, scale, concurrent, sm_split)
+        self.inputs = list(inputs)
+        self.outputs = list(outputs)
+        warm = torch.cuda.Stream()
+        warm.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(warm):
+            self._body()
+        torch.cuda.current_stream().wait_stream(warm)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self._body()
+        torch.cuda.synchronize()
+
+    def _body(self):
+        dims, w, st, ws, scale, concurrent, sm_split = self._args
+        for h, d in self.inputs:
+            d.copy_(h, non_blocking=True)
+        run_cycle(dims, w, st, ws, scale, concurrent=concurrent, sm_split=sm_split)
+        for d, h in self.outputs:
+            h.copy_(d, non_blocking=True)
+
+    def replay(self):
+        """Launch one cycle on the current stream (asynchronous)."""
+        self.graph.replay()

@@ -129,3 +129,80 @@ def test_three_cycles_carry_state(paged, concurrent):
         assert mapped.isdisjoint(free) and len(mapped) + len(free) == lay.n_pages
         for b in range(B):
             assert (table[b] >= 0).sum() == -(-int(L[b]) // 16)
+
+
+def test_cycle_graph_matches_direct_calls():
+    """CycleGraph (copies in, the four calls, copies out, one CUDA graph) gives
+    the same tokens, lengths and attention output as issuing the calls."""
+    import block_diffusion_speculative_02_gb300 as dfl
+    from block_diffusion_speculative_02_gb300.cycle import (CycleGraph, CycleState, CycleWeights,
+                                                            run_cycle)
+
+    rng = np.random.default_rng(7)
+    B, H, Hq, Hkv, D, V, nL, cap = 2, 256, 4, 2, 64, 4096, 2, 200
+    L0 = np.array([90, 41], np.int32)
+    dims = dfl.make_dims(B, H, Hq, Hkv, D, V, nL, cap)
+    w = CycleWeights(*(dev_bf16(x) for x in (
+        normal_bf16(rng, (V, H), 0.02), normal_bf16(rng, (H, nL * H), 0.02),
+        normal_bf16(rng, (H,), 0.02, 1.0), normal_bf16(rng, (Hkv * D, H), 0.02),
+        normal_bf16(rng, (Hkv * D, H), 0.02), normal_bf16(rng, (D,), 0.02, 1.0))))
+    ck = pack_contiguous_heads([normal_bf16(rng, (int(L), Hkv, D)) for L in L0], cap, Hkv, D)
+    cv = pack_contiguous_heads([normal_bf16(rng, (int(L), Hkv, D)) for L in L0], cap, Hkv, D)
+    host = {"verify_hidden": unit_rms_rows_bf16(rng, (B * 16, H)),
+            "layers": [unit_rms_rows_bf16(rng, (B * 16, H)) for _ in range(nL)],
+            "block_ids": rng.integers(0, V, size=(B, 16)).astype(np.int32),
+            "q": normal_bf16(rng, (B, 16, Hq, D)), "k": normal_bf16(rng, (B, 16, Hkv, D)),
+            "v": normal_bf16(rng, (B, 16, Hkv, D))}
+
+    def state():
+        draft = dfl.KVView(dev_bf16(ck), dev_bf16(cv), dev_i32(L0), capacity=cap)
+        commit = dev_i32(L0)
+        return CycleState(
+            layer_hidden=[torch.zeros((B * 16, H), dtype=torch.bfloat16, device="cuda")
+                          for _ in range(nL)],
+            verify_hidden=torch.zeros((B * 16, H), dtype=torch.bfloat16, device="cuda"),
+            block_ids=torch.zeros((B, 16), dtype=torch.int32, device="cuda"),
+            len_before=commit, write_pos=draft.seq_len,
+            q_blk=torch.zeros((B, 16, Hq, D), dtype=torch.bfloat16, device="cuda"),
+            k_blk=torch.zeros((B, 16, Hkv, D), dtype=torch.bfloat16, device="cuda"),
+            v_blk=torch.zeros((B, 16, Hkv, D), dtype=torch.bfloat16, device="cuda"),
+            draft_cache=draft, target_view=dfl.KVView(None, None, dev_i32(L0 + 16), capacity=cap),
+            posterior=torch.zeros((B, 16), dtype=torch.int32, device="cuda"),
+            accept_len=torch.zeros(B, dtype=torch.int32, device="cuda"),
+            next_staged=torch.zeros(B, dtype=torch.int32, device="cuda"), commit_len=commit,
+            out_tokens=torch.full((B, cap + 16), -1, dtype=torch.int32, device="cuda"),
+            attn_out=torch.zeros((B, 16, Hq, D), dtype=torch.bfloat16, device="cuda"))
+
+    def inputs_of(st):
+        dev = [st.verify_hidden, *st.layer_hidden, st.block_ids, st.q_blk, st.k_blk, st.v_blk]
+        src = [host["verify_hidden"], *host["layers"], host["block_ids"], host["q"], host["k"],
+               host["v"]]
+        pairs = []
+        for d, h in zip(dev, src):
+            t = torch.from_numpy(np.ascontiguousarray(h).view(np.int16) if h.dtype == np.uint16
+                                 else np.ascontiguousarray(h))
+            pairs.append((t.view(d.dtype).pin_memory(), d))
+        return pairs
+
+    a = state()
+    for h, d in inputs_of(a):
+        d.copy_(h)
+    run_cycle(dims, w, a, dfl.alloc_workspace(dims))
+    b = state()
+    outs = [b.accept_len, b.posterior, b.commit_len]
+    host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    # the graph's warm-up run moves the state once: capture on a throw-away copy
+    # of the lengths, then restore them and replay the captured cycle
+    saved = [b.draft_cache.seq_len.clone(), b.commit_len.clone(), b.target_view.seq_len.clone()]
+    g = CycleGraph(dims, w, b, dfl.alloc_workspace(dims), inputs_of(b), list(zip(outs, host_out)))
+    for t, s in zip([b.draft_cache.seq_len, b.commit_len, b.target_view.seq_len], saved):
+        t.copy_(s)
+    b.out_tokens.fill_(-1)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(host_out[0].numpy(), a.accept_len.cpu().numpy())
+    assert np.array_equal(host_out[1].numpy(), a.posterior.cpu().numpy())
+    assert np.array_equal(host_out[2].numpy(), a.commit_len.cpu().numpy())
+    assert np.array_equal(b.out_tokens.cpu().numpy(), a.out_tokens.cpu().numpy())
+    assert np.array_equal(b.draft_cache.seq_len.cpu().numpy(), a.draft_cache.seq_len.cpu().numpy())
+    np.testing.assert_allclose(host_f64(b.attn_out), host_f64(a.attn_out), atol=2e-2)
