@@ -20,6 +20,7 @@ line with the whole-job throughput over the max-over-ranks time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -404,7 +405,8 @@ def main(argv=None):
     __graft_entry__.build()
     world, rank = init_dist("nccl")
     import block_diffusion_speculative_02_gb300 as dfl
-    from block_diffusion_speculative_02_gb300.cycle import CycleGraph, side_stream, tune_sm_split
+    from block_diffusion_speculative_02_gb300.cycle import (CycleGraph, packed_tensors,
+                                                            side_stream, tune_sm_split)
 
     kv_bytes_per_set = 2 * cfg.n_kv_heads * cfg.head_dim * 2 * (
         cfg.batch * (cfg.ctx_len or cfg.ctx_len_range[1]) + 32)
@@ -528,17 +530,30 @@ def main(argv=None):
     # ---- end to end: host buffers in, results out, every step ----
     e2e = None
     if args.e2e_steps > 0:
-        st0 = states[0]
-        ins = [st0.verify_hidden, *st0.layer_hidden, st0.block_ids, st0.q_blk, st0.k_blk,
-               st0.v_blk]
-        host_in = [t.detach().cpu().pin_memory() for t in ins]
-        outs = [st0.accept_len, st0.next_staged, st0.commit_len, st0.posterior]
-        host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
-        h2d = sum(t.numel() * t.element_size() for t in host_in)
-        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        # the step's inputs (verify hidden, selected layer hidden states, block
+        # ids, block Q/K/V) and results (acceptance, next staged token, commit
+        # length, posterior) live in one device buffer each, so that every step
+        # moves them with one host-to-device and one device-to-host copy
+        src = states[0]
+        in_t = [src.verify_hidden, *src.layer_hidden, src.block_ids, src.q_blk, src.k_blk,
+                src.v_blk]
+        out_t = [src.accept_len, src.next_staged, src.commit_len, src.posterior]
+        dev_in, ins = packed_tensors([(t.shape, t.dtype) for t in in_t], "cuda")
+        dev_out, outs = packed_tensors([(t.shape, t.dtype) for t in out_t], "cuda")
+        for d_, t in zip(ins, in_t):
+            d_.copy_(t)
+        st0 = dataclasses.replace(
+            src, verify_hidden=ins[0], layer_hidden=ins[1:1 + len(src.layer_hidden)],
+            block_ids=ins[-4], q_blk=ins[-3], k_blk=ins[-2], v_blk=ins[-1],
+            accept_len=outs[0], next_staged=outs[1], commit_len=outs[2], posterior=outs[3])
+        st0.commit_len.copy_(src.commit_len)
+        host_in = dev_in.cpu().pin_memory()
+        host_out = torch.empty_like(dev_out, device="cpu").pin_memory()
+        h2d = host_in.numel()
+        d2h = host_out.numel()
         # the serving loop of a fixed-shape batch: the whole cycle, copies in
         # and out included, as one CUDA graph launched per step
-        cg = CycleGraph(dims, w, st0, ws, list(zip(host_in, ins)), list(zip(outs, host_out)),
+        cg = CycleGraph(dims, w, st0, ws, [(host_in, dev_in)], [(dev_out, host_out)],
                         1.0 / math.sqrt(cfg.head_dim), concurrent=concurrent,
                         sm_split=(verify_sms, project_sms) if concurrent else None)
         for _ in range(3):

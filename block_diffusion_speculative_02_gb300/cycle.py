@@ -149,6 +149,31 @@ def run_cycle(dims: Dims, w: CycleWeights, st: CycleState, ws: torch.Tensor,
                            st.attn_out, ws, main)
 
 
+def packed_tensors(specs, device, pin: bool = False):
+    """One flat buffer and views into it, one per (shape, dtype) in ``specs``
+    (each view 256-byte aligned), so that a whole set of a step's inputs or
+    outputs moves between host and device as a single copy."""
+    offs, off = [], 0
+    for shape, dtype in specs:
+        off = (off + 255) // 256 * 256
+        offs.append(off)
+        n = 1
+        for x in shape:
+            n *= int(x)
+        off += n * torch.empty((), dtype=dtype).element_size()
+    flat = torch.empty(off, dtype=torch.uint8, device=device)
+    if pin:
+        flat = flat.pin_memory()
+    views = []
+    for (shape, dtype), o in zip(specs, offs):
+        n = 1
+        for x in shape:
+            n *= int(x)
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        views.append(flat[o:o + nbytes].view(dtype).view(*shape))
+    return flat, views
+
+
 class CycleGraph:
     """One whole cycle -- the host-to-device copy of the step's inputs, the
     four calls, the device-to-host copy of its results -- captured once as a
