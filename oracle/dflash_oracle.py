@@ -191,6 +191,68 @@ def lm_head_argmax(hidden, w_lm, chunk: int = 8192) -> dict:
     return {"posterior": idx.astype(np.int32), "max": best, "gap": best - second}
 
 
+# ---------------------------------------------------------------------------
+# next: the rest of one drafter layer and the drafter's token choice
+# ---------------------------------------------------------------------------
+def draft_qkv(x, ln1_w, w_q, w_k, w_v, q_norm_w, k_norm_w, n_q_heads: int, n_kv_heads: int,
+              head_dim: int, rms_eps: float) -> dict:
+    """Block Q/K/V of one drafter layer, before the rotary embedding.
+
+    [P1] §1: the drafter is built from Qwen3 components (RMSNorm, rotary
+    embedding, MLP), i.e. a pre-norm decoder layer whose attention projections
+    are followed by a per-head RMSNorm of q and k; [P2] 块扩散草稿 steps 1-2:
+    the whole block (staged token + 15 masks) goes through one forward.
+        h = RMSNorm(x) * ln1
+        q = RMSNorm_head(h W_q^T) * q_norm,  k = RMSNorm_head(h W_k^T) * k_norm
+        v = h W_v^T
+    x [N, H] (the layer input rows, N = 16 per sequence).  Returns h [N, H],
+    q [N, Hq, D], k, v [N, Hkv, D] (the attention rotates q and k itself).
+    """
+    h = rms_norm(as_f64(x), ln1_w, rms_eps)
+    N = h.shape[0]
+    q = (h @ as_f64(w_q).T).reshape(N, n_q_heads, head_dim)
+    k = (h @ as_f64(w_k).T).reshape(N, n_kv_heads, head_dim)
+    v = (h @ as_f64(w_v).T).reshape(N, n_kv_heads, head_dim)
+    if q_norm_w is not None:
+        q = rms_norm(q, q_norm_w, rms_eps)
+    if k_norm_w is not None:
+        k = rms_norm(k, k_norm_w, rms_eps)
+    return {"h": h, "q": q, "k": k, "v": v}
+
+
+def silu(x):
+    """x * sigmoid(x), the activation of the Qwen3 MLP."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / (1.0 + np.exp(-x))
+
+
+def draft_out_mlp(x, attn_out, w_o, ln2_w, w_gate, w_up, w_down, rms_eps: float) -> dict:
+    """The rest of one drafter layer after its attention ([P1] §1, Qwen3
+    decoder layer with the Qwen3 MLP):
+        x1 = x + O W_o^T                       (O = attention output rows, [N, Hq*D])
+        x2 = x1 + (silu(h2 W_gate^T) * (h2 W_up^T)) W_down^T,  h2 = RMSNorm(x1) * ln2
+    Returns x1, x2 [N, H]."""
+    x = as_f64(x)
+    N = x.shape[0]
+    x1 = x + as_f64(attn_out).reshape(N, -1) @ as_f64(w_o).T
+    h2 = rms_norm(x1, ln2_w, rms_eps)
+    m = silu(h2 @ as_f64(w_gate).T) * (h2 @ as_f64(w_up).T)
+    x2 = x1 + m @ as_f64(w_down).T
+    return {"x1": x1, "x2": x2}
+
+
+def draft_tokens(x, final_norm_w, w_lm, rms_eps: float, chunk: int = 8192) -> dict:
+    """The drafter's prediction for every block position: greedy argmax of
+    RMSNorm(x) * final_norm W_lm^T (the drafter shares the target's LM head);
+    the mask positions 1..15 are the drafted tokens ([P2] 块扩散草稿 step 2).
+    x [B*16, H].  Returns the argmax, gap and max per row (as lm_head_argmax)
+    and tokens [B, 15]."""
+    hn = rms_norm(as_f64(x), final_norm_w, rms_eps)
+    r = lm_head_argmax(hn, w_lm, chunk)
+    r["tokens"] = r["posterior"].reshape(-1, BLOCK)[:, 1:].copy()
+    return r
+
+
 def acceptance_length(drafted, posterior) -> int:
     """[P2] 保证二: matches = (drafted == posterior); a = sum(cumprod(matches)).
 

@@ -23,7 +23,8 @@ from dataclasses import dataclass
 import numpy as np
 
 from .dflash_oracle import (BLOCK, acceptance_length, apply_rope, block_attention,
-                            ctx_project, kv_crop_lengths, rms_norm, verify_accept)
+                            ctx_project, draft_out_mlp, draft_qkv, draft_tokens,
+                            kv_crop_lengths, rms_norm, verify_accept)
 
 
 def _rows(x: np.ndarray, w: np.ndarray) -> np.ndarray:
@@ -190,18 +191,14 @@ class TinyDrafter:
         blk = np.full(T, self.mask_id)
         blk[0] = staged
         x = self.t.embed[blk]
-        hn = rms_norm(x, lay.ln1, d.rms_eps)
-        q = rms_norm(_rows(hn, lay.wq).reshape(T, d.n_q_heads, d.head_dim), lay.q_norm,
-                     d.rms_eps)
-        k = rms_norm(_rows(hn, lay.wk).reshape(T, d.n_kv_heads, d.head_dim), lay.k_norm,
-                     d.rms_eps)
-        v = _rows(hn, lay.wv).reshape(T, d.n_kv_heads, d.head_dim)
-        o = block_attention(q[None], k[None], v[None], [self.ctx_k], [self.ctx_v],
-                            [self.ctx_len], d.rope_theta, 1.0 / np.sqrt(d.head_dim))[0]
-        x = x + _rows(o.reshape(T, -1), lay.wo)
-        x = lay.mlp(x, d.rms_eps)
-        logits = _rows(rms_norm(x, self.final_norm, d.rms_eps), self.t.lm_head)
-        return np.argmax(logits[1:], axis=1).astype(np.int32)
+        r = draft_qkv(x, lay.ln1, lay.wq, lay.wk, lay.wv, lay.q_norm, lay.k_norm, d.n_q_heads,
+                      d.n_kv_heads, d.head_dim, d.rms_eps)
+        o = block_attention(r["q"][None], r["k"][None], r["v"][None], [self.ctx_k],
+                            [self.ctx_v], [self.ctx_len], d.rope_theta,
+                            1.0 / np.sqrt(d.head_dim))[0]
+        x2 = draft_out_mlp(x, o, lay.wo, lay.ln2, lay.w_gate, lay.w_up, lay.w_down,
+                           d.rms_eps)["x2"]
+        return draft_tokens(x2, self.final_norm, self.t.lm_head, d.rms_eps)["tokens"][0]
 
 
 def greedy_decode(target: TinyTarget, prompt, n_new: int) -> list:
