@@ -44,6 +44,24 @@ struct Plan {
       off_kv, off_att_o, off_att_ml, total;
 };
 
+// Workspace plan of the drafter-layer calls (dflash_draft_*).  The buffers
+// that do not depend on the MLP size come first (up to ffn_begin).
+struct DraftPlan {
+  int num_sms, budget_sms, ntok;
+  int qkv_tiles, o_tiles, gu_tiles, down_tiles;  // output tiles of 128 features
+  size_t off_status, off_lm_ticket, off_tickets_qkv, off_tickets_o, off_keys, off_ss_rows,
+      off_ss_x1, off_xhl, off_x1, off_xg, off_acc_a, ffn_begin, off_tickets_gu,
+      off_tickets_down, off_mhl, off_acc_b, total;
+};
+
+int make_draft_plan(const dflash_dims& d, int ffn, DraftPlan* p);
+
+// Per token row of x [n_tok, H] bf16: sum(x^2) into ss (if not null), and
+// x * gain either as a hi/lo bf16 pair into hl [2, n_tok, H] or rounded once
+// into out [n_tok, H] (whichever is not null).
+int launch_row_gain(const void* x, const void* gain, int H, int n_tok, void* hl, float* ss,
+                    void* out, cudaStream_t st);
+
 int check_dims(const dflash_dims* d);
 int make_plan(const dflash_dims& d, Plan* p);
 int current_num_sms();

@@ -105,7 +105,7 @@ __device__ __forceinline__ uint32_t ticket_target(const GemmCore& p, int Tt) {
 }
 
 template <class Fin>
-__global__ void __launch_bounds__(kGemmThreads)
+__global__ void __launch_bounds__(kGemmThreads, 1)
 streamk_gemm_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ BMaps tm_b,
                     const GemmCore p, const __grid_constant__ typename Fin::Params fp) {
   extern __shared__ uint8_t smem_raw[];

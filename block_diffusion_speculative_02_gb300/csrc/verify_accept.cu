@@ -75,6 +75,11 @@ struct LmParams {
   int32_t* commit_len;
   int32_t* out_tokens;
   int out_cap;
+  // drafting (dflash_draft_tokens): the argmaxes become the next block instead
+  // of being checked against one
+  int draft;
+  const int32_t* staged;                 // [B] token for block position 0, or null
+  int32_t* block_out;                    // [B, 16]
 };
 
 __device__ __forceinline__ void accept_and_commit(const LmParams& p, int b) {
@@ -113,6 +118,19 @@ __device__ __forceinline__ void accept_and_commit(const LmParams& p, int b) {
   }
   p.next_staged[b] = staged;
   p.commit_len[b] = lb + 1 + a;
+}
+
+// Drafting: every mask position's argmax is its drafted token ("dflash-mlx"
+// 块扩散草稿 step 2); position 0 takes the staged token.
+__device__ __forceinline__ void write_draft(const LmParams& p, int b) {
+#pragma unroll
+  for (int i = 0; i < kBlock; ++i) {
+    const unsigned long long k = __ldcg(&p.keys[b * kBlock + i]);
+    const int t = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
+    if (p.posterior) p.posterior[b * kBlock + i] = t;
+    if (i > 0) p.block_out[b * kBlock + i] = t;
+  }
+  if (p.staged) p.block_out[b * kBlock] = p.staged[b];
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -340,7 +358,9 @@ lmhead_argmax_accept_kernel(const __grid_constant__ CUtensorMap tm_w,
     named_bar_sync(1, 128);
     if (*last_flag) {
       __threadfence();
-      for (int b = et; b < p.batch; b += 128) accept_and_commit(p, b);
+      for (int b = et; b < p.batch; b += 128) {
+        if (p.draft) write_draft(p, b); else accept_and_commit(p, b);
+      }
       named_bar_sync(1, 128);
       for (int i = et; i < p.ntok; i += 128) p.keys[i] = 0ull;
       if (et == 0) *p.ticket = 0u;
@@ -349,6 +369,50 @@ lmhead_argmax_accept_kernel(const __grid_constant__ CUtensorMap tm_w,
 }
 
 }  // namespace
+
+// Pipeline shape, tensor maps and launch of the LM-head kernel for `p` (whose
+// workspace pointers and per-call outputs the caller has set).
+int launch_lmhead(const dflash_dims& d, int budget_sms, const void* hidden, const void* w_lm,
+                  LmParams& p, cudaStream_t st) {
+  p.vocab = d.vocab;
+  p.hidden = d.hidden;
+  p.ntok = d.batch * kBlock;
+  p.batch = d.batch;
+  p.ntok_box = p.ntok <= 256 ? p.ntok : 256;
+  p.n_xbox = (p.ntok + p.ntok_box - 1) / p.ntok_box;
+  p.n_units = (p.vocab + kUnitRows - 1) / kUnitRows;
+  p.x_chunk = ((p.n_xbox * p.ntok_box * 128) + 1023) / 1024 * 1024;
+  const int fixed = 1024 /*alignment slack*/ + 8 * 5 + 16 + 8 * p.ntok + 64;
+  // as many 64-column chunks per stage as divide K and still leave enough stages
+  p.kb = kLmChunksPerStage;
+  while (p.kb > 1 && ((p.hidden / 64) % p.kb ||
+                      (kSmemBudget - fixed) / (p.kb * (kATileBytes + p.x_chunk) + 16) < kLmMinStages))
+    p.kb >>= 1;
+  p.stage_bytes = p.kb * (kATileBytes + p.x_chunk);
+  p.n_stages = (kSmemBudget - fixed) / (p.stage_bytes + 16);
+  if (p.n_stages > kMaxStages) p.n_stages = kMaxStages;
+  if (p.n_stages < 2) return DFLASH_E_UNSUPPORTED;
+  p.n_acc = (2 * p.ntok <= 512) ? 2 : 1;
+  int cols = 32;
+  while (cols < p.n_acc * p.ntok) cols *= 2;
+  p.tmem_cols = cols;
+  CUtensorMap tm_w, tm_x;
+  PartialMaps tm_part;
+  const uint64_t pitch = static_cast<uint64_t>(d.hidden) * 2;
+  int rc;
+  if ((rc = make_tmap_2d_bf16(&tm_w, w_lm, d.hidden, d.vocab, pitch, 64, kTileRows))) return rc;
+  for (int bi = 0; bi < 4; ++bi)
+    if ((rc = make_tmap_2d_bf16(&tm_part.m[bi], w_lm, d.hidden, d.vocab, pitch, 64, 64 >> bi)))
+      return rc;
+  if ((rc = make_tmap_2d_bf16(&tm_x, hidden, d.hidden, p.ntok, pitch, 64, p.ntok_box))) return rc;
+  const int smem = p.n_stages * (p.stage_bytes + 16) + fixed;
+  if ((rc = set_smem_limit(reinterpret_cast<const void*>(lmhead_argmax_accept_kernel), smem)))
+    return rc;
+  const int grid = budget_sms < p.n_units ? budget_sms : p.n_units;
+  return launch(lmhead_argmax_accept_kernel, dim3(grid), dim3(kThreads), smem, st, tm_w, tm_part,
+                tm_x, p);
+}
+
 }  // namespace dflash
 
 using namespace dflash;
@@ -371,27 +435,6 @@ extern "C" int dflash_verify_accept(const dflash_dims* dims, const void* hidden,
   if (ws_bytes < plan.total) return DFLASH_E_WORKSPACE;
 
   LmParams p = {};
-  p.vocab = dims->vocab;
-  p.hidden = dims->hidden;
-  p.ntok = plan.ntok;
-  p.ntok_box = p.ntok <= 256 ? p.ntok : 256;
-  p.n_xbox = (p.ntok + p.ntok_box - 1) / p.ntok_box;
-  p.n_units = (p.vocab + kUnitRows - 1) / kUnitRows;
-  p.x_chunk = ((p.n_xbox * p.ntok_box * 128) + 1023) / 1024 * 1024;
-  const int fixed = 1024 /*alignment slack*/ + 8 * 5 + 16 + 8 * p.ntok + 64;
-  // as many 64-column chunks per stage as divide K and still leave enough stages
-  p.kb = kLmChunksPerStage;
-  while (p.kb > 1 && ((p.hidden / 64) % p.kb ||
-                      (kSmemBudget - fixed) / (p.kb * (kATileBytes + p.x_chunk) + 16) < kLmMinStages))
-    p.kb >>= 1;
-  p.stage_bytes = p.kb * (kATileBytes + p.x_chunk);
-  p.n_stages = (kSmemBudget - fixed) / (p.stage_bytes + 16);
-  if (p.n_stages > kMaxStages) p.n_stages = kMaxStages;
-  if (p.n_stages < 2) return DFLASH_E_UNSUPPORTED;
-  p.n_acc = (2 * p.ntok <= 512) ? 2 : 1;
-  int cols = 32;
-  while (cols < p.n_acc * p.ntok) cols *= 2;
-  p.tmem_cols = cols;
   p.keys = ws_at<unsigned long long>(ws, plan.off_keys);
   p.ticket = ws_at<uint32_t>(ws, plan.off_tickets);
   p.status = ws_at<uint32_t>(ws, plan.off_status);
@@ -405,24 +448,8 @@ extern "C" int dflash_verify_accept(const dflash_dims* dims, const void* hidden,
   p.out_tokens = out_tokens;
   p.out_cap = out_cap;
 
-  CUtensorMap tm_w, tm_x;
-  PartialMaps tm_part;
-  const uint64_t pitch = static_cast<uint64_t>(dims->hidden) * 2;
-  if ((rc = make_tmap_2d_bf16(&tm_w, w_lm, dims->hidden, dims->vocab, pitch, 64, kTileRows)))
-    return rc;
-  for (int bi = 0; bi < 4; ++bi)
-    if ((rc = make_tmap_2d_bf16(&tm_part.m[bi], w_lm, dims->hidden, dims->vocab, pitch, 64,
-                                64 >> bi)))
-      return rc;
-  if ((rc = make_tmap_2d_bf16(&tm_x, hidden, dims->hidden, p.ntok, pitch, 64, p.ntok_box)))
-    return rc;
-
-  const int smem = p.n_stages * (p.stage_bytes + 16) + fixed;
-  if ((rc = set_smem_limit(reinterpret_cast<const void*>(lmhead_argmax_accept_kernel), smem)))
-    return rc;
-  const int grid = plan.budget_sms < p.n_units ? plan.budget_sms : p.n_units;
-  return launch(lmhead_argmax_accept_kernel, dim3(grid), dim3(kThreads), smem,
-                reinterpret_cast<cudaStream_t>(stream), tm_w, tm_part, tm_x, p);
+  return launch_lmhead(*dims, plan.budget_sms, hidden, w_lm, p,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -491,26 +518,6 @@ extern "C" int dflash_verify_accept_noalloc(const dflash_dims* dims, const void*
   if ((rc = make_plan(*dims, &plan))) return rc;
 
   LmParams p = {};
-  p.vocab = dims->vocab;
-  p.hidden = dims->hidden;
-  p.ntok = plan.ntok;
-  p.ntok_box = p.ntok <= 256 ? p.ntok : 256;
-  p.n_xbox = (p.ntok + p.ntok_box - 1) / p.ntok_box;
-  p.n_units = (p.vocab + kUnitRows - 1) / kUnitRows;
-  p.x_chunk = ((p.n_xbox * p.ntok_box * 128) + 1023) / 1024 * 1024;
-  const int fixed = 1024 + 8 * 5 + 16 + 8 * p.ntok + 64;
-  p.kb = kLmChunksPerStage;
-  while (p.kb > 1 && ((p.hidden / 64) % p.kb ||
-                      (kSmemBudget - fixed) / (p.kb * (kATileBytes + p.x_chunk) + 16) < kLmMinStages))
-    p.kb >>= 1;
-  p.stage_bytes = p.kb * (kATileBytes + p.x_chunk);
-  p.n_stages = (kSmemBudget - fixed) / (p.stage_bytes + 16);
-  if (p.n_stages > kMaxStages) p.n_stages = kMaxStages;
-  if (p.n_stages < 2) return DFLASH_E_UNSUPPORTED;
-  p.n_acc = (2 * p.ntok <= 512) ? 2 : 1;
-  int cols = 32;
-  while (cols < p.n_acc * p.ntok) cols *= 2;
-  p.tmem_cols = cols;
   char* base = static_cast<char*>(scratch);
   p.keys = reinterpret_cast<unsigned long long*>(base);
   p.ticket = reinterpret_cast<uint32_t*>(base + kNoAllocKeyBytes);
@@ -525,24 +532,37 @@ extern "C" int dflash_verify_accept_noalloc(const dflash_dims* dims, const void*
   p.out_tokens = out_tokens;
   p.out_cap = out_cap;
 
-  CUtensorMap tm_w, tm_x;
-  PartialMaps tm_part;
-  const uint64_t pitch = static_cast<uint64_t>(dims->hidden) * 2;
-  if ((rc = make_tmap_2d_bf16(&tm_w, w_lm, dims->hidden, dims->vocab, pitch, 64, kTileRows)))
-    return rc;
-  for (int bi = 0; bi < 4; ++bi)
-    if ((rc = make_tmap_2d_bf16(&tm_part.m[bi], w_lm, dims->hidden, dims->vocab, pitch, 64,
-                                64 >> bi)))
-      return rc;
-  if ((rc = make_tmap_2d_bf16(&tm_x, hidden, dims->hidden, p.ntok, pitch, 64, p.ntok_box)))
-    return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the keys and the ticket must start at zero; the status word is cleared too
   if ((rc = cuda_err(cudaMemsetAsync(scratch, 0, kNoAllocKeyBytes + 8, st)))) return rc;
-  const int smem = p.n_stages * (p.stage_bytes + 16) + fixed;
-  if ((rc = set_smem_limit(reinterpret_cast<const void*>(lmhead_argmax_accept_kernel), smem)))
+  return launch_lmhead(*dims, plan.budget_sms, hidden, w_lm, p, st);
+}
+
+extern "C" int dflash_draft_tokens(const dflash_dims* dims, const void* x,
+                                   const void* final_norm_w, const void* w_lm,
+                                   const int32_t* staged, int32_t* block_ids, int32_t* posterior,
+                                   void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (!x || !w_lm || !block_ids) return DFLASH_E_ARG;
+  if (!aligned16(x) || !aligned16(w_lm)) return DFLASH_E_ALIGN;
+  if (!ws) return DFLASH_E_WORKSPACE;
+  DraftPlan plan;
+  if ((rc = make_draft_plan(*dims, 128, &plan))) return rc;
+  if (ws_bytes < plan.ffn_begin) return DFLASH_E_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // argmax(RMSNorm(x) * g W^T) = argmax((x * g) W^T): the norm's per-row factor
+  // is positive, so only the gains reach the LM head
+  void* xg = ws_at<void>(ws, plan.off_xg);
+  if ((rc = launch_row_gain(x, final_norm_w, dims->hidden, plan.ntok, nullptr, nullptr, xg, st)))
     return rc;
-  const int grid = plan.budget_sms < p.n_units ? plan.budget_sms : p.n_units;
-  return launch(lmhead_argmax_accept_kernel, dim3(grid), dim3(kThreads), smem, st, tm_w, tm_part,
-                tm_x, p);
+  LmParams p = {};
+  p.keys = ws_at<unsigned long long>(ws, plan.off_keys);
+  p.ticket = ws_at<uint32_t>(ws, plan.off_lm_ticket);
+  p.status = ws_at<uint32_t>(ws, plan.off_status);
+  p.draft = 1;
+  p.staged = staged;
+  p.block_out = block_ids;
+  p.posterior = posterior;
+  return launch_lmhead(*dims, plan.budget_sms, xg, w_lm, p, st);
 }

@@ -34,7 +34,9 @@ STATUS_BITS = {
 EXPORTED = ["dflash_workspace_bytes", "dflash_workspace_init", "dflash_ctx_project",
             "dflash_block_attention", "dflash_verify_accept", "dflash_kv_crop",
             "dflash_read_status", "dflash_status_string", "dflash_version",
-            "dflash_verify_accept_noalloc", "dflash_cycle_sm_split"]
+            "dflash_verify_accept_noalloc", "dflash_cycle_sm_split",
+            "dflash_draft_workspace_bytes", "dflash_draft_qkv", "dflash_draft_mlp",
+            "dflash_draft_tokens"]
 
 
 class DFlashError(RuntimeError):
@@ -98,6 +100,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_status_string.argtypes = [ctypes.c_int]
     lib.dflash_version.restype = ctypes.c_int
     lib.dflash_version.argtypes = []
+    lib.dflash_draft_workspace_bytes.restype = sz
+    lib.dflash_draft_workspace_bytes.argtypes = [ctypes.POINTER(Dims), i32]
+    lib.dflash_draft_qkv.restype = ctypes.c_int
+    lib.dflash_draft_qkv.argtypes = [ctypes.POINTER(Dims)] + [vp] * 10 + [vp, sz, vp]
+    lib.dflash_draft_mlp.restype = ctypes.c_int
+    lib.dflash_draft_mlp.argtypes = [ctypes.POINTER(Dims), i32] + [vp] * 8 + [vp, sz, vp]
+    lib.dflash_draft_tokens.restype = ctypes.c_int
+    lib.dflash_draft_tokens.argtypes = [ctypes.POINTER(Dims)] + [vp] * 6 + [vp, sz, vp]
     lib.dflash_cycle_sm_split.restype = ctypes.c_int
     lib.dflash_cycle_sm_split.argtypes = [ctypes.POINTER(Dims), ctypes.POINTER(i32),
                                           ctypes.POINTER(i32)]
@@ -260,3 +270,49 @@ def dflash_read_status(ws, clear: bool = True, stream=None) -> int:
 
 def dflash_version() -> int:
     return int(load_library().dflash_version())
+
+
+# ---------------------------------------------------------------------------
+# the rest of one drafter layer and the drafter's tokens
+# ---------------------------------------------------------------------------
+def dflash_draft_workspace_bytes(dims: Dims, ffn: int) -> int:
+    n = load_library().dflash_draft_workspace_bytes(ctypes.byref(dims), int(ffn))
+    if n == 0:
+        raise DFlashError(-3, "dflash_draft_workspace_bytes")
+    return int(n)
+
+
+def alloc_draft_workspace(dims: Dims, ffn: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace for the dflash_draft_* calls."""
+    return torch.zeros(dflash_draft_workspace_bytes(dims, ffn), dtype=torch.uint8, device=device)
+
+
+def dflash_draft_qkv(dims: Dims, x, ln1_w, w_q, w_k, w_v, q_norm_w, k_norm_w, q_out, k_out, v_out,
+                     ws, stream=None):
+    bf = torch.bfloat16
+    _check(load_library().dflash_draft_qkv(
+        ctypes.byref(dims), _dev(x, bf, "x"), _dev(ln1_w, bf, "ln1_w"), _dev(w_q, bf, "w_q"),
+        _dev(w_k, bf, "w_k"), _dev(w_v, bf, "w_v"), _dev(q_norm_w, bf, "q_norm_w"),
+        _dev(k_norm_w, bf, "k_norm_w"), _dev(q_out, bf, "q_out"), _dev(k_out, bf, "k_out"),
+        _dev(v_out, bf, "v_out"), _dev(ws, name="ws"), ws.numel(), _stream(stream)),
+        "dflash_draft_qkv")
+
+
+def dflash_draft_mlp(dims: Dims, ffn: int, x, attn_out, w_o, ln2_w, w_gate, w_up, w_down, x_out,
+                     ws, stream=None):
+    bf = torch.bfloat16
+    _check(load_library().dflash_draft_mlp(
+        ctypes.byref(dims), int(ffn), _dev(x, bf, "x"), _dev(attn_out, bf, "attn_out"),
+        _dev(w_o, bf, "w_o"), _dev(ln2_w, bf, "ln2_w"), _dev(w_gate, bf, "w_gate"),
+        _dev(w_up, bf, "w_up"), _dev(w_down, bf, "w_down"), _dev(x_out, bf, "x_out"),
+        _dev(ws, name="ws"), ws.numel(), _stream(stream)), "dflash_draft_mlp")
+
+
+def dflash_draft_tokens(dims: Dims, x, final_norm_w, w_lm, staged, block_ids, posterior, ws,
+                        stream=None):
+    bf = torch.bfloat16
+    _check(load_library().dflash_draft_tokens(
+        ctypes.byref(dims), _dev(x, bf, "x"), _dev(final_norm_w, bf, "final_norm_w"),
+        _dev(w_lm, bf, "w_lm"), _dev(staged, torch.int32, "staged"),
+        _dev(block_ids, torch.int32, "block_ids"), _dev(posterior, torch.int32, "posterior"),
+        _dev(ws, name="ws"), ws.numel(), _stream(stream)), "dflash_draft_tokens")

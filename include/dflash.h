@@ -239,6 +239,52 @@ DFLASH_API int dflash_verify_accept_noalloc(const dflash_dims* dims, const void*
 DFLASH_API int dflash_kv_crop(const dflash_kv_view* views, int32_t n_views, const int32_t* new_len,
                    int32_t batch, void* ws, size_t ws_bytes, dflash_stream_t stream);
 
+/*
+ * Next: the rest of one drafter layer and the drafter's tokens.
+ * [P1] §1: the drafter is built from Qwen3 components (RMSNorm, rotary
+ * embedding, MLP): pre-norm decoder layers with a per-head RMSNorm of q and k
+ * and a SwiGLU MLP; [P2] 块扩散草稿 steps 1-2: the block (staged token + 15
+ * masks) goes through one forward and every mask position predicts its own
+ * token.  x below is the layer input, bf16 [B*16, H] (row b*16 + t).
+ * These calls use their own workspace (dflash_draft_workspace_bytes, zeroed
+ * once with dflash_workspace_init); its status word reads with
+ * dflash_read_status.  ffn = MLP width F (multiple of 128).
+ */
+DFLASH_API size_t dflash_draft_workspace_bytes(const dflash_dims* dims, int32_t ffn);
+
+/* h = RMSNorm(x) * ln1_w;  q = RMSNorm_head(h W_q^T) * q_norm_w;
+ * k = RMSNorm_head(h W_k^T) * k_norm_w;  v = h W_v^T   (before RoPE:
+ * dflash_block_attention rotates q and k).  w_q: bf16 [Hq*D, H]; w_k, w_v:
+ * bf16 [Hkv*D, H]; ln1_w [H]; q_norm_w, k_norm_w [D] or NULL (no head norm).
+ * q_out: bf16 [B*16, Hq*D] (= [B,16,Hq,D]); k_out, v_out: bf16 [B*16, Hkv*D]. */
+DFLASH_API int dflash_draft_qkv(const dflash_dims* dims, const void* x, const void* ln1_w,
+                                const void* w_q, const void* w_k, const void* w_v,
+                                const void* q_norm_w, const void* k_norm_w, void* q_out,
+                                void* k_out, void* v_out, void* ws, size_t ws_bytes,
+                                dflash_stream_t stream);
+
+/* x1 = x + O W_o^T;  x_out = x1 + (silu(h2 W_gate^T) * (h2 W_up^T)) W_down^T
+ * with h2 = RMSNorm(x1) * ln2_w.  attn_out O: bf16 [B*16, Hq*D] (the output of
+ * dflash_block_attention); w_o: bf16 [H, Hq*D]; w_gate, w_up: bf16 [ffn, H];
+ * w_down: bf16 [H, ffn]; x_out: bf16 [B*16, H] (may alias x). */
+DFLASH_API int dflash_draft_mlp(const dflash_dims* dims, int32_t ffn, const void* x,
+                                const void* attn_out, const void* w_o, const void* ln2_w,
+                                const void* w_gate, const void* w_up, const void* w_down,
+                                void* x_out, void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/* The drafter's tokens: for every block row the greedy argmax (lowest index
+ * on exact ties) of RMSNorm(x) * final_norm_w W_lm^T, logits never stored
+ * (the per-row norm factor does not change an argmax, so only the gains are
+ * applied).  block_ids[b, 1..15] = the argmaxes of the mask rows 1..15;
+ * block_ids[b, 0] = staged[b] when staged != NULL (e.g. next_staged of
+ * dflash_verify_accept), else unchanged.  posterior (int32 [B,16]) receives
+ * all 16 argmaxes when not NULL.  w_lm: bf16 [V, H]; final_norm_w [H] or
+ * NULL. */
+DFLASH_API int dflash_draft_tokens(const dflash_dims* dims, const void* x,
+                                   const void* final_norm_w, const void* w_lm,
+                                   const int32_t* staged, int32_t* block_ids, int32_t* posterior,
+                                   void* ws, size_t ws_bytes, dflash_stream_t stream);
+
 /* Copy the status word to *host_status (synchronises `stream`); if clear != 0
  * reset it to zero afterwards. */
 DFLASH_API int dflash_read_status(void* ws, uint32_t* host_status, int clear, dflash_stream_t stream);
@@ -246,7 +292,7 @@ DFLASH_API int dflash_read_status(void* ws, uint32_t* host_status, int clear, df
 /* Text for a return code. */
 DFLASH_API const char* dflash_status_string(int code);
 
-/* Library ABI version (major * 100 + minor): 101. */
+/* Library ABI version (major * 100 + minor): 102. */
 DFLASH_API int dflash_version(void);
 
 #ifdef __cplusplus
