@@ -53,6 +53,9 @@ def parse_args(argv=None):
                     help="extra steps after the timed region with events around every call")
     ap.add_argument("--sets", type=int, default=0,
                     help="rotating input sets (0: enough to exceed twice the L2 size)")
+    ap.add_argument("--draft-steps", type=int, default=100,
+                    help="extra steps timing the rest of the drafter layer (Q/K/V, attention, "
+                         "output projection + MLP, tokens), reported beside the cycle")
     ap.add_argument("--sm-split", default="",
                     help="verify_sms,project_sms for the side-by-side phase (default: measured "
                          "around the proportional split before the warm-up)")
@@ -285,6 +288,43 @@ def algorithmic_bytes(cfg, lens) -> dict:
     attn = 2 * Hkv * D * 2 * ctx_len_after + B * T * (Hq + 2 * Hkv) * D * 2 + B * T * Hq * D * 2
     return {"lm_head": lm, "ctx_project": fc + kv, "attention": attn,
             "total": lm + fc + kv + attn}
+
+
+def draft_bytes(cfg) -> int:
+    """Bytes one drafter layer plus its token choice must move at least: its
+    weights and the LM head once, activations once (the attention's context
+    KV is counted with the cycle)."""
+    B, H, V, F = cfg.batch, cfg.hidden, cfg.vocab, cfg.ffn
+    qd, kvd = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    T = 16
+    weights = (qd + 2 * kvd) * H * 2 + H * qd * 2 + 3 * F * H * 2 + V * H * 2
+    acts = B * T * (2 * H + qd + 2 * kvd + qd + H) * 2
+    return weights + acts
+
+
+def build_draft(cfg, device="cuda"):
+    """Drafter-layer weights and activations of the workload's shapes (seeded)."""
+    import torch
+
+    from synthetic import device_generator, device_normal_bf16, device_unit_rms_rows_bf16
+    B, H, F = cfg.batch, cfg.hidden, cfg.ffn
+    qd, kvd = cfg.n_q_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim
+    gw = device_generator(cfg, "draft_w", device)
+    gx = device_generator(cfg, "draft_x", device)
+    n = lambda shape, std=0.02, mean=0.0: device_normal_bf16(gw, shape, std, mean, device)  # noqa
+    w = {"ln1": n((H,), 0.02, 1.0), "wq": n((qd, H)), "wk": n((kvd, H)), "wv": n((kvd, H)),
+         "qn": n((cfg.head_dim,), 0.02, 1.0), "kn": n((cfg.head_dim,), 0.02, 1.0),
+         "wo": n((H, qd)), "ln2": n((H,), 0.02, 1.0), "wg": n((F, H)), "wu": n((F, H)),
+         "wd": n((H, F)), "fn": n((H,), 0.02, 1.0)}
+    x = device_unit_rms_rows_bf16(gx, (B * 16, H), device)
+    bufs = {"q": torch.empty((B * 16, qd), dtype=torch.bfloat16, device=device),
+            "k": torch.empty((B * 16, kvd), dtype=torch.bfloat16, device=device),
+            "v": torch.empty((B * 16, kvd), dtype=torch.bfloat16, device=device),
+            "o": torch.empty((B, 16, cfg.n_q_heads, cfg.head_dim), dtype=torch.bfloat16,
+                             device=device),
+            "x_out": torch.empty((B * 16, H), dtype=torch.bfloat16, device=device),
+            "block": torch.zeros((B, 16), dtype=torch.int32, device=device)}
+    return w, x, bufs
 
 
 # ---------------------------------------------------------------------------
@@ -527,6 +567,47 @@ def main(argv=None):
                      for j, n in enumerate(names)}
         breakdown["unit"] = "us per call (one stream, events between calls)"
 
+    # ---- the rest of the drafter layer and its tokens (beside the cycle) ----
+    draft = None
+    if args.draft_steps > 0 and cfg.ffn:
+        wd, xd, bd = build_draft(cfg)
+        dws = dfl.dflash.alloc_draft_workspace(dims, cfg.ffn)
+        F = cfg.ffn
+
+        def draft_step(i):
+            st = states[i % n_sets]
+            dfl.dflash.dflash_draft_qkv(dims, xd, wd["ln1"], wd["wq"], wd["wk"], wd["wv"],
+                                        wd["qn"], wd["kn"], bd["q"], bd["k"], bd["v"], dws)
+            B_, Hq_, Hkv_, D_ = cfg.batch, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+            dfl.dflash_block_attention(dims, bd["q"].view(B_, 16, Hq_, D_),
+                                       bd["k"].view(B_, 16, Hkv_, D_),
+                                       bd["v"].view(B_, 16, Hkv_, D_), st.draft_cache,
+                                       1.0 / math.sqrt(D_), bd["o"], ws)
+            dfl.dflash.dflash_draft_mlp(dims, F, xd, bd["o"].view(B_ * 16, -1), wd["wo"],
+                                        wd["ln2"], wd["wg"], wd["wu"], wd["wd"], bd["x_out"], dws)
+            dfl.dflash.dflash_draft_tokens(dims, bd["x_out"], wd["fn"], w.w_lm, st.next_staged,
+                                           bd["block"], None, dws)
+
+        for i in range(3):
+            draft_step(i)
+        torch.cuda.synchronize()
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for i in range(args.draft_steps):
+            draft_step(i)
+        d1.record(stream)
+        torch.cuda.synchronize()
+        if dfl.dflash_read_status(dws) != 0:
+            raise RuntimeError("device status set by the drafter calls")
+        d_us = 1e3 * d0.elapsed_time(d1) / args.draft_steps
+        dbytes = draft_bytes(cfg) + bytes_["attention"]
+        draft = {"us_per_block": d_us, "bytes_per_block": dbytes,
+                 "gbs": dbytes / (d_us / 1e6) / 1e9, "frac": dbytes / (d_us / 1e6) / 1e9 / peak,
+                 "ffn": F, "launches_per_block": 9,
+                 "note": "Q/K/V + block attention + output projection and SwiGLU MLP + "
+                         "final-norm LM-head argmax, one drafter layer, not in the cycle metric"}
+
     # ---- end to end: host buffers in, results out, every step ----
     e2e = None
     if args.e2e_steps > 0:
@@ -602,6 +683,7 @@ def main(argv=None):
                          "bytes_per_launch": bytes_["lm_head"], "avg_launch_ms": lm_ms},
             "gpu_launches": launches_per_step * args.steps,
             "breakdown": breakdown,
+            "drafter_layer": draft,
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,

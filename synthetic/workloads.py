@@ -50,6 +50,7 @@ class CycleConfig:
     rope_theta: float = 1.0e6
     rms_eps: float = 1.0e-6
     seed_index: int = 0
+    ffn: int = 0                 # MLP width of a drafter layer (the target's, Qwen3)
 
     @property
     def rows(self) -> int:
@@ -66,19 +67,21 @@ class CycleConfig:
 
 CONFIGS = [
     CycleConfig("tiny_b1", batch=1, hidden=256, n_q_heads=4, n_kv_heads=2, head_dim=64,
-                vocab=4096, n_ctx_layers=2, ctx_len=128, accept=("uniform",), seed_index=0),
+                vocab=4096, n_ctx_layers=2, ctx_len=128, accept=("uniform",), seed_index=0,
+                ffn=768),
     CycleConfig("qwen3_4b_b1", batch=1, hidden=2560, n_q_heads=32, n_kv_heads=8, head_dim=128,
                 vocab=151936, n_ctx_layers=5, ctx_len=2048, accept=("geometric", 13.0),
-                seed_index=1),
+                seed_index=1, ffn=9728),
     CycleConfig("qwen3_8b_b1", batch=1, hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128,
-                vocab=151936, n_ctx_layers=5, ctx_len=8192, accept=("uniform",), seed_index=2),
+                vocab=151936, n_ctx_layers=5, ctx_len=8192, accept=("uniform",), seed_index=2,
+                ffn=12288),
     CycleConfig("qwen3_8b_b32_paged", batch=32, hidden=4096, n_q_heads=32, n_kv_heads=8,
                 head_dim=128, vocab=151936, n_ctx_layers=5, ctx_len=0,
                 ctx_len_range=(512, 16384), paged=True, page_size=16,
-                accept=("geometric", 13.0), seed_index=3),
+                accept=("geometric", 13.0), seed_index=3, ffn=12288),
     CycleConfig("qwen3_32b_b4_32k", batch=4, hidden=5120, n_q_heads=64, n_kv_heads=8,
                 head_dim=128, vocab=151936, n_ctx_layers=5, ctx_len=32768,
-                accept=("geometric", 12.0), seed_index=4),
+                accept=("geometric", 12.0), seed_index=4, ffn=25600),
 ]
 CONFIG_BY_NAME = {c.name: c for c in CONFIGS}
 
@@ -197,7 +200,7 @@ def make_block_ids(rng: np.random.Generator, posterior: np.ndarray, accept: np.n
 # --------------------------------------------------------------------------
 STREAMS = ["layer_hidden", "w_fc", "hidden_norm_w", "w_k", "w_v", "k_norm_w",
            "ctx_k", "ctx_v", "q_blk", "k_blk", "v_blk", "verify_hidden", "w_lm",
-           "blocks", "accept", "ctx_lens", "pages"]
+           "blocks", "accept", "ctx_lens", "pages", "draft_x", "draft_w"]
 
 
 def streams_for(cfg: CycleConfig) -> dict:
