@@ -192,6 +192,49 @@ def lm_head_argmax(hidden, w_lm, chunk: int = 8192) -> dict:
 
 
 # ---------------------------------------------------------------------------
+# next: the target's attention in the verify forward
+# ---------------------------------------------------------------------------
+def verify_attention(q_blk, k_blk, v_blk, ctx_k, ctx_v, seq_len, rope_theta: float,
+                     scale: float) -> dict:
+    """The target's attention for the 16 verify rows of one layer.
+
+    [P2] 单次前向验证 ⑤: the target runs one forward over the block
+    [staged, d_1..d_15]; it is an ordinary causal decoder, so block row i sees
+    the cached context rows 0..L_b-1 and the block rows 0..i, and the block's
+    K/V join the target's cache (保证三 later cuts it back to the committed
+    length).  Positions, GQA and RoPE as in block_attention.
+    Returns O [B,T,Hq,D] and the rotated block K and the block V
+    [B,T,Hkv,D] that are appended to the cache at rows L_b..L_b+15.
+    """
+    q_blk, k_blk, v_blk = as_f64(q_blk), as_f64(k_blk), as_f64(v_blk)
+    B, T, Hq, D = q_blk.shape
+    Hkv = k_blk.shape[2]
+    G = Hq // Hkv
+    out = np.zeros((B, T, Hq, D), dtype=np.float64)
+    k_rot = np.zeros((B, T, Hkv, D), dtype=np.float64)
+    for b in range(B):
+        L = int(seq_len[b])
+        pos = L + np.arange(T, dtype=np.float64)
+        q = apply_rope(q_blk[b], np.broadcast_to(pos[:, None], (T, Hq)), rope_theta)
+        kb = apply_rope(k_blk[b], np.broadcast_to(pos[:, None], (T, Hkv)), rope_theta)
+        k_rot[b] = kb
+        keys = np.concatenate([as_f64(ctx_k[b][:L]).reshape(L, Hkv, D), kb], axis=0)
+        vals = np.concatenate([as_f64(ctx_v[b][:L]).reshape(L, Hkv, D), v_blk[b]], axis=0)
+        mask = np.zeros((T, L + T), dtype=bool)
+        for i in range(T):
+            mask[i, L + i + 1:] = True                       # later block rows are hidden
+        for h in range(Hq):
+            g = h // G
+            s = (q[:, h, :] @ keys[:, g, :].T) * scale
+            s[mask] = -np.inf
+            s = s - s.max(axis=1, keepdims=True)
+            p = np.exp(s)
+            p = p / p.sum(axis=1, keepdims=True)
+            out[b, :, h, :] = p @ vals[:, g, :]
+    return {"o": out, "k": k_rot, "v": v_blk.copy()}
+
+
+# ---------------------------------------------------------------------------
 # next: the rest of one drafter layer and the drafter's token choice
 # ---------------------------------------------------------------------------
 def draft_qkv(x, ln1_w, w_q, w_k, w_v, q_norm_w, k_norm_w, n_q_heads: int, n_kv_heads: int,

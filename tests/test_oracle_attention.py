@@ -165,3 +165,62 @@ def test_context_lengths_edge_cases(lens):
     got = block_attention(q, k, v, ck, cv, L, THETA, 0.5)
     ref = brute_block_attention(q, k, v, ck, cv, L, THETA, 0.5)
     np.testing.assert_allclose(got, ref, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# the target's verify attention (causal inside the block)
+# ---------------------------------------------------------------------------
+from oracle.dflash_oracle import verify_attention  # noqa: E402
+
+
+def brute_verify_attention(q_blk, k_blk, v_blk, ctx_k, ctx_v, seq_len, theta, scale):
+    B, T, Hq, D = q_blk.shape
+    Hkv = k_blk.shape[2]
+    out = np.zeros((B, T, Hq, D))
+    for b in range(B):
+        L = int(seq_len[b])
+        for h in range(Hq):
+            g = h * Hkv // Hq
+            for i in range(T):
+                keys = [list(ctx_k[b][j, g]) for j in range(L)]
+                vals = [list(ctx_v[b][j, g]) for j in range(L)]
+                for j in range(i + 1):                     # block rows 0..i only
+                    keys.append(rope_complex(list(k_blk[b, j, g]), L + j, theta))
+                    vals.append(list(v_blk[b, j, g]))
+                q = rope_complex(list(q_blk[b, i, h]), L + i, theta)
+                s = [scale * sum(q[d] * kk[d] for d in range(D)) for kk in keys]
+                m = max(s)
+                e = [math.exp(x - m) for x in s]
+                z = sum(e)
+                for d in range(D):
+                    out[b, i, h, d] = sum(e[j] * vals[j][d] for j in range(len(vals))) / z
+    return out
+
+
+def test_verify_attention_brute_force():
+    rng = np.random.default_rng(21)
+    q, k, v, ck, cv, lens = _rand_case(rng, lens=(5, 0))
+    r = verify_attention(q, k, v, ck, cv, lens, THETA, 0.4)
+    ref = brute_verify_attention(q, k, v, ck, cv, lens, THETA, 0.4)
+    np.testing.assert_allclose(r["o"], ref, rtol=0, atol=1e-12)
+    # the appended K rows are the block keys rotated at L + j
+    for j in (0, 7, 15):
+        np.testing.assert_allclose(r["k"][0, j, 1], rope_complex(list(k[0, j, 1]), 5 + j),
+                                   atol=1e-12)
+    np.testing.assert_array_equal(r["v"], v)
+
+
+def test_verify_attention_last_row_is_the_block_attention():
+    """Row 15 sees every block row, so it equals the non-causal block attention;
+    row 0 sees the context and block row 0 only."""
+    rng = np.random.default_rng(22)
+    q, k, v, ck, cv, lens = _rand_case(rng, B=1, lens=(9,))
+    causal = verify_attention(q, k, v, ck, cv, lens, THETA, 0.3)["o"]
+    full = block_attention(q, k, v, ck, cv, lens, THETA, 0.3)
+    np.testing.assert_allclose(causal[0, 15], full[0, 15], atol=1e-12)
+    assert np.abs(causal[0, 0] - full[0, 0]).max() > 1e-6
+    k2, v2 = k.copy(), v.copy()
+    k2[0, 1:] = rng.standard_normal(k2[0, 1:].shape)        # later rows cannot reach row 0
+    v2[0, 1:] += 5.0
+    again = verify_attention(q, k2, v2, ck, cv, lens, THETA, 0.3)["o"]
+    np.testing.assert_array_equal(again[0, 0], causal[0, 0])
