@@ -58,6 +58,11 @@ struct AttnParams {
   float* part_o;
   float* part_ml;
   uint32_t* status;
+  // the target's verify attention: causal inside the block, and the block's
+  // rotated K and its V appended to the cache at rows L .. L + 15
+  int causal;
+  uint16_t* k_app;
+  uint16_t* v_app;
   // shared-memory plan (byte offsets from the 1024-aligned base)
   int n_stages, off_q, off_st, off_blk, off_sc, off_ml, off_rope, off_bar;
   RopeTable rope;
@@ -425,6 +430,25 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
           *reinterpret_cast<uint4*>(blk + off2) = y2;
           *reinterpret_cast<uint4*>(blk + C::kBlkV + off1) = v1;
           *reinterpret_cast<uint4*>(blk + C::kBlkV + off2) = v2;
+          if (p.k_app && L + kBlock <= limit) {
+            // head-major cache row L + j of KV head g
+            long long row = -1;
+            if (p.paged) {
+              const int id = p.page_table[static_cast<size_t>(b) * p.max_pages + (L + j) / kPage];
+              if (id >= 0)
+                row = (static_cast<long long>(id) * p.n_kv_heads + g) * kPage + (L + j) % kPage;
+              else
+                set_status(p.status, DFLASH_ST_PAGE_MISSING);
+            } else {
+              row = (static_cast<long long>(b) * p.n_kv_heads + g) * p.capacity + L + j;
+            }
+            if (row >= 0) {
+              *reinterpret_cast<uint4*>(p.k_app + row * D + d0) = y1;
+              *reinterpret_cast<uint4*>(p.k_app + row * D + e2) = y2;
+              *reinterpret_cast<uint4*>(p.v_app + row * D + d0) = v1;
+              *reinterpret_cast<uint4*>(p.v_app + row * D + e2) = v2;
+            }
+          }
         }
       }
       fence_proxy_async_smem();
@@ -460,13 +484,16 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
       tmem_ld_wait();
       // this thread's keys kbase .. kbase + kMine - 1, masked past nk
       const int kbase = 32 * khalf;
+      // keys of this row: all valid ones, or -- causal block chunk -- block
+      // rows 0 .. i of the row's own block position i
+      const int n_see = (p.causal && has_block && j == 0) ? min(nk, (rr & 15) + 1) : nk;
       float x[kMine];
 #pragma unroll
       for (int e = 0; e < kMine; ++e) {
         uint32_t v;
         if (dup) v = khalf ? sv[2 + (e >> 4)][e & 15] : sv[e >> 4][e & 15];
         else v = sv[e >> 4][e & 15];
-        x[e] = kbase + e < nk ? __uint_as_float(v) : -INFINITY;
+        x[e] = kbase + e < n_see ? __uint_as_float(v) : -INFINITY;
       }
       float mx4[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
@@ -724,6 +751,31 @@ int plan_attention_smem(AttnParams& p) {
   return attention_smem_for<D>(p, 2);
 }
 
+// The target's verify attention appends the block at rows L .. L + 15: map
+// the pages those rows need before the attention writes them, and move the
+// length past them once every kernel that reads L has finished.
+__global__ void append_reserve_kernel(const dflash_kv_view v, int batch, uint32_t* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  const int L = v.seq_len[b];
+  const int limit = v.max_pages * v.page_size;
+  if (L >= 0 && L + kBlock <= limit) map_rows(v, b, L, kBlock, status);
+}
+
+__global__ void append_length_kernel(int32_t* seq_len, int batch, int limit, uint32_t* status) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  const int L = seq_len[b];
+  if (L >= 0 && L + kBlock <= limit)
+    seq_len[b] = L + kBlock;
+  else
+    set_status(status, DFLASH_ST_CAPACITY);
+}
+
 template <int D>
 int launch_attention(const dflash_dims& dims, const Plan& plan, const dflash_kv_view& cache,
                      AttnParams& p, CombineParams& cp, cudaStream_t stream) {
@@ -767,8 +819,11 @@ int launch_attention(const dflash_dims& dims, const Plan& plan, const dflash_kv_
               stream, tm_k, tm_v, tm_k64, tm_v64, p);
   if (rc) return rc;
   const int rows_out = dims.batch * kBlock * dims.n_q_heads;
-  return launch(attn_combine_kernel<D>, dim3((rows_out + kCombineRows - 1) / kCombineRows),
-                dim3(32 * kCombineRows), 0, stream, cp);
+  rc = launch(attn_combine_kernel<D>, dim3((rows_out + kCombineRows - 1) / kCombineRows),
+              dim3(32 * kCombineRows), 0, stream, cp);
+  if (rc || !p.k_app) return rc;
+  return launch(append_length_kernel, dim3((dims.batch + 127) / 128), dim3(128), 0, stream,
+                cache.seq_len, dims.batch, cp.limit, p.status);
 }
 
 }  // namespace
@@ -776,10 +831,11 @@ int launch_attention(const dflash_dims& dims, const Plan& plan, const dflash_kv_
 
 using namespace dflash;
 
-extern "C" int dflash_block_attention(const dflash_dims* dims, const void* q_blk,
-                                      const void* k_blk, const void* v_blk,
-                                      const dflash_kv_view* cache, float scale, void* out,
-                                      void* ws, size_t ws_bytes, dflash_stream_t stream) {
+namespace {
+
+int run_attention(const dflash_dims* dims, const void* q_blk, const void* k_blk,
+                  const void* v_blk, const dflash_kv_view* cache, float scale, void* out,
+                  void* ws, size_t ws_bytes, dflash_stream_t stream, bool verify) {
   int rc = check_dims(dims);
   if (rc) return rc;
   if (!q_blk || !k_blk || !v_blk || !cache || !out || !cache->k || !cache->v || !cache->seq_len)
@@ -836,6 +892,33 @@ extern "C" int dflash_block_attention(const dflash_dims* dims, const void* q_blk
   cp.out = static_cast<uint16_t*>(out);
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (verify) {
+    p.causal = 1;
+    p.k_app = static_cast<uint16_t*>(cache->k);
+    p.v_app = static_cast<uint16_t*>(cache->v);
+    if (paged && (!cache->free_list || !cache->free_count)) return DFLASH_E_ARG;
+    if (paged && (rc = launch(append_reserve_kernel, dim3((dims->batch + 127) / 128), dim3(128),
+                              0, s, *cache, dims->batch, p.status)))
+      return rc;
+  }
   return dims->head_dim == 128 ? launch_attention<128>(*dims, plan, *cache, p, cp, s)
                                : launch_attention<64>(*dims, plan, *cache, p, cp, s);
+}
+
+}  // namespace
+
+extern "C" int dflash_block_attention(const dflash_dims* dims, const void* q_blk,
+                                      const void* k_blk, const void* v_blk,
+                                      const dflash_kv_view* cache, float scale, void* out,
+                                      void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  return run_attention(dims, q_blk, k_blk, v_blk, cache, scale, out, ws, ws_bytes, stream,
+                       false);
+}
+
+extern "C" int dflash_verify_attention(const dflash_dims* dims, const void* q_blk,
+                                       const void* k_blk, const void* v_blk,
+                                       const dflash_kv_view* cache, float scale, void* out,
+                                       void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  return run_attention(dims, q_blk, k_blk, v_blk, cache, scale, out, ws, ws_bytes, stream,
+                       true);
 }

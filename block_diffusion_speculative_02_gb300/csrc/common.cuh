@@ -348,6 +348,28 @@ __device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* p) {
 }
 
 // ----------------------------------------------------------------------------
+// paged caches
+// ----------------------------------------------------------------------------
+// Map the pages that rows pos .. pos + n - 1 of sequence b need, popping them
+// from the view's free list (a stack indexed by *free_count).  Returns false
+// and records DFLASH_ST_POOL_EMPTY when the pool runs dry.
+__device__ inline bool map_rows(const dflash_kv_view& v, int b, int pos, int n,
+                                uint32_t* status) {
+  int32_t* tbl = v.page_table + static_cast<size_t>(b) * v.max_pages;
+  for (int pg = pos / v.page_size; pg <= (pos + n - 1) / v.page_size; ++pg) {
+    if (tbl[pg] >= 0) continue;
+    const int slot = atomicSub(v.free_count, 1) - 1;
+    if (slot < 0) {
+      atomicAdd(v.free_count, 1);
+      set_status(status, DFLASH_ST_POOL_EMPTY);
+      return false;
+    }
+    tbl[pg] = v.free_list[slot];
+  }
+  return true;
+}
+
+// ----------------------------------------------------------------------------
 // named barriers (sub-CTA sync among a set of warps)
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {

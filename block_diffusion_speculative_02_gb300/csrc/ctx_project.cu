@@ -56,19 +56,7 @@ __device__ void reserve_block_rows(const ProjParams& p, uint32_t* status, int b)
     set_status(status, DFLASH_ST_CAPACITY);
     return;
   }
-  if (v.page_table) {
-    int32_t* tbl = v.page_table + static_cast<size_t>(b) * v.max_pages;
-    for (int pg = pos / v.page_size; pg <= (pos + kBlock - 1) / v.page_size; ++pg) {
-      if (tbl[pg] >= 0) continue;
-      const int slot = atomicSub(v.free_count, 1) - 1;
-      if (slot < 0) {
-        atomicAdd(v.free_count, 1);
-        set_status(status, DFLASH_ST_POOL_EMPTY);
-        break;
-      }
-      tbl[pg] = v.free_list[slot];
-    }
-  }
+  if (v.page_table) map_rows(v, b, pos, kBlock, status);
   v.seq_len[b] = pos + kBlock;
 }
 

@@ -36,7 +36,7 @@ EXPORTED = ["dflash_workspace_bytes", "dflash_workspace_init", "dflash_ctx_proje
             "dflash_read_status", "dflash_status_string", "dflash_version",
             "dflash_verify_accept_noalloc", "dflash_cycle_sm_split",
             "dflash_draft_workspace_bytes", "dflash_draft_qkv", "dflash_draft_mlp",
-            "dflash_draft_tokens"]
+            "dflash_draft_tokens", "dflash_verify_attention"]
 
 
 class DFlashError(RuntimeError):
@@ -86,6 +86,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_block_attention.argtypes = [ctypes.POINTER(Dims), vp, vp, vp,
                                            ctypes.POINTER(KVViewC), ctypes.c_float, vp, vp, sz,
                                            vp]
+    lib.dflash_verify_attention.restype = ctypes.c_int
+    lib.dflash_verify_attention.argtypes = [ctypes.POINTER(Dims), vp, vp, vp,
+                                            ctypes.POINTER(KVViewC), ctypes.c_float, vp, vp, sz,
+                                            vp]
     lib.dflash_verify_accept.restype = ctypes.c_int
     lib.dflash_verify_accept.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, vp, vp, vp, vp, vp,
                                          vp, i32, vp, sz, vp]
@@ -225,6 +229,17 @@ def dflash_block_attention(dims: Dims, q_blk, k_blk, v_blk, cache: KVView, scale
         _dev(k_blk, torch.bfloat16, "k_blk"), _dev(v_blk, torch.bfloat16, "v_blk"),
         ctypes.byref(view), float(scale), _dev(out, torch.bfloat16, "out"), _dev(ws, name="ws"),
         ws.numel(), _stream(stream)), "dflash_block_attention")
+
+
+def dflash_verify_attention(dims: Dims, q_blk, k_blk, v_blk, cache: KVView, scale: float, out,
+                            ws, stream=None):
+    """The target's verify attention: causal inside the block, block K/V appended to ``cache``."""
+    view = cache.c()
+    _check(load_library().dflash_verify_attention(
+        ctypes.byref(dims), _dev(q_blk, torch.bfloat16, "q_blk"),
+        _dev(k_blk, torch.bfloat16, "k_blk"), _dev(v_blk, torch.bfloat16, "v_blk"),
+        ctypes.byref(view), float(scale), _dev(out, torch.bfloat16, "out"), _dev(ws, name="ws"),
+        ws.numel(), _stream(stream)), "dflash_verify_attention")
 
 
 def dflash_verify_accept(dims: Dims, hidden, w_lm, block_ids, len_before, posterior, accept_len,

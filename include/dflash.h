@@ -177,6 +177,22 @@ DFLASH_API int dflash_block_attention(const dflash_dims* dims, const void* q_blk
                            void* out, void* ws, size_t ws_bytes, dflash_stream_t stream);
 
 /*
+ * Next: the target's attention in the verify forward ([P2] 单次前向验证 ⑤:
+ * one forward of the target over the block; 保证三: its cache is later cut
+ * back to the committed length).  Same shapes, layouts and errors as
+ * dflash_block_attention, with two differences: block row i sees the
+ * context rows 0..L-1 and the block rows 0..i only (causal inside the
+ * block), and the block's rotated K and its V are appended to `cache` at rows
+ * L..L+15 (for a paged cache the pages those rows need are first taken from
+ * its free list), after which cache->seq_len[b] = L + 16.  A length with no
+ * room for 16 more rows sets DFLASH_ST_CAPACITY and appends nothing.
+ */
+DFLASH_API int dflash_verify_attention(const dflash_dims* dims, const void* q_blk,
+                                       const void* k_blk, const void* v_blk,
+                                       const dflash_kv_view* cache, float scale, void* out,
+                                       void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/*
  * a3 — verification epilogue ([P2] 单次前向验证 ⑤–⑧, 保证一, 保证二).
  *   logits[b,i,:] = hidden[b,i,:] W_lm^T        (fp32, never written to memory)
  *   posterior[b,i] = argmax (lowest index on exact ties)
@@ -292,7 +308,7 @@ DFLASH_API int dflash_read_status(void* ws, uint32_t* host_status, int clear, df
 /* Text for a return code. */
 DFLASH_API const char* dflash_status_string(int code);
 
-/* Library ABI version (major * 100 + minor): 102. */
+/* Library ABI version (major * 100 + minor): 103. */
 DFLASH_API int dflash_version(void);
 
 #ifdef __cplusplus
