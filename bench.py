@@ -608,6 +608,37 @@ def main(argv=None):
                  "note": "Q/K/V + block attention + output projection and SwiGLU MLP + "
                          "final-norm LM-head argmax, one drafter layer, not in the cycle metric"}
 
+    # ---- the target's verify attention on a cache of the same shapes ----
+    vatt = None
+    if args.draft_steps > 0:
+        st = states[0]
+        dc = st.draft_cache
+        L0 = dc.seq_len.clone()
+        tview = dfl.KVView(dc.k, dc.v, dc.seq_len.clone(), capacity=dc.capacity,
+                           page_table=dc.page_table, free_list=dc.free_list,
+                           free_count=dc.free_count, page_size=dc.page_size)
+        o_v = torch.empty_like(st.attn_out)
+        D_ = cfg.head_dim
+        v_ms = []
+        for i in range(args.draft_steps + 3):
+            tview.seq_len.copy_(L0)
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            dfl.dflash.dflash_verify_attention(dims, st.q_blk, st.k_blk, st.v_blk, tview,
+                                               1.0 / math.sqrt(D_), o_v, ws)
+            a1.record(stream)
+            v_ms.append((a0, a1))
+        torch.cuda.synchronize()
+        if dfl.dflash_read_status(ws) != 0:
+            raise RuntimeError("device status set by the verify attention")
+        dc.seq_len.copy_(L0)
+        us = 1e3 * statistics.mean(a.elapsed_time(b) for a, b in v_ms[3:])
+        vbytes = bytes_["attention"] + 2 * cfg.batch * 16 * cfg.n_kv_heads * D_ * 2
+        vatt = {"us": us, "bytes": vbytes, "gbs": vbytes / (us / 1e6) / 1e9,
+                "note": "one layer of the target's verify forward: causal-in-block attention "
+                        "over the context plus the block K/V appended; not in the cycle metric"}
+
     # ---- end to end: host buffers in, results out, every step ----
     e2e = None
     if args.e2e_steps > 0:
@@ -684,6 +715,7 @@ def main(argv=None):
             "gpu_launches": launches_per_step * args.steps,
             "breakdown": breakdown,
             "drafter_layer": draft,
+            "verify_attention": vatt,
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -235,6 +235,42 @@ def verify_attention(q_blk, k_blk, v_blk, ctx_k, ctx_v, seq_len, rope_theta: flo
 
 
 # ---------------------------------------------------------------------------
+# next: rollback of the recurrent (GatedDeltaNet) state of a hybrid target
+# ---------------------------------------------------------------------------
+def gdn_step(S, k, v, beta: float, g: float) -> np.ndarray:
+    """One step of the gated delta rule on a state S [Dv, Dk]:
+        S <- exp(g) * S (I - beta k k^T) + beta v k^T
+    the recurrence of a GatedDeltaNet linear-attention layer (the layers whose
+    state [P1] §7 and [P2] 保证三 say cannot simply be truncated)."""
+    S = np.asarray(S, dtype=np.float64)
+    k = as_f64(k)
+    v = as_f64(v)
+    Dk = k.shape[0]
+    return np.exp(g) * S @ (np.eye(Dk) - beta * np.outer(k, k)) + beta * np.outer(v, k)
+
+
+def gdn_replay(state, tape_k, tape_v, tape_beta, tape_g, n_steps) -> np.ndarray:
+    """Tape-replay rollback ([P2] 保证三, [P1] §7): the verify forward recorded,
+    per block step t, the innovation (k_t, v_t, beta_t, g_t) of every
+    recurrent head; after acceptance only the first n_steps = 1 + a steps are
+    replayed onto the state saved before the verify forward, which rebuilds the
+    state exactly as if only the committed tokens had been processed.
+    state [B, NH, Dv, Dk] (NH = recurrent heads over all such layers);
+    tape_k [B, T, NH, Dk], tape_v [B, T, NH, Dv], tape_beta/tape_g [B, T, NH];
+    n_steps [B].  Returns the new state [B, NH, Dv, Dk]."""
+    out = np.array(state, dtype=np.float64, copy=True)
+    B, NH = out.shape[:2]
+    for b in range(B):
+        for h in range(NH):
+            S = out[b, h]
+            for t in range(int(n_steps[b])):
+                S = gdn_step(S, tape_k[b, t, h], tape_v[b, t, h], float(tape_beta[b, t, h]),
+                             float(tape_g[b, t, h]))
+            out[b, h] = S
+    return out
+
+
+# ---------------------------------------------------------------------------
 # next: the rest of one drafter layer and the drafter's token choice
 # ---------------------------------------------------------------------------
 def draft_qkv(x, ln1_w, w_q, w_k, w_v, q_norm_w, k_norm_w, n_q_heads: int, n_kv_heads: int,
