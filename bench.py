@@ -639,6 +639,43 @@ def main(argv=None):
                 "note": "one layer of the target's verify forward: causal-in-block attention "
                         "over the context plus the block K/V appended; not in the cycle metric"}
 
+    # ---- GatedDeltaNet tape-replay rollback (hybrid targets; synthetic states) ----
+    gdn = None
+    if args.draft_steps > 0:
+        NH, DK, DV = 24 * 32, 128, 128           # 24 recurrent layers x 32 heads
+        Bg = cfg.batch
+        gg = torch.Generator(device="cuda")
+        gg.manual_seed(7)
+        states_g = [0.3 * torch.randn((Bg, NH, DV, DK), generator=gg, device="cuda")
+                    for _ in range(3)]                # rotate: 3 x 48 MB > L2
+        kt = torch.nn.functional.normalize(
+            torch.randn((Bg, 16, NH, DK), generator=gg, device="cuda"), dim=-1).to(torch.bfloat16)
+        vt = torch.randn((Bg, 16, NH, DV), generator=gg, device="cuda").to(torch.bfloat16)
+        bt = torch.rand((Bg, 16, NH), generator=gg, device="cuda")
+        gt = -0.3 * torch.rand((Bg, 16, NH), generator=gg, device="cuda")
+        acc_g = states[0].accept_len
+        gws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+        for i in range(3):
+            dfl.dflash.dflash_gdn_replay(states_g[i % 3], kt, vt, bt, gt, acc_g, gws)
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for i in range(args.draft_steps):
+            dfl.dflash.dflash_gdn_replay(states_g[i % 3], kt, vt, bt, gt, acc_g, gws)
+        g1.record(stream)
+        torch.cuda.synchronize()
+        if dfl.dflash_read_status(gws) != 0:
+            raise RuntimeError("device status set by the GDN replay")
+        us = 1e3 * g0.elapsed_time(g1) / args.draft_steps
+        steps = int(acc_g.sum().item()) + Bg
+        gbytes = Bg * NH * DV * DK * 4 * 2 + steps * NH * ((DK + DV) * 2 + 8)
+        gdn = {"us": us, "bytes": gbytes, "gbs": gbytes / (us / 1e6) / 1e9,
+               "frac": gbytes / (us / 1e6) / 1e9 / peak,
+               "shape": f"B {Bg}, {NH} recurrent heads (24 layers x 32), Dk = Dv = {DK}, "
+                        f"1 + a steps replayed",
+               "note": "synthetic states; not in the cycle metric"}
+
     # ---- end to end: host buffers in, results out, every step ----
     e2e = None
     if args.e2e_steps > 0:
@@ -716,6 +753,7 @@ def main(argv=None):
             "breakdown": breakdown,
             "drafter_layer": draft,
             "verify_attention": vatt,
+            "gdn_replay": gdn,
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -36,7 +36,7 @@ EXPORTED = ["dflash_workspace_bytes", "dflash_workspace_init", "dflash_ctx_proje
             "dflash_read_status", "dflash_status_string", "dflash_version",
             "dflash_verify_accept_noalloc", "dflash_cycle_sm_split",
             "dflash_draft_workspace_bytes", "dflash_draft_qkv", "dflash_draft_mlp",
-            "dflash_draft_tokens", "dflash_verify_attention"]
+            "dflash_draft_tokens", "dflash_verify_attention", "dflash_gdn_replay"]
 
 
 class DFlashError(RuntimeError):
@@ -90,6 +90,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_verify_attention.argtypes = [ctypes.POINTER(Dims), vp, vp, vp,
                                             ctypes.POINTER(KVViewC), ctypes.c_float, vp, vp, sz,
                                             vp]
+    lib.dflash_gdn_replay.restype = ctypes.c_int
+    lib.dflash_gdn_replay.argtypes = [i32, i32, i32, i32] + [vp] * 6 + [vp, sz, vp]
     lib.dflash_verify_accept.restype = ctypes.c_int
     lib.dflash_verify_accept.argtypes = [ctypes.POINTER(Dims), vp, vp, vp, vp, vp, vp, vp, vp,
                                          vp, i32, vp, sz, vp]
@@ -331,3 +333,14 @@ def dflash_draft_tokens(dims: Dims, x, final_norm_w, w_lm, staged, block_ids, po
         _dev(w_lm, bf, "w_lm"), _dev(staged, torch.int32, "staged"),
         _dev(block_ids, torch.int32, "block_ids"), _dev(posterior, torch.int32, "posterior"),
         _dev(ws, name="ws"), ws.numel(), _stream(stream)), "dflash_draft_tokens")
+
+
+def dflash_gdn_replay(state, tape_k, tape_v, tape_beta, tape_g, accept_len, ws, stream=None):
+    """Replay the committed 1 + a steps of the recorded tape onto ``state`` (in place)."""
+    B, NH, Dv, Dk = state.shape
+    _check(load_library().dflash_gdn_replay(
+        int(B), int(NH), int(Dk), int(Dv), _dev(state, torch.float32, "state"),
+        _dev(tape_k, torch.bfloat16, "tape_k"), _dev(tape_v, torch.bfloat16, "tape_v"),
+        _dev(tape_beta, torch.float32, "tape_beta"), _dev(tape_g, torch.float32, "tape_g"),
+        _dev(accept_len, torch.int32, "accept_len"), _dev(ws, name="ws"), ws.numel(),
+        _stream(stream)), "dflash_gdn_replay")

@@ -301,6 +301,28 @@ DFLASH_API int dflash_draft_tokens(const dflash_dims* dims, const void* x,
                                    const int32_t* staged, int32_t* block_ids, int32_t* posterior,
                                    void* ws, size_t ws_bytes, dflash_stream_t stream);
 
+/*
+ * Next: rollback of the recurrent state of a hybrid target ([P2] 保证三:
+ * GatedDeltaNet states cannot be cut back; the verify forward records each
+ * step's innovation and only the accepted steps are replayed; [P1] §7).
+ * For every sequence b and recurrent head h (the heads of all GatedDeltaNet
+ * layers, n_heads in total), for t = 0 .. accept_len[b] (1 + a steps):
+ *   S <- exp(g[b,t,h]) * S (I - beta[b,t,h] k k^T) + beta[b,t,h] v k^T,
+ *   k = tape_k[b,t,h], v = tape_v[b,t,h].
+ * state: fp32 [B, n_heads, dv, dk], in place (the state saved before the
+ * verify forward in, the state after the committed tokens out).
+ * tape_k: bf16 [B, 16, n_heads, dk]; tape_v: bf16 [B, 16, n_heads, dv];
+ * tape_beta, tape_g: fp32 [B, 16, n_heads]; accept_len: int32 [B] device
+ * (from dflash_verify_accept).  dk, dv in {64, 128}.  accept_len outside
+ * 0..15 sets DFLASH_ST_CAPACITY and leaves that sequence's state.  ws: any
+ * zeroed workspace of at least 64 bytes (its status word is used).
+ */
+DFLASH_API int dflash_gdn_replay(int32_t batch, int32_t n_heads, int32_t dk, int32_t dv,
+                                 float* state, const void* tape_k, const void* tape_v,
+                                 const float* tape_beta, const float* tape_g,
+                                 const int32_t* accept_len, void* ws, size_t ws_bytes,
+                                 dflash_stream_t stream);
+
 /* Copy the status word to *host_status (synchronises `stream`); if clear != 0
  * reset it to zero afterwards. */
 DFLASH_API int dflash_read_status(void* ws, uint32_t* host_status, int clear, dflash_stream_t stream);
@@ -308,7 +330,7 @@ DFLASH_API int dflash_read_status(void* ws, uint32_t* host_status, int clear, df
 /* Text for a return code. */
 DFLASH_API const char* dflash_status_string(int code);
 
-/* Library ABI version (major * 100 + minor): 103. */
+/* Library ABI version (major * 100 + minor): 104. */
 DFLASH_API int dflash_version(void);
 
 #ifdef __cplusplus
