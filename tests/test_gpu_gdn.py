@@ -45,6 +45,57 @@ def test_gdn_replay(B, NH, Dk, Dv):
     assert err.max() <= 1e-4 * max(1.0, np.abs(ref).max()), err.max()
 
 
+@pytest.mark.parametrize("g_lo,g_hi", [(-40.0, -20.0), (-400.0, -100.0), (-60.0, 0.0)])
+def test_gdn_replay_strong_decay(g_lo, g_hi):
+    """Decays whose running product leaves the fp32 range of a scale factor
+    (and, at -100 and below, exp(g) that underflows to zero): the replay must
+    still follow the recurrence step by step."""
+    import block_diffusion_speculative_02_gb300 as dfl
+    from oracle.dflash_oracle import bf16_to_f64
+    rng = np.random.default_rng(int(-g_lo))
+    B, NH, Dk, Dv = 2, 3, 128, 64
+    S0, kb, vb, beta, _ = _case(rng, B, NH, Dk, Dv)
+    g = rng.uniform(g_lo, g_hi, size=(B, 16, NH)).astype(np.float32)
+    g[:, ::4] = -0.01                  # some steps barely decay
+    acc = np.array([15, 9], np.int32)
+    state = torch.from_numpy(S0.copy()).cuda()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    dfl.dflash.dflash_gdn_replay(state, dev_bf16(kb), dev_bf16(vb), torch.from_numpy(beta).cuda(),
+                                 torch.from_numpy(g).cuda(), dev_i32(acc), ws)
+    torch.cuda.synchronize()
+    assert dfl.dflash_read_status(ws) == 0
+    ref = ref_replay(S0, bf16_to_f64(kb), bf16_to_f64(vb), beta.astype(np.float64),
+                     g.astype(np.float64), acc + 1)
+    got = state.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    assert np.abs(got - ref).max() <= 1e-4 * max(1.0, np.abs(ref).max())
+
+
+@pytest.mark.parametrize("Dk,Dv", [(128, 128), (64, 128), (128, 64)])
+def test_gdn_replay_many_heads(Dk, Dv):
+    """More 32-row blocks than can be resident at once (several waves of
+    CTAs), over four sequences of which one has an invalid accept length and
+    must keep its state as it was."""
+    import block_diffusion_speculative_02_gb300 as dfl
+    from oracle.dflash_oracle import bf16_to_f64
+    rng = np.random.default_rng(Dk + Dv)
+    B, NH = 4, 500
+    S0, kb, vb, beta, g = _case(rng, B, NH, Dk, Dv)
+    acc = np.array([5, 16, 15, 0], np.int32)
+    state = torch.from_numpy(S0.copy()).cuda()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    dfl.dflash.dflash_gdn_replay(state, dev_bf16(kb), dev_bf16(vb), torch.from_numpy(beta).cuda(),
+                                 torch.from_numpy(g).cuda(), dev_i32(acc), ws)
+    torch.cuda.synchronize()
+    assert dfl.dflash_read_status(ws) & dfl.dflash.STATUS_BITS["capacity"]
+    got = state.cpu().numpy().astype(np.float64)
+    np.testing.assert_array_equal(got[1], S0[1])
+    ok = [0, 2, 3]
+    ref = ref_replay(S0[ok], bf16_to_f64(kb[ok]), bf16_to_f64(vb[ok]),
+                     beta[ok].astype(np.float64), g[ok].astype(np.float64), acc[ok] + 1)
+    assert np.abs(got[ok] - ref).max() <= 1e-4 * max(1.0, np.abs(ref).max())
+
+
 def test_gdn_replay_bad_accept_length_is_flagged():
     import block_diffusion_speculative_02_gb300 as dfl
     rng = np.random.default_rng(9)
