@@ -53,6 +53,8 @@ def parse_args(argv=None):
                     help="extra steps after the timed region with events around every call")
     ap.add_argument("--sets", type=int, default=0,
                     help="rotating input sets (0: enough to exceed twice the L2 size)")
+    ap.add_argument("--prefill-tokens", type=int, default=8192,
+                    help="prompt length of the prefill-projection pass (0 = skip)")
     ap.add_argument("--draft-steps", type=int, default=100,
                     help="extra steps timing the rest of the drafter layer (Q/K/V, attention, "
                          "output projection + MLP, tokens), reported beside the cycle")
@@ -156,6 +158,22 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+PEAK_FALLBACK_TFLOPS = 1900.0
+
+
+def measured_peak_tflops():
+    """Dense bf16 tensor peak (burst) from MEASURED_PEAKS.json, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            if isinstance(d.get("bf16_tflops"), (int, float)):
+                return float(d["bf16_tflops"]), "measured"
+        except (OSError, ValueError):
+            pass
+    return PEAK_FALLBACK_TFLOPS, "fallback"
 
 
 def measured_peak_gbs():
@@ -676,6 +694,54 @@ def main(argv=None):
                         f"1 + a steps replayed",
                "note": "synthetic states; not in the cycle metric"}
 
+    # ---- whole-prompt context projection (prefill), tensor-bound ----
+    prefill = None
+    if args.prefill_tokens > 0:
+        T = args.prefill_tokens
+        B_ = 1
+        gp = torch.Generator(device="cuda")
+        gp.manual_seed(11)
+        pl_hidden = [torch.randn((B_ * T, cfg.hidden), generator=gp, device="cuda")
+                     .to(torch.bfloat16) for _ in range(cfg.n_ctx_layers)]
+        pdims = dfl.make_dims(B_, cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim,
+                              cfg.vocab, cfg.n_ctx_layers, T, rope_theta=cfg.rope_theta)
+        pws = dfl.dflash.alloc_prefill_workspace(pdims, T)
+        pk = torch.empty((B_, cfg.n_kv_heads, T, cfg.head_dim), dtype=torch.bfloat16,
+                         device="cuda")
+        pview = dfl.KVView(pk, torch.empty_like(pk), torch.zeros(B_, dtype=torch.int32,
+                                                                 device="cuda"), capacity=T)
+        zero_pos = torch.zeros(B_, dtype=torch.int32, device="cuda")
+
+        def prefill_call():
+            dfl.dflash.dflash_ctx_prefill(pdims, T, pl_hidden, w.w_fc, w.hidden_norm_w, w.w_k,
+                                          w.w_v, w.k_norm_w, zero_pos, pview, pws)
+
+        for _ in range(3):
+            prefill_call()
+        torch.cuda.synchronize()
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        reps = 10
+        p0.record(stream)
+        for _ in range(reps):
+            prefill_call()
+        p1.record(stream)
+        torch.cuda.synchronize()
+        if dfl.dflash_read_status(pws) != 0:
+            raise RuntimeError("device status set by the prefill projection")
+        p_us = 1e3 * p0.elapsed_time(p1) / reps
+        kvd = cfg.n_kv_heads * cfg.head_dim
+        pflops = 2.0 * B_ * T * cfg.hidden * (cfg.n_ctx_layers * cfg.hidden + 2 * kvd)
+        tpk, tpk_kind = measured_peak_tflops()
+        prefill = {"tokens": B_ * T, "us": p_us, "tokens_per_s": B_ * T / (p_us / 1e6),
+                   "roofline": {"bound": "tensor", "achieved": pflops / (p_us / 1e6) / 1e12,
+                                "peak": tpk, "peak_kind": tpk_kind, "unit": "TFLOP/s",
+                                "frac": pflops / (p_us / 1e6) / 1e12 / tpk,
+                                "flops_per_call": pflops},
+                   "note": "fc GEMM + K/V GEMM over a whole prompt (two launches), "
+                           "not in the cycle metric"}
+        del pl_hidden, pws, pk, pview
+
     # ---- end to end: host buffers in, results out, every step ----
     e2e = None
     if args.e2e_steps > 0:
@@ -754,6 +820,7 @@ def main(argv=None):
             "drafter_layer": draft,
             "verify_attention": vatt,
             "gdn_replay": gdn,
+            "prefill_projection": prefill,
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -207,4 +207,4 @@ extern "C" const char* dflash_status_string(int code) {
   }
 }
 
-extern "C" int dflash_version(void) { return 104; }
+extern "C" int dflash_version(void) { return 105; }

@@ -36,7 +36,8 @@ EXPORTED = ["dflash_workspace_bytes", "dflash_workspace_init", "dflash_ctx_proje
             "dflash_read_status", "dflash_status_string", "dflash_version",
             "dflash_verify_accept_noalloc", "dflash_cycle_sm_split",
             "dflash_draft_workspace_bytes", "dflash_draft_qkv", "dflash_draft_mlp",
-            "dflash_draft_tokens", "dflash_verify_attention", "dflash_gdn_replay"]
+            "dflash_draft_tokens", "dflash_verify_attention", "dflash_gdn_replay",
+            "dflash_prefill_workspace_bytes", "dflash_ctx_prefill"]
 
 
 class DFlashError(RuntimeError):
@@ -90,6 +91,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_verify_attention.argtypes = [ctypes.POINTER(Dims), vp, vp, vp,
                                             ctypes.POINTER(KVViewC), ctypes.c_float, vp, vp, sz,
                                             vp]
+    lib.dflash_prefill_workspace_bytes.restype = sz
+    lib.dflash_prefill_workspace_bytes.argtypes = [ctypes.POINTER(Dims), i32]
+    lib.dflash_ctx_prefill.restype = ctypes.c_int
+    lib.dflash_ctx_prefill.argtypes = [ctypes.POINTER(Dims), i32, ctypes.POINTER(vp), vp, vp, vp,
+                                       vp, vp, vp, ctypes.POINTER(KVViewC), vp, sz, vp]
     lib.dflash_gdn_replay.restype = ctypes.c_int
     lib.dflash_gdn_replay.argtypes = [i32, i32, i32, i32] + [vp] * 6 + [vp, sz, vp]
     lib.dflash_verify_accept.restype = ctypes.c_int
@@ -221,6 +227,34 @@ def dflash_ctx_project(dims: Dims, layer_hidden: Sequence[torch.Tensor], w_fc, h
         _dev(w_v, torch.bfloat16, "w_v"), _dev(k_norm_w, torch.bfloat16, "k_norm_w"),
         _dev(write_pos, torch.int32, "write_pos"), ctypes.byref(view), _dev(ws, name="ws"),
         ws.numel(), _stream(stream)), "dflash_ctx_project")
+
+
+def dflash_prefill_workspace_bytes(dims: Dims, tokens_per_seq: int) -> int:
+    n = load_library().dflash_prefill_workspace_bytes(ctypes.byref(dims), int(tokens_per_seq))
+    if n == 0:
+        raise DFlashError(-3, "dflash_prefill_workspace_bytes")
+    return int(n)
+
+
+def alloc_prefill_workspace(dims: Dims, tokens_per_seq: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace for dflash_ctx_prefill with this many tokens per sequence."""
+    return torch.zeros(dflash_prefill_workspace_bytes(dims, tokens_per_seq), dtype=torch.uint8,
+                       device=device)
+
+
+def dflash_ctx_prefill(dims: Dims, tokens_per_seq: int, layer_hidden: Sequence[torch.Tensor],
+                       w_fc, hidden_norm_w, w_k, w_v, k_norm_w, write_pos, cache: KVView, ws,
+                       stream=None):
+    """Whole-prompt context projection: tokens_per_seq rows per sequence appended at write_pos."""
+    ptrs = (ctypes.c_void_p * len(layer_hidden))(
+        *[_dev(h, torch.bfloat16, "layer_hidden") for h in layer_hidden])
+    view = cache.c()
+    _check(load_library().dflash_ctx_prefill(
+        ctypes.byref(dims), int(tokens_per_seq), ptrs, _dev(w_fc, torch.bfloat16, "w_fc"),
+        _dev(hidden_norm_w, torch.bfloat16, "hidden_norm_w"), _dev(w_k, torch.bfloat16, "w_k"),
+        _dev(w_v, torch.bfloat16, "w_v"), _dev(k_norm_w, torch.bfloat16, "k_norm_w"),
+        _dev(write_pos, torch.int32, "write_pos"), ctypes.byref(view), _dev(ws, name="ws"),
+        ws.numel(), _stream(stream)), "dflash_ctx_prefill")
 
 
 def dflash_block_attention(dims: Dims, q_blk, k_blk, v_blk, cache: KVView, scale: float, out,

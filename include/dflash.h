@@ -302,6 +302,37 @@ DFLASH_API int dflash_draft_tokens(const dflash_dims* dims, const void* x,
                                    void* ws, size_t ws_bytes, dflash_stream_t stream);
 
 /*
+ * Next: the context projection of a whole prompt, for the prefill ([P2]
+ * 单次前向验证 ①: the target prefills the prompt in chunks and so initialises
+ * the caches; [P1] §4: the drafter's context is the projection of the
+ * target's selected-layer hidden states).  The arithmetic of
+ * dflash_ctx_project, for T = tokens_per_seq rows per sequence instead of 16:
+ *   Y = [h_1 | ... | h_nL] W_fc^T;  Y^ = RMSNorm(Y) * hidden_norm_w;
+ *   K = RoPE_pos(RMSNorm_head(Y^ W_k^T) * k_norm_w);  V = Y^ W_v^T,
+ * written into `cache` at rows write_pos[b] + t, t = 0..T-1 (RoPE position =
+ * that row index); pages the rows need are first taken from the free list of
+ * a paged cache; then cache->seq_len[b] = write_pos[b] + T.  write_pos may
+ * alias cache->seq_len.  A long prompt is projected chunk by chunk, each call
+ * appending T rows.  Y^ enters the K/V GEMM rounded once to bf16 (the
+ * per-cycle call keeps it as a hi + lo pair).
+ *   layer_hidden: HOST array of nL device pointers, each bf16 [B*T, H]
+ *                 (row b*T + t).  w_fc, hidden_norm_w, w_k, w_v, k_norm_w as
+ *                 for dflash_ctx_project.  write_pos: int32 [B] device.
+ *   ws: dflash_prefill_workspace_bytes(dims, T) bytes, zeroed once.
+ * Requires hidden % 128 == 0, n_kv_heads * head_dim % 128 == 0.
+ * Errors: DFLASH_ST_CAPACITY (no room for T rows: that sequence is left
+ * alone), DFLASH_ST_POOL_EMPTY / DFLASH_ST_PAGE_MISSING (rows without a page
+ * are skipped).
+ */
+DFLASH_API size_t dflash_prefill_workspace_bytes(const dflash_dims* dims, int32_t tokens_per_seq);
+DFLASH_API int dflash_ctx_prefill(const dflash_dims* dims, int32_t tokens_per_seq,
+                                  const void* const* layer_hidden, const void* w_fc,
+                                  const void* hidden_norm_w, const void* w_k, const void* w_v,
+                                  const void* k_norm_w, const int32_t* write_pos,
+                                  const dflash_kv_view* cache, void* ws, size_t ws_bytes,
+                                  dflash_stream_t stream);
+
+/*
  * Next: rollback of the recurrent state of a hybrid target ([P2] 保证三:
  * GatedDeltaNet states cannot be cut back; the verify forward records each
  * step's innovation and only the accepted steps are replayed; [P1] §7).
@@ -330,7 +361,7 @@ DFLASH_API int dflash_read_status(void* ws, uint32_t* host_status, int clear, df
 /* Text for a return code. */
 DFLASH_API const char* dflash_status_string(int code);
 
-/* Library ABI version (major * 100 + minor): 104. */
+/* Library ABI version (major * 100 + minor): 105. */
 DFLASH_API int dflash_version(void);
 
 #ifdef __cplusplus
