@@ -9,14 +9,19 @@
 //   K  = RoPE(RMSNorm_head(Y^ W_k^T) g_k),   V = Y^ W_v^T.
 // With that many rows the GEMMs are bound by the tensor cores, not by the
 // weight stream, so this is a tiled GEMM rather than the stream-K one:
-// persistent CTAs (one per SM) walk 128 x BN output tiles (token rows x
-// features) in a banded raster order (16 row tiles per band, so the CTAs of
-// one wave share weight tiles and token tiles in L2); a TMA pipeline stages
-// 128 x 64 token boxes and BN x 64 weight boxes; one thread issues
-// tcgen05.mma (M = 128 tokens, N = BN features, K = 16) into one of two TMEM
-// accumulators while four epilogue warps drain the other.  TMEM lane = token
-// row, so the row-wise work of the epilogues (sums of squares, head norms, the
-// RoPE partner at d + D/2) stays inside one thread.
+// persistent CTAs (one per SM) in clusters of two walk pairs of 128 x BN
+// output tiles (token rows x features) that share their feature range, in a
+// banded raster order (8 pairs of row tiles per band, so the clusters of one
+// wave share weight and token tiles in L2).  A TMA pipeline stages each CTA's
+// own 128 x 64 token box, and each CTA loads one half of the BN x 64 weight
+// box multicast to both CTAs of the pair, so every weight byte leaves L2 once
+// per pair (the L2-to-SM traffic per MMA drops by a third); a stage is
+// refilled only when the MMAs of both CTAs have released it (their commits
+// arrive on both CTAs' empty barriers).  One thread issues tcgen05.mma
+// (M = 128 tokens, N = BN features, K = 16) into one of two TMEM accumulators
+// while four epilogue warps drain the other.  TMEM lane = token row, so the
+// row-wise work of the epilogues (sums of squares, head norms, the RoPE
+// partner at d + D/2) stays inside one thread.
 //  1. fc GEMM.  The token operand of k-tile kt is read from layer
 //     floor(64 kt / H) through its own tensor map (the concatenation is never
 //     built).  Epilogue: bf16(g_h * Y) and the tile's sum of Y^2 per row.
@@ -34,7 +39,8 @@ namespace {
 constexpr int kTileThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kTileM = 128;
 constexpr int kATileBytes = kTileM * 128;  // 128 rows x 64 bf16
-constexpr int kBand = 16;                  // row tiles per raster band
+constexpr int kBand = 8;                   // pairs of row tiles per raster band
+constexpr uint16_t kPairMask = 0x3;        // both CTAs of the cluster
 constexpr int kPrefillSmemBudget = 220 * 1024;
 
 struct TileCore {
@@ -69,14 +75,15 @@ struct PrefillParams {
   RopeTable rope;
 };
 
-// Tile t of the raster: bands of kBand row tiles; inside a band the row tile
-// varies fastest, so consecutive tiles (the CTAs of one wave) share weights.
-__device__ __forceinline__ void tile_coords(const TileCore& p, int t, int* m, int* n) {
-  const int per_band = kBand * p.n_tiles;
+// Pair tile t of the raster (row-tile pair mp = rows 256 mp .. 256 mp + 255,
+// feature tile n): bands of kBand pairs; inside a band the pair varies
+// fastest, so consecutive pair tiles (the clusters of one wave) share weights.
+__device__ __forceinline__ void tile_coords(int mp_tiles, int n_tiles, int t, int* mp, int* n) {
+  const int per_band = kBand * n_tiles;
   const int band = t / per_band, r = t - band * per_band;
-  const int bm = min(kBand, p.m_tiles - band * kBand);
+  const int bm = min(kBand, mp_tiles - band * kBand);
   *n = r / bm;
-  *m = band * kBand + (r - *n * bm);
+  *mp = band * kBand + (r - *n * bm);
 }
 
 __device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
@@ -104,13 +111,17 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdrain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* rope_tab = reinterpret_cast<float*>(tmem_slot + 4);
-  const int n_total = p.m_tiles * p.n_tiles;
+  const int crank = static_cast<int>(cluster_ctarank());   // 0 or 1: which tile of the pair
+  const int cid = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  const int mp_tiles = (p.m_tiles + 1) >> 1;
+  const int n_total = mp_tiles * p.n_tiles;                // pair tiles
   const uint32_t acc_cols = static_cast<uint32_t>(p.bn);
+  const int half_rows = p.bn >> 1;                         // weight rows this CTA loads
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.n_stages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], 2);  // the MMAs of both CTAs of the pair
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -133,6 +144,7 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before anything lands in them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   griddep_wait();
@@ -143,12 +155,13 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
       uint32_t stage = 0, phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < n_total; t += gridDim.x) {
-        int m, n;
-        tile_coords(p, t, &m, &n);
+      for (int t = cid; ok && t < n_total; t += n_clusters) {
+        int mp, n;
+        tile_coords(mp_tiles, p.n_tiles, t, &mp, &n);
+        const int m = 2 * mp + crank;
         const bool second = n >= p.b_split;
         const CUtensorMap* mb = second ? &tm_b.m[1] : &tm_b.m[0];
-        const int brow = (second ? n - p.b_split : n) * p.bn;
+        const int brow = (second ? n - p.b_split : n) * p.bn + crank * half_rows;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
             ok = false;
@@ -158,7 +171,8 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
           mbar_arrive_expect_tx(&full[stage], kATileBytes + p.bn * 128);
           const int l = (kt * 64) / p.layer_cols;
           tma_load_2d(a, &tm_a.m[l], &full[stage], kt * 64 - l * p.layer_cols, m * kTileM, pol);
-          tma_load_2d(a + kATileBytes, mb, &full[stage], kt * 64, brow, pol);
+          tma_load_2d_mc(a + kATileBytes + crank * half_rows * 128, mb, &full[stage], kt * 64,
+                         brow, kPairMask, pol);
           ++issued;
           if (++stage == static_cast<uint32_t>(p.n_stages)) {
             stage = 0;
@@ -179,7 +193,7 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
       uint32_t stage = 0, phase = 0;
       int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < n_total; t += gridDim.x, ++it) {
+      for (int t = cid; ok && t < n_total; t += n_clusters, ++it) {
         const int slot = it & 1;
         if (it >= 2 && !mbar_wait(&tempty[slot], static_cast<uint32_t>(((it >> 1) - 1) & 1),
                                   abort_flag, p.status))
@@ -198,7 +212,7 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma_bf16(acc, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kt | kk) ? 1u : 0u);
-          umma_commit(&empty[stage]);
+          umma_commit_mc(&empty[stage], kPairMask);  // frees the stage in both CTAs' eyes
           if (++stage == static_cast<uint32_t>(p.n_stages)) {
             stage = 0;
             phase ^= 1;
@@ -214,9 +228,10 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
     const int q = warp & 3;  // TMEM lane quadrant this warp may read
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     int it = 0;
-    for (int t = blockIdx.x; t < n_total; t += gridDim.x, ++it) {
-      int m, n;
-      tile_coords(p, t, &m, &n);
+    for (int t = cid; t < n_total; t += n_clusters, ++it) {
+      int mp, n;
+      tile_coords(mp_tiles, p.n_tiles, t, &mp, &n);
+      const int m = 2 * mp + crank;
       const int slot = it & 1;
       if (!mbar_wait(&tfull[slot], static_cast<uint32_t>((it >> 1) & 1), abort_flag, p.status))
         break;
@@ -228,6 +243,9 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
     }
   }
   __syncthreads();
+  // the peer may still be releasing stages of this CTA (its MMA commits
+  // arrive here): neither CTA leaves before both have drained
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 2 * acc_cols);
@@ -449,12 +467,35 @@ int run_tile_gemm(TileCore& g, const TokenMaps& am, const WeightMaps& bm,
     if (rc) return rc;
     limit_set = true;
   }
-  const int n_total = g.m_tiles * g.n_tiles;
-  const int nsm = current_num_sms();
-  if (nsm <= 0) return DFLASH_E_CUDA;
-  const int grid = n_total < nsm ? n_total : nsm;
-  return launch(tile_gemm_kernel<Epi>, dim3(grid), dim3(kTileThreads), static_cast<size_t>(smem),
-                st, am, bm, g, ep);
+  // clusters of two, as many as can be resident at once (at most one CTA per SM)
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kTileThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_clusters = 0;  // per instantiation
+  if (max_clusters == 0) {
+    const int nsm = current_num_sms();
+    if (nsm <= 0) return DFLASH_E_CUDA;
+    cfg.gridDim = dim3(nsm & ~1);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tile_gemm_kernel<Epi>, &cfg) != cudaSuccess || n < 1)
+      return DFLASH_E_CUDA;
+    max_clusters = n;
+  }
+  const int pairs = ((g.m_tiles + 1) / 2) * g.n_tiles;
+  const int clusters = pairs < max_clusters ? pairs : max_clusters;
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.numAttrs = 2;
+  return cuda_err(cudaLaunchKernelEx(&cfg, tile_gemm_kernel<Epi>, am, bm, g, ep));
 }
 
 }  // namespace
@@ -539,7 +580,7 @@ extern "C" int dflash_ctx_prefill(const dflash_dims* dims, int32_t tokens_per_se
     for (int l = nL; l < kMaxCtxLayers; ++l) am.m[l] = am.m[0];
     WeightMaps bm;
     if ((rc = make_tmap_2d_bf16(&bm.m[0], w_fc, static_cast<uint64_t>(nL) * H, H,
-                                static_cast<uint64_t>(nL) * H * 2, 64, g.bn)))
+                                static_cast<uint64_t>(nL) * H * 2, 64, g.bn / 2)))
       return rc;
     bm.m[1] = bm.m[0];
     if ((rc = run_tile_gemm<FcEpi>(g, am, bm, ep, st))) return rc;
@@ -561,9 +602,11 @@ extern "C" int dflash_ctx_prefill(const dflash_dims* dims, int32_t tokens_per_se
       return rc;
     for (int l = 1; l < kMaxCtxLayers; ++l) am.m[l] = am.m[0];
     WeightMaps bm;
-    if ((rc = make_tmap_2d_bf16(&bm.m[0], w_k, H, kvd, static_cast<uint64_t>(H) * 2, 64, g.bn)))
+    if ((rc = make_tmap_2d_bf16(&bm.m[0], w_k, H, kvd, static_cast<uint64_t>(H) * 2, 64,
+                                g.bn / 2)))
       return rc;
-    if ((rc = make_tmap_2d_bf16(&bm.m[1], w_v, H, kvd, static_cast<uint64_t>(H) * 2, 64, g.bn)))
+    if ((rc = make_tmap_2d_bf16(&bm.m[1], w_v, H, kvd, static_cast<uint64_t>(H) * 2, 64,
+                                g.bn / 2)))
       return rc;
     if ((rc = run_tile_gemm<KvEpi>(g, am, bm, ep, st))) return rc;
   }
