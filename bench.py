@@ -463,7 +463,7 @@ def main(argv=None):
     __graft_entry__.build()
     world, rank = init_dist("nccl")
     import block_diffusion_speculative_02_gb300 as dfl
-    from block_diffusion_speculative_02_gb300.cycle import (CycleGraph, packed_tensors,
+    from block_diffusion_speculative_02_gb300.cycle import (PipelinedCycles, packed_tensors,
                                                             side_stream, tune_sm_split)
 
     kv_bytes_per_set = 2 * cfg.n_kv_heads * cfg.head_dim * 2 * (
@@ -746,42 +746,50 @@ def main(argv=None):
     e2e = None
     if args.e2e_steps > 0:
         # the step's inputs (verify hidden, selected layer hidden states, block
-        # ids, block Q/K/V) and results (acceptance, next staged token, commit
-        # length, posterior) live in one device buffer each, so that every step
-        # moves them with one host-to-device and one device-to-host copy
+        # ids, block Q/K/V) live in one device buffer per slot and its results
+        # (acceptance, next staged token, commit length, posterior) in one
+        # device buffer, so that every step moves them with one host-to-device
+        # and one device-to-host copy
         src = states[0]
         in_t = [src.verify_hidden, *src.layer_hidden, src.block_ids, src.q_blk, src.k_blk,
                 src.v_blk]
         out_t = [src.accept_len, src.next_staged, src.commit_len, src.posterior]
-        dev_in, ins = packed_tensors([(t.shape, t.dtype) for t in in_t], "cuda")
+        specs = [(t.shape, t.dtype) for t in in_t]
+        slots = [packed_tensors(specs, "cuda") for _ in range(2)]
         dev_out, outs = packed_tensors([(t.shape, t.dtype) for t in out_t], "cuda")
-        for d_, t in zip(ins, in_t):
-            d_.copy_(t)
-        st0 = dataclasses.replace(
+        for _, ins in slots:
+            for d_, t in zip(ins, in_t):
+                d_.copy_(t)
+        st_slots = [dataclasses.replace(
             src, verify_hidden=ins[0], layer_hidden=ins[1:1 + len(src.layer_hidden)],
             block_ids=ins[-4], q_blk=ins[-3], k_blk=ins[-2], v_blk=ins[-1],
             accept_len=outs[0], next_staged=outs[1], commit_len=outs[2], posterior=outs[3])
-        st0.commit_len.copy_(src.commit_len)
-        host_in = dev_in.cpu().pin_memory()
-        host_out = torch.empty_like(dev_out, device="cpu").pin_memory()
+            for _, ins in slots]
+        st_slots[0].commit_len.copy_(src.commit_len)
+        host_in = slots[0][0].cpu().pin_memory()
+        host_out = [torch.empty_like(dev_out, device="cpu").pin_memory() for _ in range(2)]
         h2d = host_in.numel()
-        d2h = host_out.numel()
-        # the serving loop of a fixed-shape batch: the whole cycle, copies in
-        # and out included, as one CUDA graph launched per step
-        cg = CycleGraph(dims, w, st0, ws, [(host_in, dev_in)], [(dev_out, host_out)],
-                        1.0 / math.sqrt(cfg.head_dim), concurrent=concurrent,
-                        sm_split=(verify_sms, project_sms) if concurrent else None)
+        d2h = host_out[0].numel()
+        # the serving loop of a fixed-shape batch: each step is one CUDA graph
+        # (the whole cycle plus the copy of its results to the host); the copy
+        # of the next step's inputs overlaps the current step
+        pc = PipelinedCycles(dims, w, st_slots, ws, [d for d, _ in slots],
+                             [(dev_out, host_out)], 1.0 / math.sqrt(cfg.head_dim),
+                             concurrent=concurrent,
+                             sm_split=(verify_sms, project_sms) if concurrent else None)
         for _ in range(3):
-            cg.replay()
-            torch.cuda.current_stream().synchronize()
+            pc.step(host_in)
+        pc.finish()
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
-            cg.replay()
-            torch.cuda.current_stream().synchronize()
+            pc.step(host_in)
+        pc.finish()
         e2e_s = time.perf_counter() - t0
         e2e_s = max_over_ranks(e2e_s, device="cuda")
         e2e = {"value": whole_job_value(args.e2e_steps, world, e2e_s), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "loop": "PipelinedCycles: one graph per step; the next step's host-to-device "
+                       "copy overlaps the current step; results read back every step"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -213,3 +213,65 @@ class CycleGraph:
     def replay(self):
         """Launch one cycle on the current stream (asynchronous)."""
         self.graph.replay()
+
+
+class PipelinedCycles:
+    """The serving loop of a fixed-shape batch with the host-to-device copy of
+    step k + 1's inputs overlapping step k's cycle.
+
+    Two :class:`CycleGraph` s run over two device copies of the step inputs;
+    the cache state and the results are shared by both, so consecutive steps
+    still chain on the device.  A side stream copies the next step's inputs
+    into the free copy while the current step runs, and at most two steps are
+    in flight: :meth:`step` returns once the previous step's results have
+    reached the host.
+
+    ``states``: two CycleStates that differ only in their input tensors, which
+    are views of ``dev_in[0]`` and ``dev_in[1]`` (one packed device buffer per
+    slot, filled by one copy).  ``outputs``: (device tensor, (host tensor for
+    slot 0, host tensor for slot 1)) pairs of pinned host destinations.
+    Building the object runs the cycle twice (each graph's warm-up)."""
+
+    def __init__(self, dims: Dims, w: CycleWeights, states, ws: torch.Tensor, dev_in, outputs,
+                 scale: Optional[float] = None, concurrent: bool = True,
+                 sm_split: Optional[Tuple[int, int]] = None):
+        if len(states) != 2 or len(dev_in) != 2:
+            raise ValueError("two slots of states and device inputs are needed")
+        self.dev_in = list(dev_in)
+        self.graphs = [CycleGraph(dims, w, st, ws, [], [(d, hs[s]) for d, hs in outputs], scale,
+                                  concurrent, sm_split)
+                       for s, st in enumerate(states)]
+        self.copy_stream = torch.cuda.Stream()
+        self.copied = [torch.cuda.Event(), torch.cuda.Event()]
+        self.done = [torch.cuda.Event(), torch.cuda.Event()]
+        self.k = 0
+
+    def step(self, host_in: torch.Tensor) -> Optional[int]:
+        """Queue one step whose inputs are the pinned host buffer ``host_in``
+        (the layout of ``dev_in``; it must stay unchanged until the next call
+        returns).  Returns the slot whose host outputs now hold the previous
+        step's results (None on the first step)."""
+        s = self.k & 1
+        main = torch.cuda.current_stream()
+        with torch.cuda.stream(self.copy_stream):
+            if self.k >= 2:
+                self.copy_stream.wait_event(self.done[s])   # step k-2 is done with this slot
+            self.dev_in[s].copy_(host_in, non_blocking=True)
+            self.copied[s].record(self.copy_stream)
+        main.wait_event(self.copied[s])
+        self.graphs[s].replay()
+        self.done[s].record(main)
+        prev = None
+        if self.k >= 1:
+            self.done[s ^ 1].synchronize()
+            prev = s ^ 1
+        self.k += 1
+        return prev
+
+    def finish(self) -> Optional[int]:
+        """Wait for the last step queued; returns the slot holding its results."""
+        if self.k == 0:
+            return None
+        s = (self.k - 1) & 1
+        self.done[s].synchronize()
+        return s

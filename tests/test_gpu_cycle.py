@@ -206,3 +206,93 @@ def test_cycle_graph_matches_direct_calls():
     assert np.array_equal(b.out_tokens.cpu().numpy(), a.out_tokens.cpu().numpy())
     assert np.array_equal(b.draft_cache.seq_len.cpu().numpy(), a.draft_cache.seq_len.cpu().numpy())
     np.testing.assert_allclose(host_f64(b.attn_out), host_f64(a.attn_out), atol=2e-2)
+
+
+def test_pipelined_cycles_match_direct_calls():
+    """PipelinedCycles (inputs of step k + 1 copied in while step k runs, two
+    graphs over two input sets, shared state) gives, after three steps with
+    different inputs, the tokens, lengths, results and attention output of
+    issuing the calls step by step."""
+    import dataclasses
+
+    import block_diffusion_speculative_02_gb300 as dfl
+    from block_diffusion_speculative_02_gb300.cycle import (CycleState, CycleWeights,
+                                                            PipelinedCycles, packed_tensors,
+                                                            run_cycle)
+
+    rng = np.random.default_rng(17)
+    B, H, Hq, Hkv, D, V, nL, cap = 2, 256, 4, 2, 64, 4096, 2, 260
+    L0 = np.array([70, 33], np.int32)
+    dims = dfl.make_dims(B, H, Hq, Hkv, D, V, nL, cap)
+    w = CycleWeights(*(dev_bf16(x) for x in (
+        normal_bf16(rng, (V, H), 0.02), normal_bf16(rng, (H, nL * H), 0.02),
+        normal_bf16(rng, (H,), 0.02, 1.0), normal_bf16(rng, (Hkv * D, H), 0.02),
+        normal_bf16(rng, (Hkv * D, H), 0.02), normal_bf16(rng, (D,), 0.02, 1.0))))
+    ck = pack_contiguous_heads([normal_bf16(rng, (int(L), Hkv, D)) for L in L0], cap, Hkv, D)
+    cv = pack_contiguous_heads([normal_bf16(rng, (int(L), Hkv, D)) for L in L0], cap, Hkv, D)
+    specs = [((B * 16, H), torch.bfloat16)] * (1 + nL) + [((B, 16), torch.int32)] + \
+        [((B, 16, Hq, D), torch.bfloat16), ((B, 16, Hkv, D), torch.bfloat16),
+         ((B, 16, Hkv, D), torch.bfloat16)]
+    steps = []
+    for _ in range(3):
+        flat, views = packed_tensors(specs, "cpu", pin=True)
+        vals = [unit_rms_rows_bf16(rng, (B * 16, H)) for _ in range(1 + nL)] + \
+            [rng.integers(0, V, size=(B, 16)).astype(np.int32), normal_bf16(rng, (B, 16, Hq, D)),
+             normal_bf16(rng, (B, 16, Hkv, D)), normal_bf16(rng, (B, 16, Hkv, D))]
+        for v_, x in zip(views, vals):
+            v_.copy_(torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x)
+                     .view(v_.dtype))
+        steps.append(flat)
+
+    def state(ins):
+        draft = dfl.KVView(dev_bf16(ck), dev_bf16(cv), dev_i32(L0), capacity=cap)
+        commit = dev_i32(L0)
+        return CycleState(
+            layer_hidden=list(ins[1:1 + nL]), verify_hidden=ins[0], block_ids=ins[1 + nL],
+            len_before=commit, write_pos=draft.seq_len, q_blk=ins[2 + nL], k_blk=ins[3 + nL],
+            v_blk=ins[4 + nL], draft_cache=draft,
+            target_view=dfl.KVView(None, None, dev_i32(L0 + 16), capacity=cap + 64),
+            posterior=torch.zeros((B, 16), dtype=torch.int32, device="cuda"),
+            accept_len=torch.zeros(B, dtype=torch.int32, device="cuda"),
+            next_staged=torch.zeros(B, dtype=torch.int32, device="cuda"), commit_len=commit,
+            out_tokens=torch.full((B, cap + 64), -1, dtype=torch.int32, device="cuda"),
+            attn_out=torch.zeros((B, 16, Hq, D), dtype=torch.bfloat16, device="cuda"))
+
+    # step by step
+    dev_a, ins_a = packed_tensors(specs, "cuda")
+    a = state(ins_a)
+    ws_a = dfl.alloc_workspace(dims)
+    for flat in steps:
+        dev_a.copy_(flat)
+        run_cycle(dims, w, a, ws_a)
+    torch.cuda.synchronize()
+
+    # pipelined: two input slots, shared state
+    dev0, ins0 = packed_tensors(specs, "cuda")
+    dev1, ins1 = packed_tensors(specs, "cuda")
+    dev0.copy_(steps[0])
+    dev1.copy_(steps[0])
+    b0 = state(ins0)
+    b1 = dataclasses.replace(b0, layer_hidden=list(ins1[1:1 + nL]), verify_hidden=ins1[0],
+                             block_ids=ins1[1 + nL], q_blk=ins1[2 + nL], k_blk=ins1[3 + nL],
+                             v_blk=ins1[4 + nL])
+    outs = [b0.accept_len, b0.posterior, b0.commit_len]
+    host_out = [[torch.empty_like(t, device="cpu").pin_memory() for _ in range(2)] for t in outs]
+    lens = [b0.draft_cache.seq_len, b0.commit_len, b0.target_view.seq_len]
+    saved = [t.clone() for t in lens]
+    pc = PipelinedCycles(dims, w, [b0, b1], dfl.alloc_workspace(dims), [dev0, dev1],
+                         list(zip(outs, host_out)))
+    for t, s in zip(lens, saved):          # undo the two warm-up cycles
+        t.copy_(s)
+    b0.out_tokens.fill_(-1)
+    torch.cuda.synchronize()
+    for flat in steps:
+        pc.step(flat)
+    s = pc.finish()
+    assert np.array_equal(host_out[0][s].numpy(), a.accept_len.cpu().numpy())
+    assert np.array_equal(host_out[1][s].numpy(), a.posterior.cpu().numpy())
+    assert np.array_equal(host_out[2][s].numpy(), a.commit_len.cpu().numpy())
+    assert np.array_equal(b0.out_tokens.cpu().numpy(), a.out_tokens.cpu().numpy())
+    assert np.array_equal(b0.draft_cache.seq_len.cpu().numpy(),
+                          a.draft_cache.seq_len.cpu().numpy())
+    np.testing.assert_allclose(host_f64(b0.attn_out), host_f64(a.attn_out), atol=2e-2)
