@@ -24,6 +24,7 @@ def _dfl():
     (2, 8, 2, 128, [300, 17], True),
     (3, 32, 8, 128, [1000, 64, 5], False),
     (1, 4, 4, 64, [4096], True),
+    (1, 32, 8, 128, [8192], False),        # the Qwen3-8B batch-1 shape the bench times
 ])
 def test_verify_attention(B, Hq, Hkv, D, lens, paged):
     dfl = _dfl()
