@@ -81,10 +81,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
          (static_cast<uint32_t>(float_to_bf16_bits(hi)) << 16);
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // 2^x on the special-function unit (one instruction; -inf gives +0).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

@@ -45,15 +45,16 @@ def test_gdn_replay(B, NH, Dk, Dv):
     assert err.max() <= 1e-4 * max(1.0, np.abs(ref).max()), err.max()
 
 
+@pytest.mark.parametrize("Dv", [64, 128])
 @pytest.mark.parametrize("g_lo,g_hi", [(-40.0, -20.0), (-400.0, -100.0), (-60.0, 0.0)])
-def test_gdn_replay_strong_decay(g_lo, g_hi):
+def test_gdn_replay_strong_decay(g_lo, g_hi, Dv):
     """Decays whose running product leaves the fp32 range of a scale factor
     (and, at -100 and below, exp(g) that underflows to zero): the replay must
     still follow the recurrence step by step."""
     import block_diffusion_speculative_02_gb300 as dfl
     from oracle.dflash_oracle import bf16_to_f64
-    rng = np.random.default_rng(int(-g_lo))
-    B, NH, Dk, Dv = 2, 3, 128, 64
+    rng = np.random.default_rng(int(-g_lo) + Dv)
+    B, NH, Dk = 2, 3, 128
     S0, kb, vb, beta, _ = _case(rng, B, NH, Dk, Dv)
     g = rng.uniform(g_lo, g_hi, size=(B, 16, NH)).astype(np.float32)
     g[:, ::4] = -0.01                  # some steps barely decay
