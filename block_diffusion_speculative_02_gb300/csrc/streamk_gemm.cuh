@@ -310,9 +310,6 @@ streamk_gemm_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ 
 // Dynamic shared memory: 1 KB alignment slack, the stages with their full and
 // empty barriers, then tfull[2], tempty[2], mdrain, four words and the
 // finisher list.
-// Dynamic shared memory: 1 KB alignment slack, the stages with their full and
-// empty barriers, then tfull[2], tempty[2], mdrain, four words and the
-// finisher list.
 constexpr int kGemmTail = 5 * 8 + 4 * 4 + kMaxSegments * 4;
 
 inline int gemm_smem(int stage_bytes, int n_stages) {
