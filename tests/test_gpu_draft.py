@@ -51,6 +51,7 @@ def run_qkv(dfl, dims, x, w, Hq, Hkv, D, ws):
     (1, 256, 4, 2, 64, True),
     (2, 256, 4, 2, 64, False),
     (17, 512, 8, 2, 128, True),      # 272 token rows: three 128-row chunks
+    (32, 256, 4, 2, 64, True),       # the largest batch (512 token rows)
 ])
 def test_draft_qkv(B, H, Hq, Hkv, D, norms):
     dfl = _dfl()
@@ -72,6 +73,7 @@ def test_draft_qkv(B, H, Hq, Hkv, D, norms):
     (1, 256, 4, 64, 512),
     (2, 384, 4, 128, 640),
     (17, 256, 4, 64, 384),           # 272 token rows: several chunks
+    (32, 256, 4, 64, 384),           # the largest batch (512 token rows)
 ])
 def test_draft_mlp(B, H, Hq, D, F):
     dfl = _dfl()

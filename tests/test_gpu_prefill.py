@@ -153,6 +153,47 @@ def test_prefill_flags_capacity():
     assert_close_bf16(k, ref["k"])
 
 
+def test_prefill_flags_an_exhausted_page_pool():
+    """Two 40-row prompts need three pages each; the pool holds four.  Every
+    free page is handed out exactly once, the statuses are raised, the rows
+    that got a page are correct and the others are skipped."""
+    dfl = _dfl()
+    B, T, H, nL, Hkv, D = 2, 40, 256, 2, 2, 64
+    inp = make_inputs(12, B * T, H, nL, Hkv, D)
+    layers, w_fc, gh, wk, wv, gk = inp
+    dims = dfl.make_dims(B, H, 4, Hkv, D, 1000, nL, 64, rope_theta=THETA)
+    ws = dfl.dflash.alloc_prefill_workspace(dims, T)
+    n_pages = 4
+    kc = torch.full((n_pages, Hkv, 16, D), 1.0, dtype=torch.bfloat16, device="cuda")
+    table = np.full((B, 4), -1, np.int32)
+    free = np.array([3, 0, 2, 1], np.int32)
+    view = dfl.KVView(kc, kc.clone(), dev_i32([0, 0]), capacity=64, page_table=dev_i32(table),
+                      free_list=dev_i32(free), free_count=dev_i32([4]), page_size=16)
+    dfl.dflash.dflash_ctx_prefill(dims, T, [dev_bf16(x) for x in layers], dev_bf16(w_fc),
+                                  dev_bf16(gh), dev_bf16(wk), dev_bf16(wv), dev_bf16(gk),
+                                  dev_i32([0, 0]), view, ws)
+    torch.cuda.synchronize()
+    status = dfl.dflash_read_status(ws)
+    assert status & dfl.dflash.STATUS_BITS["pool_empty"]
+    assert status & dfl.dflash.STATUS_BITS["page_missing"]
+    assert int(view.free_count.item()) == 0
+    t = view.page_table.cpu().numpy()
+    got = t[t >= 0]
+    assert sorted(got.tolist()) == [0, 1, 2, 3]
+    pos = np.tile(np.arange(T), B)
+    ref = ref_project(layers, w_fc, gh, wk, wv, gk, pos, Hkv, D, THETA, 1e-6)
+    k = host_f64(view.k)
+    checked = 0
+    for b in range(B):
+        for r in range(T):
+            pg = t[b, r // 16]
+            if pg < 0:
+                continue
+            assert_close_bf16(k[pg, :, r % 16], ref["k"][b * T + r])
+            checked += 1
+    assert checked >= 48      # the four pages carry 64 rows, at most 16 of them past 40
+
+
 def test_prefill_chunks_equal_one_call():
     """A prompt projected in two chunks (the second at write_pos = the first's
     length) lands where one call over the whole prompt puts it."""
