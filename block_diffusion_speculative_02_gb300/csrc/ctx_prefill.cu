@@ -460,14 +460,12 @@ int run_tile_gemm(TileCore& g, const TokenMaps& am, const WeightMaps& bm,
   g.n_stages = (kPrefillSmemBudget - 1024 - tail) / (g.stage_bytes + 16);
   if (g.n_stages > 8) g.n_stages = 8;
   const int smem = 1024 + g.n_stages * (g.stage_bytes + 16) + tail;
-  static bool limit_set = false;  // per instantiation; the limit covers any stage count
-  if (!limit_set) {
-    int rc = set_smem_limit(reinterpret_cast<const void*>(tile_gemm_kernel<Epi>),
-                            kPrefillSmemBudget);
-    if (rc) return rc;
-    limit_set = true;
-  }
-  // clusters of two, as many as can be resident at once (at most one CTA per SM)
+  // once per process and instantiation (thread-safe static initialisation):
+  // the shared-memory limit (it covers any stage count) and how many clusters
+  // of two fit on the device at once (at most one CTA per SM)
+  static const int limit_rc = set_smem_limit(
+      reinterpret_cast<const void*>(tile_gemm_kernel<Epi>), kPrefillSmemBudget);
+  if (limit_rc) return limit_rc;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kTileThreads);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
@@ -481,16 +479,16 @@ int run_tile_gemm(TileCore& g, const TokenMaps& am, const WeightMaps& bm,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  static int max_clusters = 0;  // per instantiation
-  if (max_clusters == 0) {
+  static const int max_clusters = [&cfg] {
     const int nsm = current_num_sms();
-    if (nsm <= 0) return DFLASH_E_CUDA;
-    cfg.gridDim = dim3(nsm & ~1);
+    if (nsm <= 0) return 0;
+    cudaLaunchConfig_t q = cfg;
+    q.gridDim = dim3(nsm & ~1);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tile_gemm_kernel<Epi>, &cfg) != cudaSuccess || n < 1)
-      return DFLASH_E_CUDA;
-    max_clusters = n;
-  }
+    if (cudaOccupancyMaxActiveClusters(&n, tile_gemm_kernel<Epi>, &q) != cudaSuccess) return 0;
+    return n;
+  }();
+  if (max_clusters < 1) return DFLASH_E_CUDA;
   const int pairs = ((g.m_tiles + 1) / 2) * g.n_tiles;
   const int clusters = pairs < max_clusters ? pairs : max_clusters;
   cfg.gridDim = dim3(2 * clusters);
