@@ -1,12 +1,21 @@
 """DFlash per-cycle hot path on GB300: hand-written sm_103a CUDA kernels behind a C ABI.
 
-The four calls of one draft/verify cycle (context projection, dual-source
-block attention, verification epilogue, KV-cache crop) live in
-``libdflash.so``; :mod:`.dflash` is the ctypes binding that the tests and the
-bench call.
+``libdflash.so`` holds the four calls of one draft/verify cycle (context
+projection, dual-source block attention, verification epilogue, KV-cache
+crop) and the calls around it: the rest of the drafter layer and its token
+choice (``dflash_draft_qkv``, ``dflash_draft_mlp``, ``dflash_draft_tokens``),
+the target's verify attention, the whole-prompt context projection of the
+prefill (``dflash_ctx_prefill``) and the GatedDeltaNet tape-replay rollback
+(``dflash_gdn_replay``).  :mod:`.dflash` is the ctypes binding (argument
+marshalling only); :mod:`.cycle` composes one cycle (``run_cycle``), captures
+it as a CUDA graph (``CycleGraph``) and runs the serving loop with the input
+copies overlapped (``PipelinedCycles``).
 """
 from . import dflash  # noqa: F401
-from .dflash import (DFlashError, Dims, KVView, alloc_workspace, dflash_block_attention,  # noqa
-                     dflash_ctx_project, dflash_cycle_sm_split, dflash_kv_crop,
-                     dflash_read_status, dflash_verify_accept, dflash_workspace_bytes,
-                     dflash_workspace_init, load_library, make_dims, with_sm_budget)
+from .dflash import (DFlashError, Dims, KVView, alloc_draft_workspace,  # noqa: F401
+                     alloc_prefill_workspace, alloc_workspace, dflash_block_attention,
+                     dflash_ctx_prefill, dflash_ctx_project, dflash_cycle_sm_split,
+                     dflash_draft_mlp, dflash_draft_qkv, dflash_draft_tokens, dflash_gdn_replay,
+                     dflash_kv_crop, dflash_read_status, dflash_verify_accept,
+                     dflash_verify_attention, dflash_workspace_bytes, dflash_workspace_init,
+                     load_library, make_dims, with_sm_budget)
