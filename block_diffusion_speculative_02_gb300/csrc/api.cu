@@ -3,8 +3,11 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
+#include "common.cuh"
 #include "host.h"
 
 namespace dflash {
@@ -30,6 +33,38 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   });
   return g_encode;
+}
+
+}  // namespace
+
+int injected_failure(const char* entry) {
+  const char* v = std::getenv("DFLASH_FAULT_INJECT");
+  if (!v || !*v) return 0;
+  const size_t n = std::strlen(entry);
+  if (std::strncmp(v, entry, n) != 0 || (v[n] != '\0' && v[n] != ':')) return 0;
+  if (v[n] == ':') {
+    const int code = std::atoi(v + n + 1);
+    if (code < 0) return code;
+  }
+  return DFLASH_E_CUDA;
+}
+
+namespace {
+
+// One warp waits on an mbarrier with the same bounded wait every kernel uses.
+// With arrive == 0 nothing ever arrives: the wait gives up after its time
+// limit and records DFLASH_ST_TIMEOUT, and the kernel returns normally.
+__global__ void selftest_wait_kernel(int arrive, uint32_t* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && arrive) mbar_arrive(&bar);
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, status);
 }
 
 }  // namespace
@@ -207,4 +242,13 @@ extern "C" const char* dflash_status_string(int code) {
   }
 }
 
-extern "C" int dflash_version(void) { return 105; }
+extern "C" int dflash_version(void) { return 106; }
+
+extern "C" int dflash_selftest_wait(int arrive, void* ws, size_t ws_bytes,
+                                    dflash_stream_t stream) {
+  DFLASH_INJECT("dflash_selftest_wait");
+  if (!ws || ws_bytes < 64) return DFLASH_E_WORKSPACE;
+  selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      arrive, static_cast<uint32_t*>(ws));
+  return cuda_err(cudaGetLastError());
+}

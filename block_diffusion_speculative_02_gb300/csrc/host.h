@@ -62,6 +62,17 @@ int make_draft_plan(const dflash_dims& d, int ffn, DraftPlan* p);
 int launch_row_gain(const void* x, const void* gain, int H, int n_tok, void* hl, float* ss,
                     void* out, cudaStream_t st);
 
+// Failure injection for tests (host side, no GPU involved): when the
+// environment variable DFLASH_FAULT_INJECT names an entry point ("name" or
+// "name:code"), that call returns the code (default DFLASH_E_CUDA) before it
+// checks or launches anything.  Read at every call.
+int injected_failure(const char* entry);
+#define DFLASH_INJECT(entry)                          \
+  do {                                                \
+    if (int rc_inj_ = ::dflash::injected_failure(entry)) \
+      return rc_inj_;                                 \
+  } while (0)
+
 int check_dims(const dflash_dims* d);
 int make_plan(const dflash_dims& d, Plan* p);
 int current_num_sms();

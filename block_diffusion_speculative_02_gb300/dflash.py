@@ -37,7 +37,7 @@ EXPORTED = ["dflash_workspace_bytes", "dflash_workspace_init", "dflash_ctx_proje
             "dflash_verify_accept_noalloc", "dflash_cycle_sm_split",
             "dflash_draft_workspace_bytes", "dflash_draft_qkv", "dflash_draft_mlp",
             "dflash_draft_tokens", "dflash_verify_attention", "dflash_gdn_replay",
-            "dflash_prefill_workspace_bytes", "dflash_ctx_prefill"]
+            "dflash_prefill_workspace_bytes", "dflash_ctx_prefill", "dflash_selftest_wait"]
 
 
 class DFlashError(RuntimeError):
@@ -91,6 +91,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_verify_attention.argtypes = [ctypes.POINTER(Dims), vp, vp, vp,
                                             ctypes.POINTER(KVViewC), ctypes.c_float, vp, vp, sz,
                                             vp]
+    lib.dflash_selftest_wait.restype = ctypes.c_int
+    lib.dflash_selftest_wait.argtypes = [ctypes.c_int, vp, sz, vp]
     lib.dflash_prefill_workspace_bytes.restype = sz
     lib.dflash_prefill_workspace_bytes.argtypes = [ctypes.POINTER(Dims), i32]
     lib.dflash_ctx_prefill.restype = ctypes.c_int
@@ -227,6 +229,13 @@ def dflash_ctx_project(dims: Dims, layer_hidden: Sequence[torch.Tensor], w_fc, h
         _dev(w_v, torch.bfloat16, "w_v"), _dev(k_norm_w, torch.bfloat16, "k_norm_w"),
         _dev(write_pos, torch.int32, "write_pos"), ctypes.byref(view), _dev(ws, name="ws"),
         ws.numel(), _stream(stream)), "dflash_ctx_project")
+
+
+def dflash_selftest_wait(arrive: bool, ws, stream=None):
+    """One bounded wait: completed at once (arrive) or timed out after ~1 s (status bit)."""
+    _check(load_library().dflash_selftest_wait(1 if arrive else 0, _dev(ws, name="ws"),
+                                               ws.numel(), _stream(stream)),
+           "dflash_selftest_wait")
 
 
 def dflash_prefill_workspace_bytes(dims: Dims, tokens_per_seq: int) -> int:

@@ -33,6 +33,14 @@
  *    Matrix products accumulate in fp32.
  *  - Device pointers handed to TMA (weights, hidden states, caches) must be
  *    16-byte aligned and their rows a multiple of 16 bytes.
+ *  - Every wait inside a kernel (on an mbarrier, a ticket or a counter) is
+ *    bounded: after about a second it records DFLASH_ST_TIMEOUT and the
+ *    kernel winds down and returns; nothing traps.
+ *  - Failure injection for tests: when the environment variable
+ *    DFLASH_FAULT_INJECT holds the name of an entry point ("dflash_kv_crop")
+ *    or a name and a negative code ("dflash_kv_crop:-5"), that entry point
+ *    returns the code (default DFLASH_E_CUDA) before checking or launching
+ *    anything.  The variable is read at every call.
  */
 #ifndef DFLASH_H_
 #define DFLASH_H_
@@ -361,7 +369,16 @@ DFLASH_API int dflash_read_status(void* ws, uint32_t* host_status, int clear, df
 /* Text for a return code. */
 DFLASH_API const char* dflash_status_string(int code);
 
-/* Library ABI version (major * 100 + minor): 105. */
+/*
+ * Self-test of the bounded wait every kernel uses: one warp waits on an
+ * mbarrier; with arrive != 0 one arrival completes it at once, with
+ * arrive == 0 nothing arrives and the wait gives up after its time limit
+ * (about a second), records DFLASH_ST_TIMEOUT in the status word of `ws`
+ * and the kernel returns; the context stays usable.  ws: at least 64 bytes.
+ */
+DFLASH_API int dflash_selftest_wait(int arrive, void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/* Library ABI version (major * 100 + minor): 106. */
 DFLASH_API int dflash_version(void);
 
 #ifdef __cplusplus

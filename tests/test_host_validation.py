@@ -54,3 +54,22 @@ def test_gdn_replay_rejects_bad_arguments_before_launching():
     assert f(1, 4, 128, 128, None, p, p, p, p, p, p, 256, None) == E_ARG       # no state
     assert f(1, 4, 128, 128, p + 4, p, p, p, p, p, p, 256, None) == E_ALIGN    # misaligned state
     assert f(1, 4, 128, 128, p, p + 2, p, p, p, p, p, 256, None) == E_ALIGN    # misaligned keys
+
+
+def test_fault_injection_returns_before_any_check(monkeypatch):
+    """DFLASH_FAULT_INJECT makes the named entry point fail before it looks at
+    its arguments (so even null pointers give the injected code), and leaves
+    the other entry points alone."""
+    _, lib = _lib()
+    p = 0x1000
+    monkeypatch.setenv("DFLASH_FAULT_INJECT", "dflash_gdn_replay")
+    assert lib.dflash_gdn_replay(0, 0, 0, 0, None, None, None, None, None, None, None, 0,
+                                 None) == -5
+    assert lib.dflash_kv_crop(None, 0, None, 0, None, 0, None) == E_ARG     # not injected
+    monkeypatch.setenv("DFLASH_FAULT_INJECT", "dflash_kv_crop:-4")
+    assert lib.dflash_kv_crop(None, 0, None, 0, None, 0, None) == -4
+    assert lib.dflash_gdn_replay(1, 4, 96, 128, p, p, p, p, p, p, p, 256, None) == E_UNSUPPORTED
+    monkeypatch.setenv("DFLASH_FAULT_INJECT", "dflash_kv")                 # a prefix only
+    assert lib.dflash_kv_crop(None, 0, None, 0, None, 0, None) == E_ARG
+    monkeypatch.delenv("DFLASH_FAULT_INJECT")
+    assert lib.dflash_selftest_wait(1, None, 0, None) == -4                 # no workspace
