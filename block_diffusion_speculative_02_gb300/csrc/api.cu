@@ -246,7 +246,7 @@ extern "C" int dflash_version(void) { return 106; }
 
 extern "C" int dflash_selftest_wait(int arrive, void* ws, size_t ws_bytes,
                                     dflash_stream_t stream) {
-  DFLASH_INJECT("dflash_selftest_wait");
+  DFLASH_ENTRY("dflash_selftest_wait");
   if (!ws || ws_bytes < 64) return DFLASH_E_WORKSPACE;
   selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       arrive, static_cast<uint32_t*>(ws));

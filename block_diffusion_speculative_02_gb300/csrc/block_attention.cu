@@ -907,7 +907,7 @@ extern "C" int dflash_block_attention(const dflash_dims* dims, const void* q_blk
                                       const void* k_blk, const void* v_blk,
                                       const dflash_kv_view* cache, float scale, void* out,
                                       void* ws, size_t ws_bytes, dflash_stream_t stream) {
-  DFLASH_INJECT("dflash_block_attention");
+  DFLASH_ENTRY("dflash_block_attention");
   return run_attention(dims, q_blk, k_blk, v_blk, cache, scale, out, ws, ws_bytes, stream,
                        false);
 }
@@ -916,7 +916,7 @@ extern "C" int dflash_verify_attention(const dflash_dims* dims, const void* q_bl
                                        const void* k_blk, const void* v_blk,
                                        const dflash_kv_view* cache, float scale, void* out,
                                        void* ws, size_t ws_bytes, dflash_stream_t stream) {
-  DFLASH_INJECT("dflash_verify_attention");
+  DFLASH_ENTRY("dflash_verify_attention");
   return run_attention(dims, q_blk, k_blk, v_blk, cache, scale, out, ws, ws_bytes, stream,
                        true);
 }

@@ -514,7 +514,7 @@ extern "C" int dflash_ctx_prefill(const dflash_dims* dims, int32_t tokens_per_se
                                   const void* k_norm_w, const int32_t* write_pos,
                                   const dflash_kv_view* cache, void* ws, size_t ws_bytes,
                                   dflash_stream_t stream) {
-  DFLASH_INJECT("dflash_ctx_prefill");
+  DFLASH_ENTRY("dflash_ctx_prefill");
   if (!dims) return DFLASH_E_ARG;
   PrefillPlan plan;
   int rc = make_prefill_plan(*dims, tokens_per_seq, &plan);

@@ -258,7 +258,7 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
                                   const void* w_v, const void* k_norm_w,
                                   const int32_t* write_pos, const dflash_kv_view* cache,
                                   void* ws, size_t ws_bytes, dflash_stream_t stream) {
-  DFLASH_INJECT("dflash_ctx_project");
+  DFLASH_ENTRY("dflash_ctx_project");
   int rc = check_dims(dims);
   if (rc) return rc;
   if (!layer_hidden || !w_fc || !w_k || !w_v || !write_pos || !cache || !cache->k ||

@@ -376,7 +376,7 @@ extern "C" int dflash_draft_qkv(const dflash_dims* dims, const void* x, const vo
                                 const void* q_norm_w, const void* k_norm_w, void* q_out,
                                 void* k_out, void* v_out, void* ws, size_t ws_bytes,
                                 dflash_stream_t stream) {
-  DFLASH_INJECT("dflash_draft_qkv");
+  DFLASH_ENTRY("dflash_draft_qkv");
   int rc = check_dims(dims);
   if (rc) return rc;
   if (!x || !ln1_w || !w_q || !w_k || !w_v || !q_out || !k_out || !v_out) return DFLASH_E_ARG;
@@ -428,7 +428,7 @@ extern "C" int dflash_draft_mlp(const dflash_dims* dims, int32_t ffn, const void
                                 const void* attn_out, const void* w_o, const void* ln2_w,
                                 const void* w_gate, const void* w_up, const void* w_down,
                                 void* x_out, void* ws, size_t ws_bytes, dflash_stream_t stream) {
-  DFLASH_INJECT("dflash_draft_mlp");
+  DFLASH_ENTRY("dflash_draft_mlp");
   int rc = check_dims(dims);
   if (rc) return rc;
   if (!x || !attn_out || !w_o || !ln2_w || !w_gate || !w_up || !w_down || !x_out)

@@ -216,7 +216,7 @@ extern "C" int dflash_gdn_replay(int32_t batch, int32_t n_heads, int32_t dk, int
                                  const float* tape_beta, const float* tape_g,
                                  const int32_t* accept_len, void* ws, size_t ws_bytes,
                                  dflash_stream_t stream) {
-  DFLASH_INJECT("dflash_gdn_replay");
+  DFLASH_ENTRY("dflash_gdn_replay");
   if (batch < 1 || n_heads < 1 || !state || !tape_k || !tape_v || !tape_beta || !tape_g ||
       !accept_len)
     return DFLASH_E_ARG;

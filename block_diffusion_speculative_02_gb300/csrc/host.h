@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <utility>
 
 #include "../../include/dflash.h"
@@ -72,6 +74,20 @@ int injected_failure(const char* entry);
     if (int rc_inj_ = ::dflash::injected_failure(entry)) \
       return rc_inj_;                                 \
   } while (0)
+
+// One NVTX range per entry-point call, named after the call (seen by
+// profilers; without one attached the push and pop do nothing).
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+
+// Opening statement of every launching entry point.
+#define DFLASH_ENTRY(entry)                  \
+  ::dflash::CallRange call_range_(entry);   \
+  DFLASH_INJECT(entry)
 
 int check_dims(const dflash_dims* d);
 int make_plan(const dflash_dims& d, Plan* p);

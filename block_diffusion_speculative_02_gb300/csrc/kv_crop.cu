@@ -66,7 +66,7 @@ using namespace dflash;
 extern "C" int dflash_kv_crop(const dflash_kv_view* views, int32_t n_views,
                               const int32_t* new_len, int32_t batch, void* ws, size_t ws_bytes,
                               dflash_stream_t stream) {
-  DFLASH_INJECT("dflash_kv_crop");
+  DFLASH_ENTRY("dflash_kv_crop");
   if (!views || n_views < 1 || n_views > kMaxViews || !new_len || batch < 1)
     return DFLASH_E_ARG;
   if (!ws || ws_bytes < 64) return DFLASH_E_WORKSPACE;

@@ -423,7 +423,7 @@ extern "C" int dflash_verify_accept(const dflash_dims* dims, const void* hidden,
                                     int32_t* accept_len, int32_t* next_staged,
                                     int32_t* commit_len, int32_t* out_tokens, int32_t out_cap,
                                     void* ws, size_t ws_bytes, dflash_stream_t stream) {
-  DFLASH_INJECT("dflash_verify_accept");
+  DFLASH_ENTRY("dflash_verify_accept");
   int rc = check_dims(dims);
   if (rc) return rc;
   if (!hidden || !w_lm || !block_ids || !len_before || !posterior || !accept_len ||
@@ -506,7 +506,7 @@ extern "C" int dflash_verify_accept_noalloc(const dflash_dims* dims, const void*
                                             int32_t* accept_len, int32_t* next_staged,
                                             int32_t* commit_len, int32_t* out_tokens,
                                             int32_t out_cap, dflash_stream_t stream) {
-  DFLASH_INJECT("dflash_verify_accept_noalloc");
+  DFLASH_ENTRY("dflash_verify_accept_noalloc");
   int rc = check_dims(dims);
   if (rc) return rc;
   if (dims->batch * kBlock > kNoAllocMaxTokens) return DFLASH_E_UNSUPPORTED;
@@ -544,7 +544,7 @@ extern "C" int dflash_draft_tokens(const dflash_dims* dims, const void* x,
                                    const void* final_norm_w, const void* w_lm,
                                    const int32_t* staged, int32_t* block_ids, int32_t* posterior,
                                    void* ws, size_t ws_bytes, dflash_stream_t stream) {
-  DFLASH_INJECT("dflash_draft_tokens");
+  DFLASH_ENTRY("dflash_draft_tokens");
   int rc = check_dims(dims);
   if (rc) return rc;
   if (!x || !w_lm || !block_ids) return DFLASH_E_ARG;
