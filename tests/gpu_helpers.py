@@ -60,3 +60,32 @@ def assert_close_bf16(got: np.ndarray, ref: np.ndarray, max_abs: float = 2e-2,
     assert mx <= max_abs, (mx, np.unravel_index(int(err.argmax()), err.shape))
     assert rl2 <= rel_l2, rl2
     return {"max_abs": mx, "rel_l2": rl2, "max_ref": float(np.abs(ref).max()) if ref.size else 0}
+
+
+class Guarded:
+    """A device output buffer with guard bands on both sides (filled with the
+    byte 0xA5); ``t`` is the buffer proper, ``check()`` asserts that nothing
+    was written into the bands."""
+
+    CANARY = 0xA5
+
+    def __init__(self, shape, dtype, fill=None, guard_bytes=4096):
+        es = torch.empty((), dtype=dtype).element_size()
+        n = 1
+        for x in shape:
+            n *= int(x)
+        self.g = guard_bytes // es
+        self.n = n
+        self.es = es
+        self.raw = torch.empty(n + 2 * self.g, dtype=dtype, device="cuda")
+        self.raw.view(torch.uint8).fill_(self.CANARY)
+        self.t = self.raw[self.g:self.g + n].view(*shape)
+        if fill is not None:
+            self.t.fill_(fill)
+
+    def check(self):
+        b = self.raw.view(torch.uint8)
+        head = b[:self.g * self.es]
+        tail = b[(self.g + self.n) * self.es:]
+        assert bool((head == self.CANARY).all()), "write before the output buffer"
+        assert bool((tail == self.CANARY).all()), "write past the output buffer"

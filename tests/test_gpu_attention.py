@@ -10,7 +10,7 @@ import torch
 from oracle.dflash_oracle import block_attention as ref_attention
 from synthetic import (CONFIG_BY_NAME, make_cycle_inputs, make_paged_layout, normal_bf16,
                        pack_contiguous_heads, scatter_paged_heads)
-from tests.gpu_helpers import assert_close_bf16, dev_bf16, dev_i32, host_f64
+from tests.gpu_helpers import Guarded, assert_close_bf16, dev_bf16, dev_i32, host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -51,12 +51,13 @@ def run_attention(q, k, v, ctx_k, ctx_v, lens, Hq, Hkv, D, theta, paged=False, c
                 kc[b, :, L:] = 0x7FC1
                 vc[b, :, L:] = 0xFF80
         view = dfl.KVView(dev_bf16(kc), dev_bf16(vc), dev_i32(lens), capacity=cap)
-    out = torch.full((B, 16, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    out = Guarded((B, 16, Hq, D), torch.bfloat16, fill=float("nan"))
     dfl.dflash_block_attention(dims, dev_bf16(q), dev_bf16(k), dev_bf16(v), view,
-                               1.0 / math.sqrt(D), out, ws)
+                               1.0 / math.sqrt(D), out.t, ws)
     torch.cuda.synchronize()
+    out.check()
     status = dfl.dflash_read_status(ws)
-    return host_f64(out), status
+    return host_f64(out.t), status
 
 
 def _rand(seed, B, Hq, Hkv, D, lens):

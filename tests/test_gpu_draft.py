@@ -11,7 +11,8 @@ from oracle.dflash_oracle import bf16_to_f64
 from oracle.dflash_oracle import block_attention as ref_attention
 from oracle.dflash_oracle import draft_out_mlp, draft_qkv, draft_tokens
 from synthetic import normal_bf16, pack_contiguous_heads, unit_rms_rows_bf16
-from tests.gpu_helpers import assert_close_bf16, check_verify, dev_bf16, dev_i32, host_bits, host_f64
+from tests.gpu_helpers import (Guarded, assert_close_bf16, check_verify, dev_bf16, dev_i32,
+                               host_bits, host_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -38,13 +39,16 @@ def _d(x):
 
 def run_qkv(dfl, dims, x, w, Hq, Hkv, D, ws):
     n = x.shape[0]
-    q = torch.empty((n, Hq * D), dtype=torch.bfloat16, device="cuda")
-    k = torch.empty((n, Hkv * D), dtype=torch.bfloat16, device="cuda")
-    v = torch.empty((n, Hkv * D), dtype=torch.bfloat16, device="cuda")
+    q = Guarded((n, Hq * D), torch.bfloat16)
+    k = Guarded((n, Hkv * D), torch.bfloat16)
+    v = Guarded((n, Hkv * D), torch.bfloat16)
     dfl.dflash.dflash_draft_qkv(dims, dev_bf16(x), dev_bf16(w["ln1"]), dev_bf16(w["wq"]),
                                 dev_bf16(w["wk"]), dev_bf16(w["wv"]), _d(w["qn"]), _d(w["kn"]),
-                                q, k, v, ws)
-    return q, k, v
+                                q.t, k.t, v.t, ws)
+    torch.cuda.synchronize()
+    for g in (q, k, v):
+        g.check()
+    return q.t, k.t, v.t
 
 
 @pytest.mark.parametrize("B,H,Hq,Hkv,D,norms", [
@@ -83,12 +87,14 @@ def test_draft_mlp(B, H, Hq, D, F):
     o = normal_bf16(rng, (B * 16, Hq * D), 0.5)
     dims = dfl.make_dims(B, H, Hq, 2, D, 1000, 1, 64)
     ws = dfl.dflash.alloc_draft_workspace(dims, F)
-    out = torch.empty((B * 16, H), dtype=torch.bfloat16, device="cuda")
+    guarded = Guarded((B * 16, H), torch.bfloat16)
+    out = guarded.t
     for _ in range(2):               # the second call finds the workspace as the first left it
         dfl.dflash.dflash_draft_mlp(dims, F, dev_bf16(x), dev_bf16(o), dev_bf16(w["wo"]),
                                     dev_bf16(w["ln2"]), dev_bf16(w["wg"]), dev_bf16(w["wu"]),
                                     dev_bf16(w["wd"]), out, ws)
         torch.cuda.synchronize()
+        guarded.check()
         assert dfl.dflash_read_status(ws) == 0
         ref = draft_out_mlp(x, o, w["wo"], w["ln2"], w["wg"], w["wu"], w["wd"], 1e-6)
         assert np.abs(ref["x2"]).max() < 8          # bf16 half-ulp stays below the tolerance
@@ -122,12 +128,15 @@ def test_draft_tokens(B, H, V):
     dims = dfl.make_dims(B, H, 4, 4, 128, V, 1, 64)
     ws = dfl.dflash.alloc_draft_workspace(dims, 128)
     staged = dev_i32(rng.integers(0, V, size=B))
-    blk = torch.full((B, 16), -5, dtype=torch.int32, device="cuda")
-    post = torch.zeros((B, 16), dtype=torch.int32, device="cuda")
+    gblk = Guarded((B, 16), torch.int32, fill=-5)
+    gpost = Guarded((B, 16), torch.int32, fill=0)
+    blk, post = gblk.t, gpost.t
     for _ in range(2):
         dfl.dflash.dflash_draft_tokens(dims, dev_bf16(x), dev_bf16(fn), dev_bf16(w_lm), staged,
                                        blk, post, ws)
         torch.cuda.synchronize()
+        gblk.check()
+        gpost.check()
         assert dfl.dflash_read_status(ws) == 0
         ref = draft_tokens(x, fn, w_lm, 1e-6)
         got = post.cpu().numpy().reshape(-1)

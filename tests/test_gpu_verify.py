@@ -7,7 +7,7 @@ import torch
 from oracle.dflash_oracle import verify_accept as ref_verify
 from synthetic import (CONFIG_BY_NAME, draw_accept_lengths, make_block_ids, make_cycle_inputs,
                        normal_bf16, unit_rms_rows_bf16)
-from tests.gpu_helpers import check_verify, dev_bf16, dev_i32
+from tests.gpu_helpers import Guarded, check_verify, dev_bf16, dev_i32
 
 pytestmark = pytest.mark.gpu
 
@@ -28,9 +28,9 @@ def gpu_verify(hidden_bits, w_bits, block_ids, len_before, out_cap, prev_out=Non
     w = dev_bf16(w_bits)
     blk = dev_i32(block_ids)
     lb = dev_i32(len_before)
-    post = torch.full((B, 16), -5, dtype=torch.int32, device="cuda")
-    acc = torch.full((B,), -5, dtype=torch.int32, device="cuda")
-    nxt = torch.full((B,), -5, dtype=torch.int32, device="cuda")
+    guards = [Guarded((B, 16), torch.int32, fill=-5), Guarded((B,), torch.int32, fill=-5),
+              Guarded((B,), torch.int32, fill=-5)]
+    post, acc, nxt = (g.t for g in guards)
     cl = lb if alias_len else torch.full((B,), -5, dtype=torch.int32, device="cuda")
     out = dev_i32(prev_out if prev_out is not None else np.full((B, out_cap), -7, np.int32))
     results = []
@@ -40,6 +40,8 @@ def gpu_verify(hidden_bits, w_bits, block_ids, len_before, out_cap, prev_out=Non
         dfl.dflash_verify_accept(dims, hid, w, blk, cl if alias_len else lb, post, acc, nxt, cl,
                                  out, ws)
         torch.cuda.synchronize()
+        for g in guards:
+            g.check()
         results.append({"posterior": post.cpu().numpy(), "accept": acc.cpu().numpy(),
                         "next_staged": nxt.cpu().numpy(), "commit_len": cl.cpu().numpy(),
                         "out_tokens": out.cpu().numpy()})

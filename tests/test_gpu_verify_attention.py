@@ -9,7 +9,7 @@ import torch
 
 from oracle.dflash_oracle import verify_attention as ref_verify_attention
 from synthetic import make_paged_layout, normal_bf16, pack_contiguous_heads, scatter_paged_heads
-from tests.gpu_helpers import assert_close_bf16, dev_bf16, dev_i32, host_bits, host_f64
+from tests.gpu_helpers import Guarded, assert_close_bf16, dev_bf16, dev_i32, host_bits, host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -51,13 +51,14 @@ def test_verify_attention(B, Hq, Hkv, D, lens, paged):
         view = dfl.KVView(dev_bf16(pack_contiguous_heads(ck, cap, Hkv, D)),
                           dev_bf16(pack_contiguous_heads(cv, cap, Hkv, D)), dev_i32(lens),
                           capacity=cap)
-    out = torch.empty((B, 16, Hq, D), dtype=torch.bfloat16, device="cuda")
+    out = Guarded((B, 16, Hq, D), torch.bfloat16)
     dfl.dflash.dflash_verify_attention(dims, dev_bf16(q), dev_bf16(k), dev_bf16(v), view,
-                                       1.0 / math.sqrt(D), out, ws)
+                                       1.0 / math.sqrt(D), out.t, ws)
     torch.cuda.synchronize()
+    out.check()
     assert dfl.dflash_read_status(ws) == 0
     ref = ref_verify_attention(q, k, v, ck, cv, lens, theta, 1.0 / math.sqrt(D))
-    assert_close_bf16(host_f64(out), ref["o"])
+    assert_close_bf16(host_f64(out.t), ref["o"])
     assert np.array_equal(view.seq_len.cpu().numpy(), lens + 16)
     kk, vv = host_f64(view.k), host_bits(view.v)
     table = view.page_table.cpu().numpy() if paged else None
