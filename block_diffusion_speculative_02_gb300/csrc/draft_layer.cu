@@ -70,24 +70,39 @@ __device__ __forceinline__ float silu(float x) { return x / (1.f + __expf(-x)); 
 
 // Per token row (one CTA of 128 threads per row): sum(x^2), and x * g either
 // as a hi/lo bf16 pair (hl != null) or rounded once to bf16 (out != null).
+// A thread's loads of up to kRowBatch groups of 4 features go out together
+// before any of them is used (the row is a handful of round trips otherwise).
+constexpr int kRowBatch = 8;
+
 __global__ void __launch_bounds__(128) row_gain_kernel(const uint16_t* __restrict__ x,
                                                        const uint16_t* __restrict__ gain, int H,
-                                                       int n_tok, uint16_t* hl, float* ss,
-                                                       uint16_t* out) {
+                                                       int n_tok, uint16_t* __restrict__ hl,
+                                                       float* __restrict__ ss,
+                                                       uint16_t* __restrict__ out) {
   griddep_wait();
   __shared__ float red[4];
   const int row = blockIdx.x;
   const uint16_t* xr = x + static_cast<size_t>(row) * H;
   float sq = 0.f;
-  for (int f0 = threadIdx.x * 4; f0 < H; f0 += 128 * 4) {
-    const float4 v = ld4_bf16(xr + f0);
-    const float4 gv = gain ? ld4_bf16(gain + f0) : make_float4(1.f, 1.f, 1.f, 1.f);
-    sq += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-    const float a[4] = {v.x * gv.x, v.y * gv.y, v.z * gv.z, v.w * gv.w};
-    if (hl) store_hilo4(hl, n_tok, H, row, f0, a);
-    if (out)
-      *reinterpret_cast<uint2*>(out + static_cast<size_t>(row) * H + f0) =
-          pack4(a[0], a[1], a[2], a[3]);
+  for (int base = threadIdx.x * 4; base < H; base += kRowBatch * 128 * 4) {
+    float4 v[kRowBatch], gv[kRowBatch];
+#pragma unroll
+    for (int u = 0; u < kRowBatch; ++u) {
+      const int f0 = base + u * 128 * 4;
+      v[u] = f0 < H ? ld4_bf16(xr + f0) : make_float4(0.f, 0.f, 0.f, 0.f);
+      gv[u] = (gain && f0 < H) ? ld4_bf16(gain + f0) : make_float4(1.f, 1.f, 1.f, 1.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kRowBatch; ++u) {
+      const int f0 = base + u * 128 * 4;
+      if (f0 >= H) break;
+      sq += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+      const float a[4] = {v[u].x * gv[u].x, v[u].y * gv[u].y, v[u].z * gv[u].z, v[u].w * gv[u].w};
+      if (hl) store_hilo4(hl, n_tok, H, row, f0, a);
+      if (out)
+        *reinterpret_cast<uint2*>(out + static_cast<size_t>(row) * H + f0) =
+            pack4(a[0], a[1], a[2], a[3]);
+    }
   }
   griddep_launch_dependents();
   if (!ss) return;
