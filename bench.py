@@ -58,6 +58,8 @@ def parse_args(argv=None):
     ap.add_argument("--draft-steps", type=int, default=100,
                     help="extra steps timing the rest of the drafter layer (Q/K/V, attention, "
                          "output projection + MLP, tokens), reported beside the cycle")
+    ap.add_argument("--graph-replays", type=int, default=200,
+                    help="cycles per rep of the graph-replay pass (5 reps; 0 = skip)")
     ap.add_argument("--sm-split", default="",
                     help="verify_sms,project_sms for the side-by-side phase (default: measured "
                          "around the proportional split before the warm-up)")
@@ -463,8 +465,9 @@ def main(argv=None):
     __graft_entry__.build()
     world, rank = init_dist("nccl")
     import block_diffusion_speculative_02_gb300 as dfl
-    from block_diffusion_speculative_02_gb300.cycle import (PipelinedCycles, packed_tensors,
-                                                            side_stream, tune_sm_split)
+    from block_diffusion_speculative_02_gb300.cycle import (CycleGraph, PipelinedCycles,
+                                                            packed_tensors, side_stream,
+                                                            tune_sm_split)
 
     kv_bytes_per_set = 2 * cfg.n_kv_heads * cfg.head_dim * 2 * (
         cfg.batch * (cfg.ctx_len or cfg.ctx_len_range[1]) + 32)
@@ -482,6 +485,7 @@ def main(argv=None):
             verify_sms, project_sms = tune_sm_split(dims, w, states, ws)
         side = side_stream(stream.device)
         fork, join = torch.cuda.Event(), torch.cuda.Event()
+        fork2, join2 = torch.cuda.Event(), torch.cuda.Event()
     else:
         verify_sms = project_sms = 0
         side = stream
@@ -507,10 +511,23 @@ def main(argv=None):
             stream.wait_event(join)
         if ev is not None:
             ev[2].record(stream)
-        dfl.dflash_kv_crop([st.target_view, st.draft_cache], st.commit_len, dims.batch, ws,
-                           stream)
-        dfl.dflash_block_attention(dims, st.q_blk, st.k_blk, st.v_blk, st.draft_cache,
-                                   1.0 / math.sqrt(cfg.head_dim), st.attn_out, ws, stream)
+        if concurrent:
+            # the crop beside the attention, which reads the drafter context's
+            # new length from the commit length (as cycle.run_cycle does)
+            fork2.record(stream)
+            side.wait_event(fork2)
+            dfl.dflash_kv_crop([st.target_view, st.draft_cache], st.commit_len, dims.batch, ws,
+                               side)
+            dfl.dflash_block_attention(dims, st.q_blk, st.k_blk, st.v_blk,
+                                       dataclasses.replace(st.draft_cache, seq_len=st.commit_len),
+                                       1.0 / math.sqrt(cfg.head_dim), st.attn_out, ws, stream)
+            join2.record(side)
+            stream.wait_event(join2)
+        else:
+            dfl.dflash_kv_crop([st.target_view, st.draft_cache], st.commit_len, dims.batch, ws,
+                               stream)
+            dfl.dflash_block_attention(dims, st.q_blk, st.k_blk, st.v_blk, st.draft_cache,
+                                       1.0 / math.sqrt(cfg.head_dim), st.attn_out, ws, stream)
 
     for i in range(args.warmup):
         step(i)
@@ -556,6 +573,35 @@ def main(argv=None):
     traffic = profiled_traffic(os.path.join(ROOT, "block_diffusion_speculative_02_gb300", "csrc",
                                             "verify_accept.cu"),
                                "lmhead_argmax_accept_qwen3_8b_b1.md")
+
+    # ---- the same cycles replayed from CUDA graphs (one per input set) ----
+    graph_cycle = None
+    if args.graph_replays > 0:
+        scale = 1.0 / math.sqrt(cfg.head_dim)
+        graphs = [CycleGraph(dims, w, states[i], ws, [], [], scale, concurrent=concurrent,
+                             sm_split=(verify_sms, project_sms) if concurrent else None)
+                  for i in range(n_sets)]
+        for i in range(3 * n_sets):
+            graphs[i % n_sets].replay()
+        torch.cuda.synchronize()
+        reps = []
+        for _ in range(5):
+            g0 = torch.cuda.Event(enable_timing=True)
+            g1 = torch.cuda.Event(enable_timing=True)
+            g0.record(stream)
+            for i in range(args.graph_replays):
+                graphs[i % n_sets].replay()
+            g1.record(stream)
+            torch.cuda.synchronize()
+            reps.append(1e3 * g0.elapsed_time(g1) / args.graph_replays)
+        if dfl.dflash_read_status(ws) != 0:
+            raise RuntimeError("device status set by the graph replays")
+        del graphs
+        us_c = statistics.median(reps)
+        graph_cycle = {"value": 1e6 / us_c, "unit": UNIT, "us_per_cycle": us_c,
+                       "reps_us": reps, "replays_per_rep": args.graph_replays,
+                       "note": "the timed cycle replayed from CUDA graphs (one per rotating input "
+                               "set), median of 5 reps"}
 
     # ---- per-call breakdown (separate pass, events between the calls) ----
     breakdown = None
@@ -887,6 +933,7 @@ def main(argv=None):
                          "frac": lm_gbs / peak, "traffic": traffic,
                          "bytes_per_launch": bytes_["lm_head"], "avg_launch_ms": lm_ms},
             "gpu_launches": launches_per_step * args.steps,
+            "graph_replay": graph_cycle,
             "breakdown": breakdown,
             "drafter_layer": draft,
             "verify_attention": vatt,

@@ -12,10 +12,13 @@ Verification and the projection do not depend on each other (the projection
 reads the target's hidden states and the drafter's write position, not the
 acceptance), so by default they run side by side: verify on the caller's
 stream, the projection on a side stream, each on its own share of the SMs
-(``dflash_cycle_sm_split``), joined before the crop.
+(``dflash_cycle_sm_split``), joined before the crop.  The crop then runs on
+the side stream beside the attention, which takes the drafter context's new
+length from the commit length rather than waiting for the crop to write it.
 """
 from __future__ import annotations
 
+import dataclasses
 import math
 from dataclasses import dataclass
 from typing import List, Optional, Tuple
@@ -136,17 +139,41 @@ def run_cycle(dims: Dims, w: CycleWeights, st: CycleState, ws: torch.Tensor,
     main = torch.cuda.current_stream() if stream is None else stream
     if concurrent:
         verify_sms, project_sms = sm_split or dflash_cycle_sm_split(dims)
+        side = side_stream(st.verify_hidden.device)
         _verify_and_project(with_sm_budget(dims, verify_sms), with_sm_budget(dims, project_sms),
-                            w, st, ws, main, side_stream(st.verify_hidden.device))
-    else:
-        dflash_verify_accept(dims, st.verify_hidden, w.w_lm, st.block_ids, st.len_before,
-                             st.posterior, st.accept_len, st.next_staged, st.commit_len,
-                             st.out_tokens, ws, main)
-        dflash_ctx_project(dims, st.layer_hidden, w.w_fc, w.hidden_norm_w, w.w_k, w.w_v,
-                           w.k_norm_w, st.write_pos, st.draft_cache, ws, main)
+                            w, st, ws, main, side)
+        _crop_beside_attention(dims, st, ws, scale, main, side)
+        return
+    dflash_verify_accept(dims, st.verify_hidden, w.w_lm, st.block_ids, st.len_before,
+                         st.posterior, st.accept_len, st.next_staged, st.commit_len,
+                         st.out_tokens, ws, main)
+    dflash_ctx_project(dims, st.layer_hidden, w.w_fc, w.hidden_norm_w, w.w_k, w.w_v,
+                       w.k_norm_w, st.write_pos, st.draft_cache, ws, main)
     dflash_kv_crop([st.target_view, st.draft_cache], st.commit_len, dims.batch, ws, main)
     dflash_block_attention(dims, st.q_blk, st.k_blk, st.v_blk, st.draft_cache, scale,
                            st.attn_out, ws, main)
+
+
+def _crop_beside_attention(dims: Dims, st: CycleState, ws: torch.Tensor, scale: float, main,
+                           side):
+    """The crop on ``side`` while the attention runs on ``main``, joined back.
+
+    The crop sets the drafter context's length to the commit length; the
+    attention reads that length from ``commit_len`` itself, so it need not
+    wait for the crop.  The crop releases only pages at or past the new
+    length, which the attention never reads, and it touches only the status
+    word of the workspace.  The join keeps the next cycle (whose verification
+    rewrites ``commit_len``) behind the crop."""
+    fork = torch.cuda.Event()
+    fork.record(main)
+    side.wait_event(fork)
+    dflash_kv_crop([st.target_view, st.draft_cache], st.commit_len, dims.batch, ws, side)
+    dflash_block_attention(dims, st.q_blk, st.k_blk, st.v_blk,
+                           dataclasses.replace(st.draft_cache, seq_len=st.commit_len), scale,
+                           st.attn_out, ws, main)
+    join = torch.cuda.Event()
+    join.record(side)
+    main.wait_event(join)
 
 
 def packed_tensors(specs, device, pin: bool = False):

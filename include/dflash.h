@@ -19,7 +19,9 @@
  *    dflash_workspace_init(); every call leaves its part of it zeroed again.
  *    Calls that share a workspace must be ordered on the GPU (same stream or
  *    events), except dflash_ctx_project and dflash_verify_accept, which use
- *    disjoint parts of it and may run concurrently on two streams.
+ *    disjoint parts of it and may run concurrently on two streams, and
+ *    dflash_kv_crop, which only sets bits of the status word (atomically)
+ *    and may run concurrently with any call.
  *  - Every call is asynchronous on `stream` and never synchronises the host,
  *    except dflash_read_status.  Lengths stay on the device, so a whole cycle
  *    can be captured in a CUDA graph.
@@ -179,6 +181,11 @@ DFLASH_API int dflash_ctx_project(const dflash_dims* dims, const void* const* la
  *   out: bf16 [B,16,Hq,D].  Lengths above cache capacity set DFLASH_ST_CAPACITY
  *   (that sequence's output is left unwritten); unmapped pages inside the
  *   length set DFLASH_ST_PAGE_MISSING and are read as zeros.
+ *   The cache is only read: its rows, and its page-table slots, below L.
+ *   cache->seq_len may point at any int32 [B] array of lengths, e.g. the
+ *   commit_len written by dflash_verify_accept, so that the attention need
+ *   not wait for the dflash_kv_crop that stores the same lengths in the view
+ *   (the crop releases only pages at or past the new length).
  */
 DFLASH_API int dflash_block_attention(const dflash_dims* dims, const void* q_blk, const void* k_blk,
                            const void* v_blk, const dflash_kv_view* cache, float scale,
