@@ -10,7 +10,10 @@ written at a fixed context position, the crop trims it to the committed
 length and the attention of the next block reads that length.  Verification
 and the projection run side by side on two streams, each on its own share of
 the SMs (the split is measured once before the warm-up; --sm-split fixes it,
---serial queues everything on one stream).
+--serial queues everything on one stream); the crop then runs on the side
+stream beside the attention, which reads the committed length directly.
+Beside `value` (calls issued step by step) the line reports the same cycle
+replayed from CUDA graphs (`graph_replay`).
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 N > 1 runs under torchrun: every rank runs an independent replica (sequences
