@@ -251,7 +251,9 @@ def build_workload(cfg, n_sets: int, device="cuda"):
     for r in range(n_sets):
         i32 = lambda a: torch.as_tensor(np.asarray(a, np.int32), device=device)  # noqa: E731
         if cfg.paged:
-            lay = make_paged_layout(host["pages"], lens, reserve_tokens=16, slack_pages=64)
+            # room for the cycle's 16 projected rows and, on top of the
+            # committed length, the 16 rows the verify-attention pass appends
+            lay = make_paged_layout(host["pages"], lens, reserve_tokens=32, slack_pages=64)
             n_rows = lay.n_pages * 16
             k = device_normal_bf16(gen["ctx_k"], (lay.n_pages, Hkv, 16, D), device=device)
             v = device_normal_bf16(gen["ctx_v"], (lay.n_pages, Hkv, 16, D), device=device)
@@ -573,9 +575,29 @@ def main(argv=None):
     peak, peak_kind = measured_peak_gbs()
     lm_gbs = bytes_["lm_head"] / (lm_ms / 1e3) / 1e9
     cycle_gbs = bytes_["total"] * args.steps / elapsed_s / 1e9
+    # the committed DRAM capture is of the Qwen3-8B batch-1 launch only
     traffic = profiled_traffic(os.path.join(ROOT, "block_diffusion_speculative_02_gb300", "csrc",
                                             "verify_accept.cu"),
-                               "lmhead_argmax_accept_qwen3_8b_b1.md")
+                               "lmhead_argmax_accept_qwen3_8b_b1.md") \
+        if cfg.name == "qwen3_8b_b1" else None
+
+    # the LM head's bound is the larger of its weight-stream time and its
+    # tensor time (2 B 16 H V flops): HBM at small batch, the tensor cores at
+    # batch 32; both fractions are reported
+    lm_flops = 2.0 * cfg.batch * 16 * cfg.hidden * cfg.vocab
+    tpk, tpk_kind = measured_peak_tflops()
+    lm_tflops = lm_flops / (lm_ms / 1e3) / 1e12
+    tensor_bound = lm_flops / (tpk * 1e12) > bytes_["lm_head"] / (peak * 1e9)
+    lm_roofline = {"bound": "tensor" if tensor_bound else "hbm",
+                   "kernel": "lmhead_argmax_accept",
+                   "achieved": lm_tflops if tensor_bound else lm_gbs,
+                   "peak": tpk if tensor_bound else peak,
+                   "peak_kind": tpk_kind if tensor_bound else peak_kind,
+                   "unit": "TFLOP/s" if tensor_bound else "GB/s",
+                   "frac": lm_tflops / tpk if tensor_bound else lm_gbs / peak,
+                   "traffic": traffic, "bytes_per_launch": bytes_["lm_head"],
+                   "flops_per_launch": lm_flops, "avg_launch_ms": lm_ms,
+                   "hbm_frac": lm_gbs / peak, "tensor_frac": lm_tflops / tpk}
 
     # ---- the same cycles replayed from CUDA graphs (one per input set) ----
     graph_cycle = None
@@ -598,7 +620,8 @@ def main(argv=None):
             torch.cuda.synchronize()
             reps.append(1e3 * g0.elapsed_time(g1) / args.graph_replays)
         if dfl.dflash_read_status(ws) != 0:
-            raise RuntimeError("device status set by the graph replays")
+            raise RuntimeError(f"device status {dfl.dflash_read_status(ws):#x} "
+                               "set by the graph replays")
         del graphs
         us_c = statistics.median(reps)
         graph_cycle = {"value": 1e6 / us_c, "unit": UNIT, "us_per_cycle": us_c,
@@ -666,7 +689,8 @@ def main(argv=None):
         d1.record(stream)
         torch.cuda.synchronize()
         if dfl.dflash_read_status(dws) != 0:
-            raise RuntimeError("device status set by the drafter calls")
+            raise RuntimeError(f"device status {dfl.dflash_read_status(dws):#x} "
+                               "set by the drafter calls")
         d_us_calls = 1e3 * d0.elapsed_time(d1) / args.draft_steps
         # the same steps replayed from CUDA graphs (one per rotating input set,
         # so the context caches still come from DRAM): no host work between
@@ -693,7 +717,8 @@ def main(argv=None):
         d1.record()
         torch.cuda.synchronize()
         if dfl.dflash_read_status(dws) != 0:
-            raise RuntimeError("device status set by the drafter calls")
+            raise RuntimeError(f"device status {dfl.dflash_read_status(dws):#x} "
+                               "set by the drafter calls")
         d_us = 1e3 * d0.elapsed_time(d1) / args.draft_steps
         del graphs
         dbytes = draft_bytes(cfg) + bytes_["attention"]
@@ -760,7 +785,8 @@ def main(argv=None):
         us_reset = replay_us(g_r, args.draft_steps)
         us = us_both - us_reset
         if dfl.dflash_read_status(ws) != 0:
-            raise RuntimeError("device status set by the verify attention")
+            raise RuntimeError(f"device status {dfl.dflash_read_status(ws):#x} "
+                               "set by the verify attention")
         dc.seq_len.copy_(L0)
         vbytes = bytes_["attention"] + 2 * cfg.batch * 16 * cfg.n_kv_heads * D_ * 2
         vatt = {"us": us, "bytes": vbytes, "gbs": vbytes / (us / 1e6) / 1e9,
@@ -796,7 +822,8 @@ def main(argv=None):
         g1.record(stream)
         torch.cuda.synchronize()
         if dfl.dflash_read_status(gws) != 0:
-            raise RuntimeError("device status set by the GDN replay")
+            raise RuntimeError(f"device status {dfl.dflash_read_status(gws):#x} "
+                               "set by the GDN replay")
         us = 1e3 * g0.elapsed_time(g1) / args.draft_steps
         steps = int(acc_g.sum().item()) + Bg
         gbytes = Bg * NH * DV * DK * 4 * 2 + steps * NH * ((DK + DV) * 2 + 8)
@@ -840,7 +867,8 @@ def main(argv=None):
         p1.record(stream)
         torch.cuda.synchronize()
         if dfl.dflash_read_status(pws) != 0:
-            raise RuntimeError("device status set by the prefill projection")
+            raise RuntimeError(f"device status {dfl.dflash_read_status(pws):#x} "
+                               "set by the prefill projection")
         p_us = 1e3 * p0.elapsed_time(p1) / reps
         kvd = cfg.n_kv_heads * cfg.head_dim
         pflops = 2.0 * B_ * T * cfg.hidden * (cfg.n_ctx_layers * cfg.hidden + 2 * kvd)
@@ -931,10 +959,7 @@ def main(argv=None):
             "verify_project_phase": {
                 "us": 1e3 * phase_ms,
                 "gbs": (bytes_["lm_head"] + bytes_["ctx_project"]) / (phase_ms / 1e3) / 1e9},
-            "roofline": {"bound": "hbm", "kernel": "lmhead_argmax_accept", "achieved": lm_gbs,
-                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": lm_gbs / peak, "traffic": traffic,
-                         "bytes_per_launch": bytes_["lm_head"], "avg_launch_ms": lm_ms},
+            "roofline": lm_roofline,
             "gpu_launches": launches_per_step * args.steps,
             "graph_replay": graph_cycle,
             "breakdown": breakdown,

@@ -8,20 +8,11 @@
 //   Y  = [h_1 | ... | h_nL] W_fc^T,   Y^ = RMSNorm(Y) g_h,
 //   K  = RoPE(RMSNorm_head(Y^ W_k^T) g_k),   V = Y^ W_v^T.
 // With that many rows the GEMMs are bound by the tensor cores, not by the
-// weight stream, so this is a tiled GEMM rather than the stream-K one:
-// persistent CTAs (one per SM) in clusters of two walk pairs of 128 x BN
-// output tiles (token rows x features) that share their feature range, in a
-// banded raster order (8 pairs of row tiles per band, so the clusters of one
-// wave share weight and token tiles in L2).  A TMA pipeline stages each CTA's
-// own 128 x 64 token box, and each CTA loads one half of the BN x 64 weight
-// box multicast to both CTAs of the pair, so every weight byte leaves L2 once
-// per pair (the L2-to-SM traffic per MMA drops by a third); a stage is
-// refilled only when the MMAs of both CTAs have released it (their commits
-// arrive on both CTAs' empty barriers).  One thread issues tcgen05.mma
-// (M = 128 tokens, N = BN features, K = 16) into one of two TMEM accumulators
-// while four epilogue warps drain the other.  TMEM lane = token row, so the
-// row-wise work of the epilogues (sums of squares, head norms, the RoPE
-// partner at d + D/2) stays inside one thread.
+// weight stream, so they run on the tiled GEMM of tile_gemm.cuh (persistent
+// clusters of two CTAs over 128 x BN output tiles, the weight box multicast
+// to both CTAs of a pair, TMEM lane = token row) rather than on the stream-K
+// one; the row-wise work of the epilogues (sums of squares, head norms, the
+// RoPE partner at d + D/2) stays inside one thread.
 //  1. fc GEMM.  The token operand of k-tile kt is read from layer
 //     floor(64 kt / H) through its own tensor map (the concatenation is never
 //     built).  Epilogue: bf16(g_h * Y) and the tile's sum of Y^2 per row.
@@ -32,34 +23,10 @@
 //     bf16 stores into the cache rows.
 #include "common.cuh"
 #include "host.h"
+#include "tile_gemm.cuh"
 
 namespace dflash {
 namespace {
-
-constexpr int kTileThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kTileM = 128;
-constexpr int kATileBytes = kTileM * 128;  // 128 rows x 64 bf16
-constexpr int kBand = 8;                   // pairs of row tiles per raster band
-constexpr uint16_t kPairMask = 0x3;        // both CTAs of the cluster
-constexpr int kPrefillSmemBudget = 220 * 1024;
-
-struct TileCore {
-  int rows;          // token rows (M)
-  int m_tiles, n_tiles, k_tiles;
-  int bn;            // features per tile: 128 or 256
-  int layer_cols;    // token map l holds columns [l * layer_cols, (l + 1) * layer_cols)
-  int b_split;       // feature tiles below it read weight map 0, the others map 1
-  int n_stages, stage_bytes;
-  uint32_t* status;
-};
-
-struct TokenMaps {
-  CUtensorMap m[kMaxCtxLayers];
-};
-
-struct WeightMaps {
-  CUtensorMap m[2];
-};
 
 struct PrefillParams {
   int hidden, fc_n_tiles, tokens_per_seq, batch;
@@ -75,182 +42,9 @@ struct PrefillParams {
   RopeTable rope;
 };
 
-// Pair tile t of the raster (row-tile pair mp = rows 256 mp .. 256 mp + 255,
-// feature tile n): bands of kBand pairs; inside a band the pair varies
-// fastest, so consecutive pair tiles (the clusters of one wave) share weights.
-__device__ __forceinline__ void tile_coords(int mp_tiles, int n_tiles, int t, int* mp, int* n) {
-  const int per_band = kBand * n_tiles;
-  const int band = t / per_band, r = t - band * per_band;
-  const int bm = min(kBand, mp_tiles - band * kBand);
-  *n = r / bm;
-  *mp = band * kBand + (r - *n * bm);
-}
-
 __device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
   return static_cast<uint32_t>(float_to_bf16_bits(a)) |
          (static_cast<uint32_t>(float_to_bf16_bits(b)) << 16);
-}
-
-// Shared memory after the stages: full[n], empty[n], tfull[2], tempty[2],
-// mdrain, the TMEM address, the abort flag, two spare words, then the RoPE
-// table (hi[64], lo[64]).
-constexpr int kTileTailFixed = 5 * 8 + 4 * 4 + 128 * 4;
-
-template <class Epi>
-__global__ void __launch_bounds__(kTileThreads, 1)
-tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__ WeightMaps tm_b,
-                 const TileCore p, const __grid_constant__ PrefillParams ep) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align_smem_1024(smem_raw);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.n_stages * p.stage_bytes);
-  uint64_t* empty = full + p.n_stages;
-  uint64_t* tfull = empty + p.n_stages;   // [2] accumulator ready
-  uint64_t* tempty = tfull + 2;           // [2] accumulator drained
-  uint64_t* mdrain = tempty + 2;          // every MMA issued has completed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdrain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* rope_tab = reinterpret_cast<float*>(tmem_slot + 4);
-  const int crank = static_cast<int>(cluster_ctarank());   // 0 or 1: which tile of the pair
-  const int cid = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
-  const int mp_tiles = (p.m_tiles + 1) >> 1;
-  const int n_total = mp_tiles * p.n_tiles;                // pair tiles
-  const uint32_t acc_cols = static_cast<uint32_t>(p.bn);
-  const int half_rows = p.bn >> 1;                         // weight rows this CTA loads
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < p.n_stages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 2);  // the MMAs of both CTAs of the pair
-    }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 128);
-    }
-    mbar_init(mdrain, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, 2 * acc_cols);
-    tmem_relinquish();
-  }
-  if (threadIdx.x >= 64) {
-    const int i = threadIdx.x - 64;
-    if (i < 64) {
-      rope_tab[i] = ep.rope.hi[i];
-      rope_tab[64 + i] = ep.rope.lo[i];
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // the peer's barriers are initialised before anything lands in them
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  griddep_wait();
-
-  if (warp == 0) {
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_normal();
-      uint32_t stage = 0, phase = 0;
-      int issued = 0;
-      bool ok = true;
-      for (int t = cid; ok && t < n_total; t += n_clusters) {
-        int mp, n;
-        tile_coords(mp_tiles, p.n_tiles, t, &mp, &n);
-        const int m = 2 * mp + crank;
-        const bool second = n >= p.b_split;
-        const CUtensorMap* mb = second ? &tm_b.m[1] : &tm_b.m[0];
-        const int brow = (second ? n - p.b_split : n) * p.bn + crank * half_rows;
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          uint8_t* a = smem + stage * p.stage_bytes;
-          mbar_arrive_expect_tx(&full[stage], kATileBytes + p.bn * 128);
-          const int l = (kt * 64) / p.layer_cols;
-          tma_load_2d(a, &tm_a.m[l], &full[stage], kt * 64 - l * p.layer_cols, m * kTileM, pol);
-          tma_load_2d_mc(a + kATileBytes + crank * half_rows * 128, mb, &full[stage], kt * 64,
-                         brow, kPairMask, pol);
-          ++issued;
-          if (++stage == static_cast<uint32_t>(p.n_stages)) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-      }
-      // no copy may still be landing when the CTA exits
-      for (int st = 0; st < p.n_stages && st < issued; ++st) {
-        const int last = st + ((issued - 1 - st) / p.n_stages) * p.n_stages;
-        mbar_wait_drain(&full[st], static_cast<uint32_t>((last / p.n_stages) & 1), p.status);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t base = smem_u32(smem);
-      const uint32_t idesc = umma_idesc_bf16(kTileM, p.bn);
-      uint32_t stage = 0, phase = 0;
-      int it = 0;
-      bool ok = true;
-      for (int t = cid; ok && t < n_total; t += n_clusters, ++it) {
-        const int slot = it & 1;
-        if (it >= 2 && !mbar_wait(&tempty[slot], static_cast<uint32_t>(((it >> 1) - 1) & 1),
-                                  abort_flag, p.status))
-          break;
-        tc_fence_after();
-        const uint32_t acc = tmem_base + slot * acc_cols;
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = base + stage * p.stage_bytes;
-          const uint64_t adesc = umma_sdesc_sw128(a_addr);
-          const uint64_t bdesc = umma_sdesc_sw128(a_addr + kATileBytes);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(acc, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kt | kk) ? 1u : 0u);
-          umma_commit_mc(&empty[stage], kPairMask);  // frees the stage in both CTAs' eyes
-          if (++stage == static_cast<uint32_t>(p.n_stages)) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-        if (ok) umma_commit(&tfull[slot]);
-      }
-      umma_commit(mdrain);
-      mbar_wait_drain(mdrain, 0, p.status);
-    }
-  } else {
-    if (blockIdx.x == 0) Epi::prologue(p, ep);
-    const int q = warp & 3;  // TMEM lane quadrant this warp may read
-    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    int it = 0;
-    for (int t = cid; t < n_total; t += n_clusters, ++it) {
-      int mp, n;
-      tile_coords(mp_tiles, p.n_tiles, t, &mp, &n);
-      const int m = 2 * mp + crank;
-      const int slot = it & 1;
-      if (!mbar_wait(&tfull[slot], static_cast<uint32_t>((it >> 1) & 1), abort_flag, p.status))
-        break;
-      tc_fence_after();
-      Epi::tile(p, ep, n, tmem_base + slot * acc_cols + lane_base, m * kTileM + q * 32 + lane,
-                rope_tab);
-      tc_fence_before();
-      mbar_arrive(&tempty[slot]);
-    }
-  }
-  __syncthreads();
-  // the peer may still be releasing stages of this CTA (its MMA commits
-  // arrive here): neither CTA leaves before both have drained
-  cluster_sync();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, 2 * acc_cols);
-  }
-  griddep_launch_dependents();
 }
 
 // Per sequence: snapshot the write position, map the pages rows pos..pos+T-1
@@ -272,6 +66,8 @@ __device__ void reserve_prompt_rows(const PrefillParams& e, uint32_t* status, in
 // fc epilogue: thread = token row; Y of the tile's bn features in 16-column
 // pieces: bf16(g_h * Y) to yhat and the row's sum of Y^2 over the tile.
 struct FcEpi {
+  using Params = PrefillParams;
+  static __device__ void setup(const PrefillParams&, float*, int) {}
   static __device__ void prologue(const TileCore& p, const PrefillParams& e) {
     for (int b = threadIdx.x - 64; b < e.batch; b += 128) reserve_prompt_rows(e, p.status, b);
   }
@@ -322,6 +118,14 @@ struct FcEpi {
 // RoPE with the partner dimension d + D/2 loaded beside d; bf16 stores into
 // the cache row write_pos + t.
 struct KvEpi {
+  using Params = PrefillParams;
+  // the RoPE table (hi[64], lo[64]) into shared memory
+  static __device__ void setup(const PrefillParams& e, float* tab, int i) {
+    if (i < 64) {
+      tab[i] = e.rope.hi[i];
+      tab[64 + i] = e.rope.lo[i];
+    }
+  }
   static __device__ void prologue(const TileCore&, const PrefillParams&) {}
   static __device__ void tile(const TileCore& p, const PrefillParams& e, int n, uint32_t tacc,
                               int row, const float* rope_tab) {
@@ -452,49 +256,6 @@ int make_prefill_plan(const dflash_dims& d, int tokens_per_seq, PrefillPlan* p) 
   return DFLASH_OK;
 }
 
-template <class Epi>
-int run_tile_gemm(TileCore& g, const TokenMaps& am, const WeightMaps& bm,
-                  const PrefillParams& ep, cudaStream_t st) {
-  g.stage_bytes = kATileBytes + g.bn * 128;
-  const int tail = 2 * 8 + kTileTailFixed;  // per-stage barriers counted below
-  g.n_stages = (kPrefillSmemBudget - 1024 - tail) / (g.stage_bytes + 16);
-  if (g.n_stages > 8) g.n_stages = 8;
-  const int smem = 1024 + g.n_stages * (g.stage_bytes + 16) + tail;
-  // once per process and instantiation (thread-safe static initialisation):
-  // the shared-memory limit (it covers any stage count) and how many clusters
-  // of two fit on the device at once (at most one CTA per SM)
-  static const int limit_rc = set_smem_limit(
-      reinterpret_cast<const void*>(tile_gemm_kernel<Epi>), kPrefillSmemBudget);
-  if (limit_rc) return limit_rc;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kTileThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  static const int max_clusters = [&cfg] {
-    const int nsm = current_num_sms();
-    if (nsm <= 0) return 0;
-    cudaLaunchConfig_t q = cfg;
-    q.gridDim = dim3(nsm & ~1);
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tile_gemm_kernel<Epi>, &q) != cudaSuccess) return 0;
-    return n;
-  }();
-  if (max_clusters < 1) return DFLASH_E_CUDA;
-  const int pairs = ((g.m_tiles + 1) / 2) * g.n_tiles;
-  const int clusters = pairs < max_clusters ? pairs : max_clusters;
-  cfg.gridDim = dim3(2 * clusters);
-  cfg.numAttrs = 2;
-  return cuda_err(cudaLaunchKernelEx(&cfg, tile_gemm_kernel<Epi>, am, bm, g, ep));
-}
 
 }  // namespace
 }  // namespace dflash

@@ -26,6 +26,7 @@
 
 #include "common.cuh"
 #include "host.h"
+#include "tile_gemm.cuh"
 
 namespace dflash {
 namespace {
@@ -368,6 +369,84 @@ lmhead_argmax_accept_kernel(const __grid_constant__ CUtensorMap tm_w,
   }
 }
 
+// ---------------------------------------------------------------------------
+// Large batches.  Past 256 token rows (batch 17 and up) the LM head is bound
+// by the tensor cores rather than by the W_lm stream (2 * 16B flops per weight
+// byte), and the token tile no longer fits beside a useful pipeline, so the
+// logits are produced by the tiled GEMM of tile_gemm.cuh (128 token rows x
+// 256 vocabulary rows per tile, clusters of two sharing each W_lm box) with an
+// argmax epilogue, and one thread per sequence then finishes the verification
+// (or the drafting) exactly as the skinny kernel's last CTA does.
+// ---------------------------------------------------------------------------
+constexpr int kWideMinRows = 257;
+
+struct ArgmaxEpi {
+  struct Params {
+    unsigned long long* keys;  // [ntok] argmax keys, zero between calls
+    int vocab, ntok;
+  };
+  static __device__ void setup(const Params&, float*, int) {}
+  static __device__ void prologue(const TileCore&, const Params&) {}
+  // thread = token row: the best key (order-preserving logit | ~vocabulary
+  // index, so the lowest index wins an exact tie) over the tile's rows of
+  // W_lm below the vocabulary size, merged into the row's key
+  static __device__ void tile(const TileCore& p, const Params& e, int n, uint32_t tacc, int row,
+                              const float*) {
+    const int n0 = n * p.bn;
+    unsigned long long best = 0ull;
+    for (int c0 = 0; c0 < p.bn; c0 += 16) {
+      uint32_t v[16];
+      tmem_ld_32x32b_x16(tacc + c0, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int f = n0 + c0 + j;
+        const unsigned long long k =
+            (static_cast<unsigned long long>(float_order_key(__uint_as_float(v[j]))) << 32) |
+            (0xFFFFFFFFu - static_cast<uint32_t>(f));
+        if (f < e.vocab && k > best) best = k;
+      }
+    }
+    if (row < e.ntok && best != 0ull) atomicMax(&e.keys[row], best);
+  }
+};
+
+// One thread per sequence: acceptance and commit (or the drafted block) from
+// the keys, which are then cleared for the next call.
+__global__ void lm_finish_kernel(const LmParams p) {
+  griddep_wait();
+  griddep_launch_dependents();
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= p.batch) return;
+  if (p.draft) write_draft(p, b); else accept_and_commit(p, b);
+  for (int i = 0; i < kBlock; ++i) p.keys[b * kBlock + i] = 0ull;
+}
+
+int launch_lmhead_wide(const dflash_dims& d, int budget_sms, const void* hidden,
+                       const void* w_lm, LmParams& p, cudaStream_t st) {
+  TileCore g = {};
+  g.status = p.status;
+  g.rows = p.ntok;
+  g.m_tiles = (p.ntok + kTileM - 1) / kTileM;
+  g.bn = 256;
+  g.n_tiles = (d.vocab + g.bn - 1) / g.bn;  // the last tile's rows past V read as zeros
+  g.k_tiles = d.hidden / 64;
+  g.layer_cols = d.hidden;
+  g.b_split = g.n_tiles;
+  const uint64_t pitch = static_cast<uint64_t>(d.hidden) * 2;
+  TokenMaps am;
+  WeightMaps bm;
+  int rc;
+  if ((rc = make_tmap_2d_bf16(&am.m[0], hidden, d.hidden, p.ntok, pitch, 64, kTileM))) return rc;
+  for (int l = 1; l < kMaxCtxLayers; ++l) am.m[l] = am.m[0];
+  if ((rc = make_tmap_2d_bf16(&bm.m[0], w_lm, d.hidden, d.vocab, pitch, 64, g.bn / 2)))
+    return rc;
+  bm.m[1] = bm.m[0];
+  ArgmaxEpi::Params ep = {p.keys, d.vocab, p.ntok};
+  if ((rc = run_tile_gemm<ArgmaxEpi>(g, am, bm, ep, st, budget_sms))) return rc;
+  return launch(lm_finish_kernel, dim3((p.batch + 127) / 128), dim3(128), 0, st, p);
+}
+
 }  // namespace
 
 // Pipeline shape, tensor maps and launch of the LM-head kernel for `p` (whose
@@ -378,6 +457,7 @@ int launch_lmhead(const dflash_dims& d, int budget_sms, const void* hidden, cons
   p.hidden = d.hidden;
   p.ntok = d.batch * kBlock;
   p.batch = d.batch;
+  if (p.ntok >= kWideMinRows) return launch_lmhead_wide(d, budget_sms, hidden, w_lm, p, st);
   p.ntok_box = p.ntok <= 256 ? p.ntok : 256;
   p.n_xbox = (p.ntok + p.ntok_box - 1) / p.ntok_box;
   p.n_units = (p.vocab + kUnitRows - 1) / kUnitRows;

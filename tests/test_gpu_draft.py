@@ -118,7 +118,7 @@ def test_draft_mlp_output_may_alias_input():
     assert_close_bf16(host_f64(xd), ref["x2"])
 
 
-@pytest.mark.parametrize("B,H,V", [(1, 256, 4096), (3, 512, 12345)])
+@pytest.mark.parametrize("B,H,V", [(1, 256, 4096), (3, 512, 12345), (32, 256, 9001)])
 def test_draft_tokens(B, H, V):
     dfl = _dfl()
     rng = np.random.default_rng(V)

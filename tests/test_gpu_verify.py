@@ -18,11 +18,11 @@ def _dfl():
 
 
 def gpu_verify(hidden_bits, w_bits, block_ids, len_before, out_cap, prev_out=None, calls=1,
-               alias_len=False):
+               alias_len=False, sm_budget=0):
     dfl = _dfl()
     B = block_ids.shape[0]
     V, H = w_bits.shape
-    dims = dfl.make_dims(B, H, 4, 4, 128, V, 1, 64)
+    dims = dfl.make_dims(B, H, 4, 4, 128, V, 1, 64, sm_budget=sm_budget)
     ws = dfl.alloc_workspace(dims)
     hid = dev_bf16(hidden_bits.reshape(B * 16, H))
     w = dev_bf16(w_bits)
@@ -82,8 +82,8 @@ def _run_and_check(hidden, w, blk, len_before, out_cap, calls=1, alias_len=False
     (1, 1, 256, 4096),          # tiny cycle shapes
     (2, 3, 256, 50005),         # several 128-row tiles per CTA + partial tile + ragged vocab
     (3, 4, 512, 33000),         # 64 token columns
-    (4, 17, 128, 9000),         # 272 columns: second MMA chunk of 16
-    (5, 32, 256, 20000),        # 512 columns, single accumulator
+    (4, 17, 128, 9000),         # 272 token rows: the tiled path, a third row tile of 16
+    (5, 32, 256, 20000),        # 512 token rows, ragged last vocabulary tile
     (6, 2, 128, 150),           # fewer vocabulary rows than SMs
 ])
 def test_verify_parity_small(seed, B, H, V):
@@ -126,6 +126,53 @@ def test_exact_tie_goes_to_the_lowest_index():
     for i in range(4):
         assert ref["posterior"][0][i] == 100 + 7 * i
         assert res[0]["posterior"][0][i] == 100 + 7 * i
+
+
+def test_tiled_path_exact_ties_go_to_the_lowest_index():
+    """Past 256 token rows the logits come from the tiled GEMM (256 vocabulary
+    rows per tile).  Copies of a row's winner in an earlier tile, in the same
+    tile and at the end of the vocabulary tie exactly; the lowest index wins."""
+    B, H, V = 17, 256, 70001
+    rng = np.random.default_rng(21)
+    hidden = unit_rms_rows_bf16(rng, (B, 16, H))
+    w = normal_bf16(rng, (V, H), 0.02)
+    zeros, lb = np.zeros((B, 16), np.int32), np.zeros(B, np.int32)
+    ref = ref_verify(hidden, w, zeros, lb, out_cap=32)
+    want = {}
+    for i in range(8):
+        p = int(ref["posterior"][0][i])
+        w[V - 1 - i] = w[p]                               # a later copy never wins
+        if i < 4:
+            lo = 100 + 7 * i                              # an earlier tile
+        else:
+            t0 = p // 256 * 256
+            if p == t0:
+                continue
+            lo = t0 + (p - t0) // 2                       # earlier in the same tile
+        w[lo] = w[p]
+        want[i] = lo
+    ref = ref_verify(hidden, w, zeros, lb, out_cap=32)
+    res, status = gpu_verify(hidden, w, zeros, lb, 32)
+    assert status == 0
+    for i, lo in want.items():
+        assert ref["posterior"][0][i] == lo
+        assert res[0]["posterior"][0][i] == lo
+    check_verify(ref, res[0], lb)
+
+
+@pytest.mark.parametrize("B,H,V,budget", [(24, 256, 30011, 40), (32, 128, 9000, 7)])
+def test_tiled_path_under_an_sm_budget(B, H, V, budget):
+    """The tiled path confined to a few SMs (clusters of two within the
+    budget) gives the same verification as on the whole device."""
+    hidden, w, blk, lb, cap = _case(30 + B, B, H, V)
+    full, st0 = gpu_verify(hidden, w, blk, lb, cap)
+    part, st1 = gpu_verify(hidden, w, blk, lb, cap, sm_budget=budget)
+    assert st0 == 0 and st1 == 0
+    for k in full[0]:
+        assert np.array_equal(full[0][k], part[0][k]), k
+    ref = ref_verify(hidden, w, blk, lb, out_cap=cap,
+                     out_tokens=np.full((B, cap), -7, np.int32))
+    check_verify(ref, part[0], lb)
 
 
 def test_overflow_and_bad_token_set_status_and_skip_commit():

@@ -26,7 +26,7 @@ def _outputs(B, cap):
             torch.full((B, cap), -3, dtype=torch.int32, device="cuda")]
 
 
-@pytest.mark.parametrize("B,H,V", [(1, 512, 30011), (4, 256, 20000)])
+@pytest.mark.parametrize("B,H,V", [(1, 512, 30011), (4, 256, 20000), (32, 256, 9001)])
 def test_noalloc_matches_workspace_entry_point_twice(B, H, V):
     import __graft_entry__
     __graft_entry__.build()
