@@ -33,6 +33,7 @@ struct PrefillParams {
   float rms_eps;
   const uint16_t* hidden_norm_w;  // [H] or null
   uint16_t* yhat;                 // [rows][H]: bf16(g_h * Y)
+  uint16_t* yhat_lo;              // [rows][H]: bf16(g_h * Y - yhat), or null (not kept)
   float* ss;                      // [fc_n_tiles][rows]: partial sums of Y^2
   const int32_t* write_pos;
   int32_t* pos_snapshot;          // [B]; -1: the sequence's rows are skipped
@@ -95,17 +96,25 @@ struct FcEpi {
         for (int j = 0; j < 16; ++j) g[j] = 1.f;
       }
       tmem_ld_wait();
-      uint32_t out[8];
+      uint32_t out[8], lo[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float y0 = __uint_as_float(v[2 * j]), y1 = __uint_as_float(v[2 * j + 1]);
         ss = fmaf(y0, y0, fmaf(y1, y1, ss));
-        out[j] = pack2_bf16(y0 * g[2 * j], y1 * g[2 * j + 1]);
+        const float a0 = y0 * g[2 * j], a1 = y1 * g[2 * j + 1];
+        out[j] = pack2_bf16(a0, a1);
+        lo[j] = pack2_bf16(a0 - __uint_as_float(out[j] << 16),
+                           a1 - __uint_as_float(out[j] & 0xFFFF0000u));
       }
       if (live) {
         uint4* d = reinterpret_cast<uint4*>(dst + c0);
         d[0] = make_uint4(out[0], out[1], out[2], out[3]);
         d[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        if (e.yhat_lo) {
+          uint4* dl = reinterpret_cast<uint4*>(e.yhat_lo + (dst - e.yhat) + c0);
+          dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        }
       }
     }
     if (live) e.ss[static_cast<size_t>(n) * p.rows + row] = ss;
@@ -260,6 +269,104 @@ int make_prefill_plan(const dflash_dims& d, int tokens_per_seq, PrefillPlan* p) 
 }  // namespace
 }  // namespace dflash
 
+namespace dflash {
+
+// The two tiled GEMMs of the projection for tokens_per_seq rows per sequence
+// (arguments checked by the caller; the scratch pointers are regions of the
+// caller's workspace).  Also used by dflash_ctx_project when its batch makes
+// the projection tensor-bound, with the lo half of g_h Y kept.
+int tiled_projection(const dflash_dims& d, int tokens_per_seq, const void* const* layer_hidden,
+                     const void* w_fc, const void* hidden_norm_w, const void* w_k,
+                     const void* w_v, const void* k_norm_w, const int32_t* write_pos,
+                     const dflash_kv_view& cache_view, uint32_t* status, int32_t* pos_snapshot,
+                     float* ss, uint16_t* yhat, uint16_t* yhat_lo, int max_ctas,
+                     cudaStream_t st) {
+  PrefillPlan plan;
+  int rc = make_prefill_plan(d, tokens_per_seq, &plan);
+  if (rc) return rc;
+  const dflash_dims* dims = &d;
+  const dflash_kv_view* cache = &cache_view;
+  const int nL = d.n_ctx_layers, H = d.hidden;
+  const int kvd = d.n_kv_heads * d.head_dim;
+  const uint64_t rows = static_cast<uint64_t>(plan.rows);
+  PrefillParams ep = {};
+  ep.hidden = H;
+  ep.fc_n_tiles = plan.fc_n_tiles;
+  ep.tokens_per_seq = tokens_per_seq;
+  ep.batch = dims->batch;
+  ep.rms_eps = dims->rms_eps;
+  ep.hidden_norm_w = static_cast<const uint16_t*>(hidden_norm_w);
+  ep.yhat = yhat;
+  ep.yhat_lo = yhat_lo;
+  ep.ss = ss;
+  ep.write_pos = write_pos;
+  ep.pos_snapshot = pos_snapshot;
+  ep.cache = *cache;
+  ep.n_kv_heads = dims->n_kv_heads;
+  ep.head_dim = dims->head_dim;
+  ep.k_norm_w = static_cast<const uint16_t*>(k_norm_w);
+  fill_rope_table(ep.rope.hi, ep.rope.lo, dims->head_dim, dims->rope_theta);
+
+  // ---- 1. fc GEMM: bf16(g_h * Y) and sums of Y^2 ----
+  {
+    TileCore g = {};
+    g.status = status;
+    g.rows = plan.rows;
+    g.m_tiles = (plan.rows + kTileM - 1) / kTileM;
+    g.bn = plan.fc_bn;
+    g.n_tiles = plan.fc_n_tiles;
+    g.k_tiles = nL * H / 64;
+    g.layer_cols = H;
+    g.b_split = g.n_tiles;
+    TokenMaps am;
+    for (int l = 0; l < nL; ++l)
+      if ((rc = make_tmap_2d_bf16(&am.m[l], layer_hidden[l], H, rows,
+                                  static_cast<uint64_t>(H) * 2, 64, kTileM)))
+        return rc;
+    for (int l = nL; l < kMaxCtxLayers; ++l) am.m[l] = am.m[0];
+    WeightMaps bm;
+    if ((rc = make_tmap_2d_bf16(&bm.m[0], w_fc, static_cast<uint64_t>(nL) * H, H,
+                                static_cast<uint64_t>(nL) * H * 2, 64, g.bn / 2)))
+      return rc;
+    bm.m[1] = bm.m[0];
+    if ((rc = run_tile_gemm<FcEpi>(g, am, bm, ep, st, max_ctas))) return rc;
+  }
+  // ---- 2. K/V GEMM: row factor, head norm + RoPE for K, cache stores ----
+  {
+    TileCore g = {};
+    g.status = status;
+    g.rows = plan.rows;
+    g.m_tiles = (plan.rows + kTileM - 1) / kTileM;
+    g.bn = plan.kv_bn;
+    g.n_tiles = 2 * kvd / g.bn;
+    // with the lo half kept, K runs twice over the weights: bf16(g_h Y) and
+    // then its rounding remainder, summed in the accumulator
+    g.k_tiles = (yhat_lo ? 2 : 1) * H / 64;
+    g.layer_cols = H;
+    g.b_split = kvd / g.bn;
+    g.b_cols = H;
+    TokenMaps am;
+    if ((rc = make_tmap_2d_bf16(&am.m[0], yhat, H, rows, static_cast<uint64_t>(H) * 2, 64,
+                                kTileM)))
+      return rc;
+    for (int l = 1; l < kMaxCtxLayers; ++l) am.m[l] = am.m[0];
+    if (yhat_lo && (rc = make_tmap_2d_bf16(&am.m[1], yhat_lo, H, rows,
+                                           static_cast<uint64_t>(H) * 2, 64, kTileM)))
+      return rc;
+    WeightMaps bm;
+    if ((rc = make_tmap_2d_bf16(&bm.m[0], w_k, H, kvd, static_cast<uint64_t>(H) * 2, 64,
+                                g.bn / 2)))
+      return rc;
+    if ((rc = make_tmap_2d_bf16(&bm.m[1], w_v, H, kvd, static_cast<uint64_t>(H) * 2, 64,
+                                g.bn / 2)))
+      return rc;
+    if ((rc = run_tile_gemm<KvEpi>(g, am, bm, ep, st, max_ctas))) return rc;
+  }
+  return DFLASH_OK;
+}
+
+}  // namespace dflash
+
 using namespace dflash;
 
 extern "C" size_t dflash_prefill_workspace_bytes(const dflash_dims* dims, int32_t tokens_per_seq) {
@@ -283,7 +390,7 @@ extern "C" int dflash_ctx_prefill(const dflash_dims* dims, int32_t tokens_per_se
   if (!layer_hidden || !w_fc || !w_k || !w_v || !write_pos || !cache || !cache->k ||
       !cache->v || !cache->seq_len)
     return DFLASH_E_ARG;
-  const int nL = dims->n_ctx_layers, H = dims->hidden;
+  const int nL = dims->n_ctx_layers;
   for (int l = 0; l < nL; ++l) {
     if (!layer_hidden[l]) return DFLASH_E_ARG;
     if (!aligned16(layer_hidden[l])) return DFLASH_E_ALIGN;
@@ -299,76 +406,9 @@ extern "C" int dflash_ctx_prefill(const dflash_dims* dims, int32_t tokens_per_se
   }
   if (!ws) return DFLASH_E_WORKSPACE;
   if (ws_bytes < plan.total) return DFLASH_E_WORKSPACE;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int kvd = dims->n_kv_heads * dims->head_dim;
-  const uint64_t rows = static_cast<uint64_t>(plan.rows);
-  uint16_t* yhat = ws_at<uint16_t>(ws, plan.off_yhat);
-
-  PrefillParams ep = {};
-  ep.hidden = H;
-  ep.fc_n_tiles = plan.fc_n_tiles;
-  ep.tokens_per_seq = tokens_per_seq;
-  ep.batch = dims->batch;
-  ep.rms_eps = dims->rms_eps;
-  ep.hidden_norm_w = static_cast<const uint16_t*>(hidden_norm_w);
-  ep.yhat = yhat;
-  ep.ss = ws_at<float>(ws, plan.off_ss);
-  ep.write_pos = write_pos;
-  ep.pos_snapshot = ws_at<int32_t>(ws, plan.off_pos);
-  ep.cache = *cache;
-  ep.n_kv_heads = dims->n_kv_heads;
-  ep.head_dim = dims->head_dim;
-  ep.k_norm_w = static_cast<const uint16_t*>(k_norm_w);
-  fill_rope_table(ep.rope.hi, ep.rope.lo, dims->head_dim, dims->rope_theta);
-
-  // ---- 1. fc GEMM: bf16(g_h * Y) and sums of Y^2 ----
-  {
-    TileCore g = {};
-    g.status = ws_at<uint32_t>(ws, plan.off_status);
-    g.rows = plan.rows;
-    g.m_tiles = (plan.rows + kTileM - 1) / kTileM;
-    g.bn = plan.fc_bn;
-    g.n_tiles = plan.fc_n_tiles;
-    g.k_tiles = nL * H / 64;
-    g.layer_cols = H;
-    g.b_split = g.n_tiles;
-    TokenMaps am;
-    for (int l = 0; l < nL; ++l)
-      if ((rc = make_tmap_2d_bf16(&am.m[l], layer_hidden[l], H, rows,
-                                  static_cast<uint64_t>(H) * 2, 64, kTileM)))
-        return rc;
-    for (int l = nL; l < kMaxCtxLayers; ++l) am.m[l] = am.m[0];
-    WeightMaps bm;
-    if ((rc = make_tmap_2d_bf16(&bm.m[0], w_fc, static_cast<uint64_t>(nL) * H, H,
-                                static_cast<uint64_t>(nL) * H * 2, 64, g.bn / 2)))
-      return rc;
-    bm.m[1] = bm.m[0];
-    if ((rc = run_tile_gemm<FcEpi>(g, am, bm, ep, st))) return rc;
-  }
-  // ---- 2. K/V GEMM: row factor, head norm + RoPE for K, cache stores ----
-  {
-    TileCore g = {};
-    g.status = ws_at<uint32_t>(ws, plan.off_status);
-    g.rows = plan.rows;
-    g.m_tiles = (plan.rows + kTileM - 1) / kTileM;
-    g.bn = plan.kv_bn;
-    g.n_tiles = 2 * kvd / g.bn;
-    g.k_tiles = H / 64;
-    g.layer_cols = H;
-    g.b_split = kvd / g.bn;
-    TokenMaps am;
-    if ((rc = make_tmap_2d_bf16(&am.m[0], yhat, H, rows, static_cast<uint64_t>(H) * 2, 64,
-                                kTileM)))
-      return rc;
-    for (int l = 1; l < kMaxCtxLayers; ++l) am.m[l] = am.m[0];
-    WeightMaps bm;
-    if ((rc = make_tmap_2d_bf16(&bm.m[0], w_k, H, kvd, static_cast<uint64_t>(H) * 2, 64,
-                                g.bn / 2)))
-      return rc;
-    if ((rc = make_tmap_2d_bf16(&bm.m[1], w_v, H, kvd, static_cast<uint64_t>(H) * 2, 64,
-                                g.bn / 2)))
-      return rc;
-    if ((rc = run_tile_gemm<KvEpi>(g, am, bm, ep, st))) return rc;
-  }
-  return DFLASH_OK;
+  return tiled_projection(*dims, tokens_per_seq, layer_hidden, w_fc, hidden_norm_w, w_k, w_v,
+                          k_norm_w, write_pos, *cache, ws_at<uint32_t>(ws, plan.off_status),
+                          ws_at<int32_t>(ws, plan.off_pos), ws_at<float>(ws, plan.off_ss),
+                          ws_at<uint16_t>(ws, plan.off_yhat), nullptr, 0,
+                          reinterpret_cast<cudaStream_t>(stream));
 }

@@ -61,6 +61,7 @@ __device__ void reserve_block_rows(const ProjParams& p, uint32_t* status, int b)
 }
 
 constexpr int kTokGroup = 4;  // token rows a warp finishes together (loads in flight)
+constexpr int kTiledProjectionRows = 257;  // from here on the tiled GEMMs project
 
 __device__ __forceinline__ uint2 pack4_bf16(float a, float b, float c, float d) {
   return make_uint2(static_cast<uint32_t>(float_to_bf16_bits(a)) |
@@ -305,6 +306,24 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
   fp.k_norm_w = static_cast<const uint16_t*>(k_norm_w);
   fill_rope_table(fp.rope.hi, fp.rope.lo, dims->head_dim, dims->rope_theta);
   uint32_t* tickets = ws_at<uint32_t>(ws, plan.off_ctx_tickets);
+
+  // Past 256 token rows (batch 17 and up) the projection is bound by the
+  // tensor cores, not by the weight stream.  Confined to part of the device
+  // (beside the verification) it runs on the tiled GEMMs of the prefill, 16
+  // rows per sequence, with g_h Y kept as the same hi/lo bf16 pair (the two
+  // halves in the hi and lo rows of this workspace region): at 512 rows and
+  // 23 SMs they take the verify || projection phase from 765 to 525 us.  With
+  // the whole device the streamed GEMMs stay faster (168 vs 209 us at 512
+  // rows: the fc GEMM's 32 tile pairs leave most clusters idle).  Shapes the
+  // tiles do not cover stay here too.
+  if (ntok >= kTiledProjectionRows && plan.budget_sms < plan.num_sms &&
+      aligned16(cache->k) && aligned16(cache->v) &&
+      (!hidden_norm_w || aligned16(hidden_norm_w))) {
+    rc = tiled_projection(*dims, kBlock, layer_hidden, w_fc, hidden_norm_w, w_k, w_v, k_norm_w,
+                          write_pos, *cache, status, pos_snap, fp.ss, yhat,
+                          yhat + static_cast<size_t>(ntok) * H, plan.budget_sms, st);
+    if (rc != DFLASH_E_UNSUPPORTED) return rc;
+  }
 
   // ---- 1. fc GEMM; its finisher writes hi/lo of g_h * Y and sums of Y^2 ----
   {

@@ -106,6 +106,21 @@ int make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t 
 // hi/lo pairs; filled in double precision on the host.
 void fill_rope_table(float* hi, float* lo, int head_dim, double theta);
 
+// The context projection as two tiled tensor-core GEMMs (ctx_prefill.cu), for
+// tokens_per_seq rows per sequence written at write_pos.  The scratch
+// pointers are regions of the caller's workspace: the status word, B
+// write-position snapshots, (H / 128) x rows floats, rows x H bf16 for
+// bf16(g_h Y) and, unless null, rows x H bf16 for its rounding remainder
+// (then the K/V GEMM reads g_h Y as that hi/lo pair, else rounded once).  At
+// most max_ctas CTAs (0: the whole device).  DFLASH_E_UNSUPPORTED, before
+// anything is launched, for shapes the tiles do not cover.
+int tiled_projection(const dflash_dims& d, int tokens_per_seq, const void* const* layer_hidden,
+                     const void* w_fc, const void* hidden_norm_w, const void* w_k,
+                     const void* w_v, const void* k_norm_w, const int32_t* write_pos,
+                     const dflash_kv_view& cache, uint32_t* status, int32_t* pos_snapshot,
+                     float* ss, uint16_t* yhat, uint16_t* yhat_lo, int max_ctas,
+                     cudaStream_t st);
+
 // Raise the dynamic shared-memory limit of a kernel once per device.
 int set_smem_limit(const void* func, int bytes);
 

@@ -44,6 +44,8 @@ struct TileCore {
   int bn;            // features per tile: 128 or 256
   int layer_cols;    // token map l holds columns [l * layer_cols, (l + 1) * layer_cols)
   int b_split;       // feature tiles below it read weight map 0, the others map 1
+  int b_cols;        // > 0: weight columns; k-tile kt reads weight column (64 kt) % b_cols
+                     // (the same weights against two token operands summed along K)
   int n_stages, stage_bytes;
   uint32_t* status;
 };
@@ -141,7 +143,8 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
           mbar_arrive_expect_tx(&full[stage], kTileABytes + p.bn * 128);
           const int l = (kt * 64) / p.layer_cols;
           tma_load_2d(a, &tm_a.m[l], &full[stage], kt * 64 - l * p.layer_cols, m * kTileM, pol);
-          tma_load_2d_mc(a + kTileABytes + crank * half_rows * 128, mb, &full[stage], kt * 64,
+          const int bcol = p.b_cols > 0 ? (kt * 64) % p.b_cols : kt * 64;
+          tma_load_2d_mc(a + kTileABytes + crank * half_rows * 128, mb, &full[stage], bcol,
                          brow, kPairMask, pol);
           ++issued;
           if (++stage == static_cast<uint32_t>(p.n_stages)) {

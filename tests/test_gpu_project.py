@@ -114,7 +114,7 @@ def test_project_tiny(norms):
 
 @pytest.mark.parametrize("B,H,nL,Hkv,D,pos", [
     (3, 512, 3, 2, 128, [0, 13, 100]),
-    (17, 256, 2, 2, 64, list(range(0, 17 * 5, 5))),    # 272 token rows: several chunks
+    (17, 256, 2, 2, 64, list(range(0, 17 * 5, 5))),    # 272 token rows: two token chunks
     (2, 1024, 5, 8, 128, [2048, 7]),
 ])
 def test_project_contiguous(B, H, nL, Hkv, D, pos):
@@ -124,7 +124,7 @@ def test_project_contiguous(B, H, nL, Hkv, D, pos):
 
 @pytest.mark.parametrize("sm_budget", [1, 3, 20])
 @pytest.mark.parametrize("B,H,nL,Hkv,D,pos", [
-    (17, 256, 2, 2, 64, list(range(0, 17 * 5, 5))),    # two 256-row token chunks
+    (17, 256, 2, 2, 64, list(range(0, 17 * 5, 5))),    # on part of the device: the tiled path
     (2, 1024, 5, 8, 128, [2048, 7]),
 ])
 def test_project_small_sm_budget(sm_budget, B, H, nL, Hkv, D, pos):
@@ -166,6 +166,41 @@ def test_project_paged_reserves_pages():
     fc = int(view.free_count.item())
     assert fc == lay.free_count - len(newly)
     assert set(view.free_list.cpu().numpy()[:fc].tolist()) == before_free - set(newly)
+
+
+@pytest.mark.parametrize("norms", [False, True])
+def test_project_tiled_path_paged_and_aliased(norms):
+    """Past 256 token rows (here 20 sequences) on part of the device the tiled
+    GEMMs project: a paged cache with blocks straddling pages, write positions
+    aliasing the lengths, both norm settings; rows and newly mapped pages as on
+    the streamed path."""
+    B, H, nL, Hkv, D = 20, 512, 3, 2, 128
+    rng = np.random.default_rng(31)
+    pos = [int(x) for x in rng.integers(0, 90, size=B)]
+    layers, w_fc, gh, wk, wv, gk = make_inputs(11, B, H, nL, Hkv, D)
+    if not norms:
+        gh = gk = None
+    view, lay, _, _ = check_project(layers, w_fc, gh, wk, wv, gk, pos, 4 * Hkv, Hkv, D,
+                                    paged=True, alias=True, sm_budget=40)
+    table = view.page_table.cpu().numpy()
+    for b, slots in enumerate(pages_needed(pos, 16, 16)):
+        assert all(table[b, s] >= 0 for s in slots)
+    mapped = table[table >= 0]
+    assert len(set(mapped.tolist())) == len(mapped)
+
+
+def test_project_tiled_path_flags_capacity():
+    """The tiled path, like the streamed one, leaves a sequence without room
+    for its 16 rows untouched and flags it."""
+    dfl = _dfl()
+    B = 18
+    layers, w_fc, gh, wk, wv, gk = make_inputs(12, B, 256, 2, 2, 64)
+    pos = [0] * (B - 1) + [30]
+    view, _, status = run_project(layers, w_fc, gh, wk, wv, gk, pos, 4, 2, 64, 1e6, capacity=40,
+                                  sm_budget=30)
+    assert status & dfl.dflash.STATUS_BITS["capacity"]
+    assert list(view.seq_len.cpu().numpy()) == [16] * (B - 1) + [0]
+    assert np.all(host_bits(view.k)[B - 1] == SENTINEL)
 
 
 def test_project_write_pos_aliases_seq_len():
