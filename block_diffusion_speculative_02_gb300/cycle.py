@@ -90,15 +90,21 @@ def _verify_and_project(dims_v: Dims, dims_p: Dims, w: CycleWeights, st: CycleSt
 
 
 def tune_sm_split(dims: Dims, w: CycleWeights, states: List[CycleState], ws: torch.Tensor,
-                  spread: int = 4, reps: int = 8, rounds: int = 2) -> Tuple[int, int]:
+                  spread: Optional[int] = None, reps: int = 8,
+                  rounds: int = 2) -> Tuple[int, int]:
     """Measure the verify || projection phase for SM splits around
     ``dflash_cycle_sm_split`` and return the fastest (verify_sms, project_sms).
 
     The proportional split is only a first guess: the two kernels' per-SM
-    bandwidth shares and tile boundaries move the optimum by a few SMs.  Runs
-    ``rounds * (2 * spread + 1) * reps`` phases on the given states (their
-    outputs are overwritten; lengths written by the projection are restored).
+    bandwidth shares and tile boundaries move the optimum by a few SMs (by
+    more past 256 token rows, where both sides are bound by the tensor cores
+    and run as tiled GEMMs: the default spread is then 8 SMs instead of 4).
+    Runs ``rounds * (2 * spread + 1) * reps`` phases on the given states
+    (their outputs are overwritten; lengths written by the projection are
+    restored).
     """
+    if spread is None:
+        spread = 8 if dims.batch * dims.block > 256 else 4
     v0, p0 = dflash_cycle_sm_split(dims)
     nsm = v0 + p0
     main = torch.cuda.current_stream()

@@ -136,10 +136,12 @@ DFLASH_API size_t dflash_workspace_bytes(const dflash_dims* dims);
 DFLASH_API int dflash_workspace_init(void* ws, size_t ws_bytes, dflash_stream_t stream);
 
 /* Budgets (dflash_dims::sm_budget) for running dflash_verify_accept and
- * dflash_ctx_project side by side on two streams.  Both are bound by the
- * weights they stream (W_lm; W_fc, W_k, W_v), so the device's SMs are split
- * in proportion to those bytes, each side getting at least one SM.  Writes
- * the two budgets (summing to the SM count of the current device). */
+ * dflash_ctx_project side by side on two streams.  At small batch both are
+ * bound by the weights they stream (W_lm; W_fc, W_k, W_v), so the device's
+ * SMs are split in proportion to those bytes, each side getting at least one
+ * SM (past 256 token rows both are bound by the tensor cores instead and the
+ * split is only a starting point for measuring).  Writes the two budgets
+ * (summing to the SM count of the current device). */
 DFLASH_API int dflash_cycle_sm_split(const dflash_dims* dims, int32_t* verify_sms,
                                      int32_t* project_sms);
 
