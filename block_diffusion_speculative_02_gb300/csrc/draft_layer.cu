@@ -21,6 +21,7 @@
 // The gate and up tiles of the same features are finished together (paired
 // tickets), so silu(g) * u never leaves the SM in fp32.
 #include "streamk_gemm.cuh"
+#include "tile_gemm.cuh"
 
 namespace dflash {
 namespace {
@@ -292,6 +293,85 @@ struct DownFin {
   }
 };
 
+// Past 256 token rows (batch 17 and up) the MLP's two GEMMs are bound by the
+// tensor cores: they run on the clustered tile GEMM of tile_gemm.cuh with the
+// same operands (hi/lo pairs summed along a doubled K) and these epilogues,
+// thread = token row.
+constexpr int kTiledDraftRows = 257;
+
+// Gate and up: CTA c of a pair loads the rows of the same 128 features from
+// W_gate (c = 0) or W_up (c = 1), so accumulator columns [0, 128) are the
+// gate and [128, 256) the up products of features 128 n ...: the RMSNorm
+// factor of x1, silu(gate) * up, hi/lo for the down projection.
+struct GateUpTileEpi {
+  using Params = DraftParams;
+  static __device__ void setup(const Params&, float*, int) {}
+  static __device__ void prologue(const TileCore&, const Params&) {}
+  static __device__ void tile(const TileCore& p, const Params& e, int n, uint32_t tacc, int row,
+                              const float*) {
+    const int n_ss = e.hidden / 128, f0 = n * 128;
+    const bool live = row < p.rows;
+    float tot = 0.f;
+    if (live) {
+#pragma unroll 8
+      for (int q = 0; q < n_ss; ++q) tot += __ldcg(e.ss_x1 + static_cast<size_t>(q) * p.rows + row);
+    }
+    const float r = rsqrtf(tot / e.hidden + e.rms_eps);
+    for (int c0 = 0; c0 < 128; c0 += 16) {
+      uint32_t gv[16], uv[16];
+      tmem_ld_32x32b_x16(tacc + c0, gv);
+      tmem_ld_32x32b_x16(tacc + 128 + c0, uv);
+      tmem_ld_wait();
+      if (!live) continue;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float m[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          m[j] = silu(__uint_as_float(gv[4 * q4 + j]) * r) * (__uint_as_float(uv[4 * q4 + j]) * r);
+        store_hilo4(e.mhl, p.rows, e.ffn, row, f0 + c0 + 4 * q4, m);
+      }
+    }
+  }
+};
+
+// Down: x2 = x1 + M W_down^T, bf16.
+struct DownTileEpi {
+  using Params = DraftParams;
+  static __device__ void setup(const Params&, float*, int) {}
+  static __device__ void prologue(const TileCore&, const Params&) {}
+  static __device__ void tile(const TileCore& p, const Params& e, int n, uint32_t tacc, int row,
+                              const float*) {
+    const int H = e.hidden, f0 = n * p.bn;
+    const bool live = row < p.rows;
+    for (int c0 = 0; c0 < p.bn; c0 += 16) {
+      uint32_t v[16];
+      tmem_ld_32x32b_x16(tacc + c0, v);
+      tmem_ld_wait();
+      if (!live) continue;
+      const size_t off = static_cast<size_t>(row) * H + f0 + c0;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(e.x1 + off) + q4);
+        *reinterpret_cast<uint2*>(e.x_out + off + 4 * q4) =
+            pack4(x.x + __uint_as_float(v[4 * q4]), x.y + __uint_as_float(v[4 * q4 + 1]),
+                  x.z + __uint_as_float(v[4 * q4 + 2]), x.w + __uint_as_float(v[4 * q4 + 3]));
+      }
+    }
+  }
+};
+
+// The token operand of a tiled GEMM: the hi rows (map 0) and lo rows (map 1)
+// of a [2, rows, cols] pair.
+int hilo_token_maps(TokenMaps& am, const uint16_t* hl, int rows, int cols) {
+  const uint64_t pitch = static_cast<uint64_t>(cols) * 2;
+  int rc = make_tmap_2d_bf16(&am.m[0], hl, cols, rows, pitch, 64, kTileM);
+  if (!rc) rc = make_tmap_2d_bf16(&am.m[1], hl + static_cast<size_t>(rows) * cols, cols, rows,
+                                  pitch, 64, kTileM);
+  for (int l = 2; l < kMaxCtxLayers; ++l) am.m[l] = am.m[0];
+  return rc;
+}
+
 // Fill the common GEMM fields for n_tok token rows of a K-column operand.
 void gemm_shape(GemmCore& g, const DraftPlan& plan, int k_cols, int out_tiles, int hilo,
                 uint32_t* tickets, float* acc, void* ws) {
@@ -483,6 +563,47 @@ extern "C" int dflash_draft_mlp(const dflash_dims* dims, int32_t ffn, const void
     if ((rc = token_map(bm, attn_out, qd, plan.ntok, g.chunk_rows))) return rc;
     if ((rc = sk::run_streamk<OprojFin>(g, g.chunk_rows, am, bm, fp, plan.budget_sms, st)))
       return rc;
+  }
+  if (plan.ntok >= kTiledDraftRows) {
+    // 2. gate | up of the same features in one tile; silu(g) * u as hi/lo
+    TileCore g = {};
+    g.status = ws_at<uint32_t>(ws, plan.off_status);
+    g.rows = plan.ntok;
+    g.m_tiles = (plan.ntok + kTileM - 1) / kTileM;
+    g.bn = 256;
+    g.n_tiles = ffn / 128;
+    g.k_tiles = 2 * H / 64;
+    g.layer_cols = H;
+    g.b_split = g.n_tiles;
+    g.b_cols = H;
+    g.b_paired = 1;
+    TokenMaps am;
+    WeightMaps bm;
+    if ((rc = hilo_token_maps(am, fp.xhl, plan.ntok, H))) return rc;
+    if ((rc = make_tmap_2d_bf16(&bm.m[0], w_gate, H, ffn, static_cast<uint64_t>(H) * 2, 64,
+                                128)) ||
+        (rc = make_tmap_2d_bf16(&bm.m[1], w_up, H, ffn, static_cast<uint64_t>(H) * 2, 64, 128)))
+      return rc;
+    if ((rc = run_tile_gemm<GateUpTileEpi>(g, am, bm, fp, st, plan.budget_sms))) return rc;
+    // 3. x2 = x1 + M W_down^T
+    TileCore d = {};
+    d.status = g.status;
+    d.rows = plan.ntok;
+    d.m_tiles = g.m_tiles;
+    d.bn = H % 256 == 0 ? 256 : 128;
+    d.n_tiles = H / d.bn;
+    d.k_tiles = 2 * ffn / 64;
+    d.layer_cols = ffn;
+    d.b_split = d.n_tiles;
+    d.b_cols = ffn;
+    TokenMaps dm;
+    WeightMaps wm;
+    if ((rc = hilo_token_maps(dm, fp.mhl, plan.ntok, ffn))) return rc;
+    if ((rc = make_tmap_2d_bf16(&wm.m[0], w_down, ffn, H, static_cast<uint64_t>(ffn) * 2, 64,
+                                d.bn / 2)))
+      return rc;
+    wm.m[1] = wm.m[0];
+    return run_tile_gemm<DownTileEpi>(d, dm, wm, fp, st, plan.budget_sms);
   }
   // 2. [gate; up] on hi/lo of x1 * ln2; paired finishing: silu(g) * u as hi/lo
   {

@@ -46,6 +46,9 @@ struct TileCore {
   int b_split;       // feature tiles below it read weight map 0, the others map 1
   int b_cols;        // > 0: weight columns; k-tile kt reads weight column (64 kt) % b_cols
                      // (the same weights against two token operands summed along K)
+  int b_paired;      // 1: CTA c of the pair loads its half of feature tile n from weight
+                     // map c, rows n * BN/2 ..: accumulator columns [0, BN/2) are map 0's
+                     // features, [BN/2, BN) map 1's same features (b_split unused)
   int n_stages, stage_bytes;
   uint32_t* status;
 };
@@ -131,9 +134,10 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
         int mp, n;
         tile_coords(mp_tiles, p.n_tiles, t, &mp, &n);
         const int m = 2 * mp + crank;
-        const bool second = n >= p.b_split;
+        const bool second = p.b_paired ? crank == 1 : n >= p.b_split;
         const CUtensorMap* mb = second ? &tm_b.m[1] : &tm_b.m[0];
-        const int brow = (second ? n - p.b_split : n) * p.bn + crank * half_rows;
+        const int brow = p.b_paired ? n * half_rows
+                                    : (second ? n - p.b_split : n) * p.bn + crank * half_rows;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
             ok = false;

@@ -76,8 +76,9 @@ def test_draft_qkv(B, H, Hq, Hkv, D, norms):
 @pytest.mark.parametrize("B,H,Hq,D,F", [
     (1, 256, 4, 64, 512),
     (2, 384, 4, 128, 640),
-    (17, 256, 4, 64, 384),           # 272 token rows: several chunks
+    (17, 256, 4, 64, 384),           # 272 token rows: the tiled gate/up and down GEMMs
     (32, 256, 4, 64, 384),           # the largest batch (512 token rows)
+    (20, 384, 4, 128, 640),          # tiled, hidden not a multiple of 256 (128-wide down tiles)
 ])
 def test_draft_mlp(B, H, Hq, D, F):
     dfl = _dfl()
