@@ -328,7 +328,7 @@ int tiled_projection(const dflash_dims& d, int tokens_per_seq, const void* const
     if ((rc = make_tmap_2d_bf16(&bm.m[0], w_fc, static_cast<uint64_t>(nL) * H, H,
                                 static_cast<uint64_t>(nL) * H * 2, 64, g.bn / 2)))
       return rc;
-    bm.m[1] = bm.m[0];
+    bm.m[1] = bm.m[2] = bm.m[0];
     if ((rc = run_tile_gemm<FcEpi>(g, am, bm, ep, st, max_ctas))) return rc;
   }
   // ---- 2. K/V GEMM: row factor, head norm + RoPE for K, cache stores ----
@@ -360,6 +360,7 @@ int tiled_projection(const dflash_dims& d, int tokens_per_seq, const void* const
     if ((rc = make_tmap_2d_bf16(&bm.m[1], w_v, H, kvd, static_cast<uint64_t>(H) * 2, 64,
                                 g.bn / 2)))
       return rc;
+    bm.m[2] = bm.m[1];
     if ((rc = run_tile_gemm<KvEpi>(g, am, bm, ep, st, max_ctas))) return rc;
   }
   return DFLASH_OK;

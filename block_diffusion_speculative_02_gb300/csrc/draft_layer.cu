@@ -299,6 +299,96 @@ struct DownFin {
 // thread = token row.
 constexpr int kTiledDraftRows = 257;
 
+// q/k/v: one tile of BN features of q, k or v (weight maps 0, 1, 2): the
+// row's 1/rms(x), per-head RMSNorm of q and k (a first pass over the head's
+// columns for the sum of squares), bf16 store.
+struct QkvTileEpi {
+  using Params = DraftParams;
+  static __device__ void setup(const Params&, float*, int) {}
+  static __device__ void prologue(const TileCore&, const Params&) {}
+  static __device__ void tile(const TileCore& p, const Params& e, int n, uint32_t tacc, int row,
+                              const float*) {
+    const int D = e.head_dim;
+    const int region = n < p.b_split ? 0 : (n < p.b_split2 ? 1 : 2);  // q, k, v
+    const int f0 = (n - (region == 0 ? 0 : (region == 1 ? p.b_split : p.b_split2))) * p.bn;
+    const int width = (region == 0 ? e.n_q_heads : e.n_kv_heads) * D;
+    uint16_t* out = region == 0 ? e.q_out : (region == 1 ? e.k_out : e.v_out);
+    const uint16_t* nw = region == 0 ? e.q_norm_w : (region == 1 ? e.k_norm_w : nullptr);
+    const bool live = row < p.rows;
+    const float r = live ? rsqrtf(__ldcg(e.ss_rows + row) / e.hidden + e.rms_eps) : 0.f;
+    for (int h0 = 0; h0 < p.bn; h0 += D) {
+      float rs = 1.f;
+      if (nw) {
+        float sq = 0.f;
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tacc + h0 + c0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float x = __uint_as_float(v[j]) * r;
+            sq = fmaf(x, x, sq);
+          }
+        }
+        rs = rsqrtf(sq / D + e.rms_eps);
+      }
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tacc + h0 + c0, v);
+        tmem_ld_wait();
+        if (!live) continue;
+        const float s = r * rs;
+        uint16_t* dst = out + static_cast<size_t>(row) * width + f0 + h0 + c0;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 gn = nw ? ld4_bf16(nw + c0 + 4 * q4) : make_float4(1.f, 1.f, 1.f, 1.f);
+          *reinterpret_cast<uint2*>(dst + 4 * q4) =
+              pack4(__uint_as_float(v[4 * q4]) * s * gn.x, __uint_as_float(v[4 * q4 + 1]) * s * gn.y,
+                    __uint_as_float(v[4 * q4 + 2]) * s * gn.z,
+                    __uint_as_float(v[4 * q4 + 3]) * s * gn.w);
+        }
+      }
+    }
+  }
+};
+
+// Output projection: x1 = x + O W_o^T (fp32), hi/lo of x1 * ln2 and, per 128
+// features, the partial sums of x1^2 (the layout of the streamed path).
+struct OprojTileEpi {
+  using Params = DraftParams;
+  static __device__ void setup(const Params&, float*, int) {}
+  static __device__ void prologue(const TileCore&, const Params&) {}
+  static __device__ void tile(const TileCore& p, const Params& e, int n, uint32_t tacc, int row,
+                              const float*) {
+    const int H = e.hidden, f0 = n * p.bn;
+    const bool live = row < p.rows;
+    for (int half = 0; half < p.bn; half += 128) {
+      float sq = 0.f;
+      for (int c0 = half; c0 < half + 128; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tacc + c0, v);
+        tmem_ld_wait();
+        if (!live) continue;
+        const size_t off = static_cast<size_t>(row) * H + f0 + c0;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 xin = ld4_bf16(e.x + off + 4 * q4);
+          const float4 gn = ld4_bf16(e.ln2_w + f0 + c0 + 4 * q4);
+          const float4 y = make_float4(xin.x + __uint_as_float(v[4 * q4]),
+                                       xin.y + __uint_as_float(v[4 * q4 + 1]),
+                                       xin.z + __uint_as_float(v[4 * q4 + 2]),
+                                       xin.w + __uint_as_float(v[4 * q4 + 3]));
+          *reinterpret_cast<float4*>(e.x1 + off + 4 * q4) = y;
+          sq += y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w;
+          const float z[4] = {y.x * gn.x, y.y * gn.y, y.z * gn.z, y.w * gn.w};
+          store_hilo4(e.xhl, p.rows, H, row, f0 + c0 + 4 * q4, z);
+        }
+      }
+      if (live) e.ss_x1[static_cast<size_t>((f0 + half) / 128) * p.rows + row] = sq;
+    }
+  }
+};
+
 // Gate and up: CTA c of a pair loads the rows of the same 128 features from
 // W_gate (c = 0) or W_up (c = 1), so accumulator columns [0, 128) are the
 // gate and [128, 256) the up products of features 128 n ...: the RMSNorm
@@ -504,6 +594,30 @@ extern "C" int dflash_draft_qkv(const dflash_dims* dims, const void* x, const vo
   fp.k_out = static_cast<uint16_t*>(k_out);
   fp.v_out = static_cast<uint16_t*>(v_out);
 
+  const int tbn = (qd % 256 == 0 && kvd % 256 == 0) ? 256 : 128;
+  if (plan.ntok >= kTiledDraftRows && qd % tbn == 0 && kvd % tbn == 0) {
+    TileCore t = {};
+    t.status = ws_at<uint32_t>(ws, plan.off_status);
+    t.rows = plan.ntok;
+    t.m_tiles = (plan.ntok + kTileM - 1) / kTileM;
+    t.bn = tbn;
+    t.n_tiles = (qd + 2 * kvd) / tbn;
+    t.k_tiles = 2 * H / 64;
+    t.layer_cols = H;
+    t.b_split = qd / tbn;
+    t.b_split2 = (qd + kvd) / tbn;
+    t.b_cols = H;
+    TokenMaps am;
+    WeightMaps bm;
+    if ((rc = hilo_token_maps(am, xhl, plan.ntok, H))) return rc;
+    const uint64_t pitch = static_cast<uint64_t>(H) * 2;
+    if ((rc = make_tmap_2d_bf16(&bm.m[0], w_q, H, qd, pitch, 64, tbn / 2)) ||
+        (rc = make_tmap_2d_bf16(&bm.m[1], w_k, H, kvd, pitch, 64, tbn / 2)) ||
+        (rc = make_tmap_2d_bf16(&bm.m[2], w_v, H, kvd, pitch, 64, tbn / 2)))
+      return rc;
+    return run_tile_gemm<QkvTileEpi>(t, am, bm, fp, st, plan.budget_sms);
+  }
+
   GemmCore g = {};
   gemm_shape(g, plan, H, plan.qkv_tiles, 1, ws_at<uint32_t>(ws, plan.off_tickets_qkv),
              ws_at<float>(ws, plan.off_acc_a), ws);
@@ -551,7 +665,28 @@ extern "C" int dflash_draft_mlp(const dflash_dims* dims, int32_t ffn, const void
   fp.x_out = static_cast<uint16_t*>(x_out);
 
   // 1. x1 = x + O W_o^T; hi/lo of x1 * ln2; sums of x1^2
-  {
+  if (plan.ntok >= kTiledDraftRows) {
+    TileCore t = {};
+    t.status = ws_at<uint32_t>(ws, plan.off_status);
+    t.rows = plan.ntok;
+    t.m_tiles = (plan.ntok + kTileM - 1) / kTileM;
+    t.bn = H % 256 == 0 ? 256 : 128;
+    t.n_tiles = H / t.bn;
+    t.k_tiles = qd / 64;
+    t.layer_cols = qd;
+    t.b_split = t.n_tiles;
+    TokenMaps am;
+    WeightMaps bm;
+    if ((rc = make_tmap_2d_bf16(&am.m[0], attn_out, qd, plan.ntok,
+                                static_cast<uint64_t>(qd) * 2, 64, kTileM)))
+      return rc;
+    for (int l = 1; l < kMaxCtxLayers; ++l) am.m[l] = am.m[0];
+    if ((rc = make_tmap_2d_bf16(&bm.m[0], w_o, qd, H, static_cast<uint64_t>(qd) * 2, 64,
+                                t.bn / 2)))
+      return rc;
+    bm.m[1] = bm.m[2] = bm.m[0];
+    if ((rc = run_tile_gemm<OprojTileEpi>(t, am, bm, fp, st, plan.budget_sms))) return rc;
+  } else {
     GemmCore g = {};
     gemm_shape(g, plan, qd, plan.o_tiles, 0, ws_at<uint32_t>(ws, plan.off_tickets_o),
                ws_at<float>(ws, plan.off_acc_a), ws);
@@ -584,6 +719,7 @@ extern "C" int dflash_draft_mlp(const dflash_dims* dims, int32_t ffn, const void
                                 128)) ||
         (rc = make_tmap_2d_bf16(&bm.m[1], w_up, H, ffn, static_cast<uint64_t>(H) * 2, 64, 128)))
       return rc;
+    bm.m[2] = bm.m[1];
     if ((rc = run_tile_gemm<GateUpTileEpi>(g, am, bm, fp, st, plan.budget_sms))) return rc;
     // 3. x2 = x1 + M W_down^T
     TileCore d = {};
@@ -602,7 +738,7 @@ extern "C" int dflash_draft_mlp(const dflash_dims* dims, int32_t ffn, const void
     if ((rc = make_tmap_2d_bf16(&wm.m[0], w_down, ffn, H, static_cast<uint64_t>(ffn) * 2, 64,
                                 d.bn / 2)))
       return rc;
-    wm.m[1] = wm.m[0];
+    wm.m[1] = wm.m[2] = wm.m[0];
     return run_tile_gemm<DownTileEpi>(d, dm, wm, fp, st, plan.budget_sms);
   }
   // 2. [gate; up] on hi/lo of x1 * ln2; paired finishing: silu(g) * u as hi/lo

@@ -44,6 +44,7 @@ struct TileCore {
   int bn;            // features per tile: 128 or 256
   int layer_cols;    // token map l holds columns [l * layer_cols, (l + 1) * layer_cols)
   int b_split;       // feature tiles below it read weight map 0, the others map 1
+  int b_split2;      // > 0: feature tiles from it on read weight map 2
   int b_cols;        // > 0: weight columns; k-tile kt reads weight column (64 kt) % b_cols
                      // (the same weights against two token operands summed along K)
   int b_paired;      // 1: CTA c of the pair loads its half of feature tile n from weight
@@ -58,7 +59,7 @@ struct TokenMaps {
 };
 
 struct WeightMaps {
-  CUtensorMap m[2];
+  CUtensorMap m[3];
 };
 
 // Pair tile t of the raster (row-tile pair mp = rows 256 mp .. 256 mp + 255,
@@ -134,10 +135,11 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
         int mp, n;
         tile_coords(mp_tiles, p.n_tiles, t, &mp, &n);
         const int m = 2 * mp + crank;
-        const bool second = p.b_paired ? crank == 1 : n >= p.b_split;
-        const CUtensorMap* mb = second ? &tm_b.m[1] : &tm_b.m[0];
-        const int brow = p.b_paired ? n * half_rows
-                                    : (second ? n - p.b_split : n) * p.bn + crank * half_rows;
+        const bool third = !p.b_paired && p.b_split2 > 0 && n >= p.b_split2;
+        const bool second = p.b_paired ? crank == 1 : (!third && n >= p.b_split);
+        const CUtensorMap* mb = third ? &tm_b.m[2] : (second ? &tm_b.m[1] : &tm_b.m[0]);
+        const int n_local = third ? n - p.b_split2 : (second && !p.b_paired ? n - p.b_split : n);
+        const int brow = p.b_paired ? n * half_rows : n_local * p.bn + crank * half_rows;
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
             ok = false;

@@ -441,7 +441,7 @@ int launch_lmhead_wide(const dflash_dims& d, int budget_sms, const void* hidden,
   for (int l = 1; l < kMaxCtxLayers; ++l) am.m[l] = am.m[0];
   if ((rc = make_tmap_2d_bf16(&bm.m[0], w_lm, d.hidden, d.vocab, pitch, 64, g.bn / 2)))
     return rc;
-  bm.m[1] = bm.m[0];
+  bm.m[1] = bm.m[2] = bm.m[0];
   ArgmaxEpi::Params ep = {p.keys, d.vocab, p.ntok};
   if ((rc = run_tile_gemm<ArgmaxEpi>(g, am, bm, ep, st, budget_sms))) return rc;
   return launch(lm_finish_kernel, dim3((p.batch + 127) / 128), dim3(128), 0, st, p);

@@ -56,6 +56,8 @@ def run_qkv(dfl, dims, x, w, Hq, Hkv, D, ws):
     (2, 256, 4, 2, 64, False),
     (17, 512, 8, 2, 128, True),      # 272 token rows: three 128-row chunks
     (32, 256, 4, 2, 64, True),       # the largest batch (512 token rows)
+    (20, 512, 8, 2, 128, True),      # tiled: 256-feature tiles of q and k|v
+    (24, 512, 8, 2, 128, False),
 ])
 def test_draft_qkv(B, H, Hq, Hkv, D, norms):
     dfl = _dfl()
