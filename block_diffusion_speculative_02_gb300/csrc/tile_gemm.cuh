@@ -232,6 +232,11 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
   griddep_launch_dependents();
 }
 
+// Pipeline shape and launch: as many stages as the shared-memory budget
+// holds, one cluster of two per pair of SMs that can hold it, at most one per
+// pair tile, and at most max_ctas / 2 clusters when max_ctas >= 2 (below that
+// the whole device: a cluster needs two SMs).  The clusters stride over the
+// pair tiles, so any cluster count covers the work.
 template <class Epi>
 int run_tile_gemm(TileCore& g, const TokenMaps& am, const WeightMaps& bm,
                   const typename Epi::Params& ep, cudaStream_t st, int max_ctas = 0) {
