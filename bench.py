@@ -300,6 +300,28 @@ def build_workload(cfg, n_sets: int, device="cuda"):
     return dims, w, states, accepts, ws, lens
 
 
+def lm_head_roofline(cfg, lm_bytes: int, lm_ms: float, hbm_peak, tensor_peak, traffic) -> dict:
+    """The `roofline` entry for the LM-head launch: bound by the larger of its
+    weight-stream time (bytes / HBM peak) and its tensor time (2 B 16 H V
+    flops / bf16 peak) -- HBM at small batch, the tensor cores at batch 32 --
+    with both fractions reported.  Peaks are (value, kind) pairs in GB/s and
+    TFLOP/s; lm_ms is the mean launch duration in milliseconds."""
+    peak, peak_kind = hbm_peak
+    tpk, tpk_kind = tensor_peak
+    lm_flops = 2.0 * cfg.batch * 16 * cfg.hidden * cfg.vocab
+    lm_gbs = lm_bytes / (lm_ms / 1e3) / 1e9
+    lm_tflops = lm_flops / (lm_ms / 1e3) / 1e12
+    tensor_bound = lm_flops / (tpk * 1e12) > lm_bytes / (peak * 1e9)
+    return {"bound": "tensor" if tensor_bound else "hbm", "kernel": "lmhead_argmax_accept",
+            "achieved": lm_tflops if tensor_bound else lm_gbs,
+            "peak": tpk if tensor_bound else peak,
+            "peak_kind": tpk_kind if tensor_bound else peak_kind,
+            "unit": "TFLOP/s" if tensor_bound else "GB/s",
+            "frac": lm_tflops / tpk if tensor_bound else lm_gbs / peak,
+            "traffic": traffic, "bytes_per_launch": lm_bytes, "flops_per_launch": lm_flops,
+            "avg_launch_ms": lm_ms, "hbm_frac": lm_gbs / peak, "tensor_frac": lm_tflops / tpk}
+
+
 def algorithmic_bytes(cfg, lens) -> dict:
     """Bytes one cycle must move at least: every weight once, the context KV of
     one drafter layer once, activations once."""
@@ -573,7 +595,6 @@ def main(argv=None):
                               for i in range(args.steps)]))
     bytes_ = algorithmic_bytes(cfg, lens)
     peak, peak_kind = measured_peak_gbs()
-    lm_gbs = bytes_["lm_head"] / (lm_ms / 1e3) / 1e9
     cycle_gbs = bytes_["total"] * args.steps / elapsed_s / 1e9
     # the committed DRAM capture is of the Qwen3-8B batch-1 launch only
     traffic = profiled_traffic(os.path.join(ROOT, "block_diffusion_speculative_02_gb300", "csrc",
@@ -581,23 +602,8 @@ def main(argv=None):
                                "lmhead_argmax_accept_qwen3_8b_b1.md") \
         if cfg.name == "qwen3_8b_b1" else None
 
-    # the LM head's bound is the larger of its weight-stream time and its
-    # tensor time (2 B 16 H V flops): HBM at small batch, the tensor cores at
-    # batch 32; both fractions are reported
-    lm_flops = 2.0 * cfg.batch * 16 * cfg.hidden * cfg.vocab
-    tpk, tpk_kind = measured_peak_tflops()
-    lm_tflops = lm_flops / (lm_ms / 1e3) / 1e12
-    tensor_bound = lm_flops / (tpk * 1e12) > bytes_["lm_head"] / (peak * 1e9)
-    lm_roofline = {"bound": "tensor" if tensor_bound else "hbm",
-                   "kernel": "lmhead_argmax_accept",
-                   "achieved": lm_tflops if tensor_bound else lm_gbs,
-                   "peak": tpk if tensor_bound else peak,
-                   "peak_kind": tpk_kind if tensor_bound else peak_kind,
-                   "unit": "TFLOP/s" if tensor_bound else "GB/s",
-                   "frac": lm_tflops / tpk if tensor_bound else lm_gbs / peak,
-                   "traffic": traffic, "bytes_per_launch": bytes_["lm_head"],
-                   "flops_per_launch": lm_flops, "avg_launch_ms": lm_ms,
-                   "hbm_frac": lm_gbs / peak, "tensor_frac": lm_tflops / tpk}
+    lm_roofline = lm_head_roofline(cfg, bytes_["lm_head"], lm_ms, (peak, peak_kind),
+                                   measured_peak_tflops(), traffic)
 
     # ---- the same cycles replayed from CUDA graphs (one per input set) ----
     graph_cycle = None

@@ -64,3 +64,23 @@ def test_reference_arm_under_two_ranks_prints_only_on_rank_zero():
                         "--steps", "1", "--warmup", "0", "--config", "tiny_b1"],
                        capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_lm_head_roofline_picks_the_binding_resource():
+    """The LM head is reported against the HBM peak when its bytes take longer
+    than its flops (batch 1: 1.2 GB for 20 GFLOP) and against the bf16 tensor
+    peak otherwise (batch 32: 637 GFLOP); both fractions are always given."""
+    import bench
+    from synthetic import CONFIG_BY_NAME
+    hbm, tc = (6782.8, "measured"), (1915.7, "measured")
+    b1 = bench.lm_head_roofline(CONFIG_BY_NAME["qwen3_8b_b1"], 1_244_791_040, 0.2, hbm, tc, 7)
+    assert b1["bound"] == "hbm" and b1["unit"] == "GB/s" and b1["traffic"] == 7
+    assert abs(b1["achieved"] - 1_244_791_040 / 0.2e-3 / 1e9) < 1e-9 * b1["achieved"]
+    assert b1["frac"] == b1["hbm_frac"] and b1["peak"] == 6782.8
+    flops = 2.0 * 32 * 16 * 4096 * 151936
+    b32 = bench.lm_head_roofline(CONFIG_BY_NAME["qwen3_8b_b32_paged"], 1_248_862_208, 0.5, hbm,
+                                 tc, None)
+    assert b32["bound"] == "tensor" and b32["unit"] == "TFLOP/s"
+    assert b32["flops_per_launch"] == flops and b32["peak"] == 1915.7
+    assert abs(b32["achieved"] - flops / 0.5e-3 / 1e12) < 1e-9 * b32["achieved"]
+    assert b32["frac"] == b32["tensor_frac"]
