@@ -242,7 +242,7 @@ extern "C" const char* dflash_status_string(int code) {
   }
 }
 
-extern "C" int dflash_version(void) { return 106; }
+extern "C" int dflash_version(void) { return 107; }
 
 extern "C" int dflash_selftest_wait(int arrive, void* ws, size_t ws_bytes,
                                     dflash_stream_t stream) {

@@ -387,7 +387,7 @@ DFLASH_API const char* dflash_status_string(int code);
  */
 DFLASH_API int dflash_selftest_wait(int arrive, void* ws, size_t ws_bytes, dflash_stream_t stream);
 
-/* Library ABI version (major * 100 + minor): 106. */
+/* Library ABI version (major * 100 + minor): 107. */
 DFLASH_API int dflash_version(void);
 
 #ifdef __cplusplus
