@@ -235,6 +235,72 @@ def verify_attention(q_blk, k_blk, v_blk, ctx_k, ctx_v, seq_len, rope_theta: flo
 
 
 # ---------------------------------------------------------------------------
+# next: the target's prefill (attention over prompt chunks, staged token)
+# ---------------------------------------------------------------------------
+def prefill_attention(q, k, v, ctx_k, ctx_v, seq_len, rope_theta: float, scale: float) -> dict:
+    """The target's attention over one chunk of the prompt, one layer.
+
+    [P2] 单次前向验证 ①: the target prefills the prompt chunk by chunk, which
+    initialises its KV cache.  A decoder is causal, so chunk row t of sequence
+    b, at position L_b + t, attends to the rows already cached (0..L_b-1) and
+    to the chunk rows 0..t; the chunk's rotated K and its V join the cache at
+    rows L_b..L_b+T-1.  A whole prompt fed in chunks therefore gives the same
+    rows as the prompt fed at once.  GQA, RoPE and positions as in
+    block_attention.
+    q [B,T,Hq,D], k/v [B,T,Hkv,D] (pre-RoPE), any T >= 1; ctx_k/ctx_v per
+    sequence with at least L_b rows [.., Hkv, D] (stored rotated); seq_len [B].
+    Returns o [B,T,Hq,D], the rotated chunk K and the chunk V [B,T,Hkv,D].
+    """
+    q, k, v = as_f64(q), as_f64(k), as_f64(v)
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    G = Hq // Hkv
+    out = np.zeros((B, T, Hq, D), dtype=np.float64)
+    k_rot = np.zeros((B, T, Hkv, D), dtype=np.float64)
+    for b in range(B):
+        L = int(seq_len[b])
+        pos = L + np.arange(T, dtype=np.float64)
+        qr = apply_rope(q[b], np.broadcast_to(pos[:, None], (T, Hq)), rope_theta)
+        kr = apply_rope(k[b], np.broadcast_to(pos[:, None], (T, Hkv)), rope_theta)
+        k_rot[b] = kr
+        keys = np.concatenate([as_f64(ctx_k[b][:L]).reshape(L, Hkv, D), kr], axis=0)
+        vals = np.concatenate([as_f64(ctx_v[b][:L]).reshape(L, Hkv, D), v[b]], axis=0)
+        # row t sees keys 0 .. L + t
+        hidden = np.arange(L + T)[None, :] > (L + np.arange(T))[:, None]
+        for h in range(Hq):
+            g = h // G
+            s = (qr[:, h, :] @ keys[:, g, :].T) * scale
+            s[hidden] = -np.inf
+            s = s - s.max(axis=1, keepdims=True)
+            p = np.exp(s)
+            p = p / p.sum(axis=1, keepdims=True)
+            out[b, :, h, :] = p @ vals[:, g, :]
+    return {"o": out, "k": k_rot, "v": v.copy()}
+
+
+def prefill_staged(last_hidden, w_lm, chunk: int = 8192) -> dict:
+    """The first staged token ([P2] 单次前向验证 ②): the target's greedy token
+    after the prompt, i.e. the argmax (lowest index on exact ties) of the LM
+    head at the last prompt row.  last_hidden [B, H] (final-normed).  Returns
+    the tokens [B] with the gap and max of lm_head_argmax."""
+    r = lm_head_argmax(last_hidden, w_lm, chunk)
+    r["staged"] = r["posterior"].copy()
+    return r
+
+
+def round_bf16(x) -> np.ndarray:
+    """float64 -> bf16 bit patterns (uint16), rounding to nearest even via the
+    float32 value (x rounded to float32, then its 16 low bits rounded away).
+    Used where a float64 computation hands values to a bf16 consumer."""
+    f = np.asarray(x, dtype=np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    nan = np.isnan(f)
+    r = ((u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16))
+    r = np.where(nan, (u >> np.uint64(16)) | np.uint64(0x40), r)
+    return r.astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
 # next: rollback of the recurrent (GatedDeltaNet) state of a hybrid target
 # ---------------------------------------------------------------------------
 def gdn_step(S, k, v, beta: float, g: float) -> np.ndarray:

@@ -224,3 +224,82 @@ def test_verify_attention_last_row_is_the_block_attention():
     v2[0, 1:] += 5.0
     again = verify_attention(q, k2, v2, ck, cv, lens, THETA, 0.3)["o"]
     np.testing.assert_array_equal(again[0, 0], causal[0, 0])
+
+
+# ---------------------------------------------------------------------------
+# the target's prefill attention (causal over prompt chunks)
+# ---------------------------------------------------------------------------
+from oracle.dflash_oracle import prefill_attention, prefill_staged  # noqa: E402
+
+
+def test_prefill_attention_brute_force_ragged_chunk():
+    """A chunk of 37 rows (not a multiple of 16) after 5 and after 0 cached rows."""
+    rng = np.random.default_rng(31)
+    q, k, v, ck, cv, lens = _rand_case(rng, T=37, lens=(5, 0))
+    r = prefill_attention(q, k, v, ck, cv, lens, THETA, 0.35)
+    ref = brute_verify_attention(q, k, v, ck, cv, lens, THETA, 0.35)
+    np.testing.assert_allclose(r["o"], ref, rtol=0, atol=1e-12)
+    for j in (0, 16, 36):
+        np.testing.assert_allclose(r["k"][1, j, 0], rope_complex(list(k[1, j, 0]), j),
+                                   atol=1e-12)
+    np.testing.assert_array_equal(r["v"], v)
+
+
+def test_prefill_attention_chunked_equals_whole():
+    """Feeding a 50-row prompt as chunks of 16, 7 and 27 rows, each appended to
+    the cache before the next, gives the rows of one 50-row chunk."""
+    rng = np.random.default_rng(32)
+    q, k, v, ck, cv, lens = _rand_case(rng, B=2, T=50, lens=(3, 0))
+    whole = prefill_attention(q, k, v, ck, cv, lens, THETA, 0.3)
+    cache_k = [c.copy() for c in ck]
+    cache_v = [c.copy() for c in cv]
+    L = lens.copy()
+    outs = []
+    for a, b in ((0, 16), (16, 23), (23, 50)):
+        r = prefill_attention(q[:, a:b], k[:, a:b], v[:, a:b], cache_k, cache_v, L, THETA, 0.3)
+        outs.append(r["o"])
+        for s in range(2):
+            cache_k[s] = np.concatenate([cache_k[s][:L[s]], r["k"][s]])
+            cache_v[s] = np.concatenate([cache_v[s][:L[s]], r["v"][s]])
+        L = L + (b - a)
+    np.testing.assert_allclose(np.concatenate(outs, axis=1), whole["o"], rtol=0, atol=1e-12)
+    for s in range(2):
+        np.testing.assert_allclose(cache_k[s][lens[s]:], whole["k"][s], rtol=0, atol=1e-13)
+
+
+def test_prefill_attention_reduces_to_textbook_causal_mha():
+    """No cached rows, G = 1: plain causal multi-head attention over the chunk."""
+    rng = np.random.default_rng(33)
+    T = 24
+    q, k, v, ck, cv, lens = _rand_case(rng, B=1, T=T, Hq=2, Hkv=2, D=8, lens=(0,))
+    got = prefill_attention(q, k, v, ck, cv, lens, THETA, 1 / math.sqrt(8))["o"]
+    qr = np.array([[rope_complex(list(q[0, i, h]), i) for i in range(T)] for h in range(2)])
+    kr = np.array([[rope_complex(list(k[0, i, h]), i) for i in range(T)] for h in range(2)])
+    vr = np.transpose(v[0], (1, 0, 2))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(qr)[None], torch.from_numpy(kr)[None], torch.from_numpy(vr)[None],
+        is_causal=True)[0].numpy()
+    np.testing.assert_allclose(got[0], np.transpose(ref, (1, 0, 2)), rtol=0, atol=1e-12)
+
+
+def test_prefill_attention_of_16_rows_is_the_verify_attention():
+    rng = np.random.default_rng(34)
+    q, k, v, ck, cv, lens = _rand_case(rng, lens=(11, 4))
+    a = prefill_attention(q, k, v, ck, cv, lens, THETA, 0.25)
+    b = verify_attention(q, k, v, ck, cv, lens, THETA, 0.25)
+    for key in ("o", "k", "v"):
+        np.testing.assert_allclose(a[key], b[key], rtol=0, atol=1e-12)
+
+
+def test_prefill_staged_is_the_argmax_at_the_last_row():
+    """The staged token: the plain argmax of the logits, lowest index on exact ties."""
+    rng = np.random.default_rng(35)
+    h = rng.standard_normal((3, 16))
+    w = rng.standard_normal((300, 16))
+    w[57] *= 5.0                                     # row 1's maximum: the pair 57, 200
+    w[200] = w[57]                                   # an exact tie: 57 must win
+    h[1] = w[57]
+    r = prefill_staged(h, w, chunk=64)
+    logits = h @ w.T
+    assert list(r["staged"]) == [int(np.argmax(x)) for x in logits]
+    assert r["staged"][1] == 57
