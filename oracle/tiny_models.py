@@ -22,9 +22,9 @@ from dataclasses import dataclass
 
 import numpy as np
 
-from .dflash_oracle import (BLOCK, acceptance_length, apply_rope, block_attention,
+from .dflash_oracle import (BLOCK, acceptance_length, apply_rope, bf16_to_f64, block_attention,
                             ctx_project, draft_out_mlp, draft_qkv, draft_tokens,
-                            kv_crop_lengths, rms_norm, verify_accept)
+                            kv_crop_lengths, rms_norm, round_bf16, verify_accept)
 
 
 def _rows(x: np.ndarray, w: np.ndarray) -> np.ndarray:
@@ -35,6 +35,11 @@ def _rows(x: np.ndarray, w: np.ndarray) -> np.ndarray:
 
 def _silu(x):
     return x / (1.0 + np.exp(-x))
+
+
+def _bf16_values(x):
+    """x rounded to the nearest bf16 values (float64 holding them exactly)."""
+    return bf16_to_f64(round_bf16(x))
 
 
 @dataclass
@@ -88,14 +93,25 @@ class KVCache:
 
 
 class TinyTarget:
-    def __init__(self, seed: int = 0, dims: TinyDims = TinyDims()):
+    """With ``bf16_head`` the target is a bf16 model at its boundaries: the
+    embedding table and the LM head hold bf16 values, and the final hidden
+    state reaches the LM head rounded to bf16 (as a bf16 model hands it over);
+    the body still computes in float64.  Greedy decoding and the speculative
+    loop both take logits through :meth:`logits` / :meth:`head_input`, so the
+    loop stays exactly lossless."""
+
+    def __init__(self, seed: int = 0, dims: TinyDims = TinyDims(), bf16_head: bool = False):
         rng = np.random.default_rng(seed)
         self.d = dims
+        self.bf16_head = bf16_head
         self.embed = rng.standard_normal((dims.vocab, dims.hidden))
         self.layers = [_Layer(rng, dims) for _ in range(dims.n_layers)]
         self.final_norm = 1.0 + 0.1 * rng.standard_normal(dims.hidden)
         self.lm_head = (1.0 / np.sqrt(dims.hidden)) * rng.standard_normal((dims.vocab,
                                                                            dims.hidden))
+        if bf16_head:
+            self.embed = _bf16_values(self.embed)
+            self.lm_head = _bf16_values(self.lm_head)
 
     def new_cache(self) -> KVCache:
         d = self.d
@@ -142,14 +158,18 @@ class TinyTarget:
         cache.length = start + n
         return rms_norm(x, self.final_norm, d.rms_eps), outs
 
+    def head_input(self, final_hidden):
+        """The final hidden rows as the LM head receives them."""
+        return _bf16_values(final_hidden) if self.bf16_head else final_hidden
+
     def logits(self, final_hidden):
-        return _rows(final_hidden, self.lm_head)
+        return _rows(self.head_input(final_hidden), self.lm_head)
 
 
 class TinyDrafter:
     """One-layer block-diffusion drafter sharing the target's embedding and LM head."""
 
-    def __init__(self, target: TinyTarget, seed: int = 1):
+    def __init__(self, target: TinyTarget, seed: int = 1, bf16_weights: bool = False):
         d = target.d
         rng = np.random.default_rng(seed)
         self.t = target
@@ -160,6 +180,12 @@ class TinyDrafter:
         self.hidden_norm = 1.0 + 0.1 * rng.standard_normal(d.hidden)
         self.layer = _Layer(rng, d)
         self.final_norm = 1.0 + 0.1 * rng.standard_normal(d.hidden)
+        if bf16_weights:         # every weight a bf16 value (a bf16 drafter's weights)
+            self.w_fc = _bf16_values(self.w_fc)
+            self.hidden_norm = _bf16_values(self.hidden_norm)
+            self.final_norm = _bf16_values(self.final_norm)
+            for name, w in vars(self.layer).items():
+                setattr(self.layer, name, _bf16_values(w))
         self.mask_id = d.vocab - 1
         self.ctx_k = np.zeros((d.capacity, d.n_kv_heads, d.head_dim))
         self.ctx_v = np.zeros((d.capacity, d.n_kv_heads, d.head_dim))
@@ -231,7 +257,7 @@ def spec_loop(target: TinyTarget, drafter, prompt, n_new: int, on_cycle=None) ->
         drafts = drafter.draft(staged)                           # ③④
         block = np.concatenate([[staged], drafts]).astype(np.int32)
         hv, outs = target.forward(block, cache)                  # ⑤ one target forward
-        r = verify_accept(hv[None], target.lm_head, block[None],
+        r = verify_accept(target.head_input(hv)[None], target.lm_head, block[None],
                           np.array([len(committed)]), out_cap=len(committed) + BLOCK)
         a = int(r["accept"][0])                                   # ⑥
         committed.extend(int(t) for t in r["out_tokens"][0, len(committed):

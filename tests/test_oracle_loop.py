@@ -49,6 +49,21 @@ def test_spec_loop_equals_greedy_decode(seed):
     assert max(peek["accepts"]) >= 5              # long acceptances exercised
 
 
+@pytest.mark.parametrize("seed", [4, 5])
+def test_spec_loop_equals_greedy_decode_with_bf16_boundaries(seed):
+    """The same property for a target whose embedding, LM head and LM-head
+    input are bf16 values (and a drafter with bf16 weights): the form a GPU
+    loop consumes."""
+    t = TinyTarget(seed, bf16_head=True)
+    assert np.array_equal(t.lm_head.astype(np.float32).astype(np.float64), t.lm_head)
+    prompt = list(np.random.default_rng(200 + seed).integers(0, 90, size=9))
+    n = 40
+    greedy = greedy_decode(t, prompt, n)
+    assert spec_loop(t, TinyDrafter(t, seed + 20, bf16_weights=True), prompt, n)["tokens"] == greedy
+    truth = greedy_decode(t, prompt, n + 40)
+    assert spec_loop(t, PeekingDrafter(t, truth, len(prompt), seed), prompt, n)["tokens"] == greedy
+
+
 def test_crop_invariant_after_every_cycle():
     t = TinyTarget(3)
     prompt = [4, 8, 15, 16, 23, 42]
