@@ -9,10 +9,10 @@
 //   K  = RoPE(RMSNorm_head(Y^ W_k^T) g_k),   V = Y^ W_v^T.
 // With that many rows the GEMMs are bound by the tensor cores, not by the
 // weight stream, so they run on the tiled GEMM of tile_gemm.cuh (persistent
-// clusters of two CTAs over 128 x BN output tiles, the weight box multicast
-// to both CTAs of a pair, TMEM lane = token row) rather than on the stream-K
-// one; the row-wise work of the epilogues (sums of squares, head norms, the
-// RoPE partner at d + D/2) stays inside one thread.
+// clusters of two CTAs over 128 x BN output tiles, the pair reading each
+// weight box once from DRAM and once from L2, TMEM lane = token row) rather
+// than on the stream-K one; the row-wise work of the epilogues (sums of
+// squares, head norms, the RoPE partner at d + D/2) stays inside one thread.
 //  1. fc GEMM.  The token operand of k-tile kt is read from layer
 //     floor(64 kt / H) through its own tensor map (the concatenation is never
 //     built).  Epilogue: bf16(g_h * Y) and the tile's sum of Y^2 per row.
@@ -374,7 +374,10 @@ extern "C" size_t dflash_prefill_workspace_bytes(const dflash_dims* dims, int32_
   if (!dims) return 0;
   PrefillPlan p;
   if (make_prefill_plan(*dims, tokens_per_seq, &p)) return 0;
-  return p.total;
+  // one workspace serves both prefill calls (status word at offset 0 in both)
+  const size_t att = prefill_attention_workspace(*dims, tokens_per_seq);
+  if (att == 0) return 0;
+  return att > p.total ? att : p.total;
 }
 
 extern "C" int dflash_ctx_prefill(const dflash_dims* dims, int32_t tokens_per_seq,

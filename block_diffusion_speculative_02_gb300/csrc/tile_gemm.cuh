@@ -6,14 +6,13 @@
 // clusters of two walk pairs of 128 x BN output tiles (token rows x
 // features) that share their feature range, in a banded raster order (8 pairs
 // of row tiles per band, so the clusters of one wave share weight and token
-// tiles in L2).  A TMA pipeline stages each CTA's own 128 x 64 token box, and
-// each CTA loads one half of the BN x 64 weight box multicast to both CTAs of
-// the pair, so every weight byte leaves L2 once per pair; a stage is refilled
-// only when the MMAs of both CTAs have released it (their commits arrive on
-// both CTAs' empty barriers).  One thread issues tcgen05.mma (M = 128 tokens,
-// N = BN features, K = 16) into one of two TMEM accumulators while four
-// epilogue warps drain the other.  TMEM lane = token row, so an epilogue's
-// row-wise work stays inside one thread.
+// tiles in L2).  The cluster only places the two CTAs of a pair on one GPC:
+// each CTA's TMA pipeline stages its own 128 x 64 token box and the whole
+// BN x 64 weight box (two boxes of BN/2 rows), so the pair's second read of
+// the weight box is an L2 hit.  One thread issues tcgen05.mma (M = 128
+// tokens, N = BN features, K = 16) into one of two TMEM accumulators while
+// four epilogue warps drain the other.  TMEM lane = token row, so an
+// epilogue's row-wise work stays inside one thread.
 //
 // The epilogue is a policy class Epi with
 //   using Params = ...;                        (passed as a grid constant)
@@ -35,7 +34,6 @@ constexpr int kTileThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kTileM = 128;
 constexpr int kTileABytes = kTileM * 128;  // 128 rows x 64 bf16
 constexpr int kBand = 8;                   // pairs of row tiles per raster band
-constexpr uint16_t kPairMask = 0x3;        // both CTAs of the cluster
 constexpr int kTileSmemBudget = 220 * 1024;
 
 struct TileCore {
@@ -47,8 +45,8 @@ struct TileCore {
   int b_split2;      // > 0: feature tiles from it on read weight map 2
   int b_cols;        // > 0: weight columns; k-tile kt reads weight column (64 kt) % b_cols
                      // (the same weights against two token operands summed along K)
-  int b_paired;      // 1: CTA c of the pair loads its half of feature tile n from weight
-                     // map c, rows n * BN/2 ..: accumulator columns [0, BN/2) are map 0's
+  int b_paired;      // 1: half h of feature tile n's weight box comes from weight map h,
+                     // rows n * BN/2 ..: accumulator columns [0, BN/2) are map 0's
                      // features, [BN/2, BN) map 1's same features (b_split unused)
   int n_stages, stage_bytes;
   uint32_t* status;
@@ -98,12 +96,12 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
   const int mp_tiles = (p.m_tiles + 1) >> 1;
   const int n_total = mp_tiles * p.n_tiles;                // pair tiles
   const uint32_t acc_cols = static_cast<uint32_t>(p.bn);
-  const int half_rows = p.bn >> 1;                         // weight rows this CTA loads
+  const int half_rows = p.bn >> 1;                         // rows of one weight box
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.n_stages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 2);  // the MMAs of both CTAs of the pair
+      mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
@@ -120,7 +118,6 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
   if (threadIdx.x >= 64) Epi::setup(ep, tab, threadIdx.x - 64);
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers are initialised before anything lands in them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   griddep_wait();
@@ -136,10 +133,9 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
         tile_coords(mp_tiles, p.n_tiles, t, &mp, &n);
         const int m = 2 * mp + crank;
         const bool third = !p.b_paired && p.b_split2 > 0 && n >= p.b_split2;
-        const bool second = p.b_paired ? crank == 1 : (!third && n >= p.b_split);
+        const bool second = !p.b_paired && !third && n >= p.b_split;
         const CUtensorMap* mb = third ? &tm_b.m[2] : (second ? &tm_b.m[1] : &tm_b.m[0]);
-        const int n_local = third ? n - p.b_split2 : (second && !p.b_paired ? n - p.b_split : n);
-        const int brow = p.b_paired ? n * half_rows : n_local * p.bn + crank * half_rows;
+        const int n_local = third ? n - p.b_split2 : (second ? n - p.b_split : n);
         for (int kt = 0; kt < p.k_tiles; ++kt) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) {
             ok = false;
@@ -150,8 +146,13 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
           const int l = (kt * 64) / p.layer_cols;
           tma_load_2d(a, &tm_a.m[l], &full[stage], kt * 64 - l * p.layer_cols, m * kTileM, pol);
           const int bcol = p.b_cols > 0 ? (kt * 64) % p.b_cols : kt * 64;
-          tma_load_2d_mc(a + kTileABytes + crank * half_rows * 128, mb, &full[stage], bcol,
-                         brow, kPairMask, pol);
+          // the weight box in two halves of BN/2 rows (a box has at most 256 rows)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const CUtensorMap* mh = p.b_paired ? &tm_b.m[h] : mb;
+            const int brow = p.b_paired ? n * half_rows : n_local * p.bn + h * half_rows;
+            tma_load_2d(a + kTileABytes + h * half_rows * 128, mh, &full[stage], bcol, brow, pol);
+          }
           ++issued;
           if (++stage == static_cast<uint32_t>(p.n_stages)) {
             stage = 0;
@@ -191,7 +192,7 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             umma_bf16(acc, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kt | kk) ? 1u : 0u);
-          umma_commit_mc(&empty[stage], kPairMask);  // frees the stage in both CTAs' eyes
+          umma_commit(&empty[stage]);
           if (++stage == static_cast<uint32_t>(p.n_stages)) {
             stage = 0;
             phase ^= 1;
@@ -222,9 +223,6 @@ tile_gemm_kernel(const __grid_constant__ TokenMaps tm_a, const __grid_constant__
     }
   }
   __syncthreads();
-  // the peer may still be releasing stages of this CTA (its MMA commits
-  // arrive here): neither CTA leaves before both have drained
-  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 2 * acc_cols);
