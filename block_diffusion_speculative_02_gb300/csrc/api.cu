@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "host.h"
+#include "streamk_gemm.cuh"
 
 namespace dflash {
 
@@ -130,10 +131,14 @@ int make_plan(const dflash_dims& d, Plan* p) {
   off = align_up(off + sizeof(uint32_t) * (q.fc_out_tiles * q.fc_tok_chunks +
                                            q.kv_out_tiles * q.kv_tok_chunks), 256);
   q.off_ss = off;      off = align_up(off + sizeof(float) * (size_t)q.fc_out_tiles * q.ntok, 256);
-  q.off_fc = off;      off = align_up(off + sizeof(float) * (size_t)q.ntok * d.hidden, 256);
+  // partial tiles of the two stream-K GEMMs (sk::partial_bytes: every SM budget fits)
+  q.off_fc = off;
+  off = align_up(off + sk::partial_bytes(sk::gemm_dims(q.ntok, d.n_ctx_layers * d.hidden,
+                                                       q.fc_out_tiles, 0), q.num_sms), 256);
   q.off_yhat = off;    off = align_up(off + 2 * sizeof(uint16_t) * (size_t)q.ntok * d.hidden, 1024);
   q.off_kv = off;
-  off = align_up(off + sizeof(float) * (size_t)q.ntok * 2 * d.n_kv_heads * d.head_dim, 256);
+  off = align_up(off + sk::partial_bytes(sk::gemm_dims(q.ntok, d.hidden, q.kv_out_tiles, 1),
+                                         q.num_sms), 256);
   const size_t att_units = (size_t)d.batch * d.n_kv_heads * q.att_splits * q.att_rows;
   q.off_att_o = off;   off = align_up(off + sizeof(float) * att_units * d.head_dim, 256);
   q.off_att_ml = off;  off = align_up(off + sizeof(float) * 2 * att_units, 256);
@@ -242,7 +247,7 @@ extern "C" const char* dflash_status_string(int code) {
   }
 }
 
-extern "C" int dflash_version(void) { return 107; }
+extern "C" int dflash_version(void) { return 108; }
 
 extern "C" int dflash_selftest_wait(int arrive, void* ws, size_t ws_bytes,
                                     dflash_stream_t stream) {

@@ -18,14 +18,15 @@
 //  2. K/V GEMM  [K;V] = [hi;lo] W_{k|v}^T.  Finisher: the RMSNorm scale of Y
 //     (one factor per token row, so it commutes with the GEMM), per-head
 //     RMSNorm and RoPE for K, bf16 store into the cache rows.
-// The order of the fp32 additions across CTAs is not fixed, so results can
-// differ between runs by fp32 rounding (well inside the bf16 outputs' ulp).
+// The CTAs' partial sums of a tile are added in a fixed order, so the same
+// inputs give the same cache bytes on every run (with the same SM budget).
 #include "streamk_gemm.cuh"
 
 namespace dflash {
 namespace {
 
 using sk::GemmCore;
+using sk::take4;
 
 // Parameters of both finishers.
 struct ProjParams {
@@ -74,15 +75,6 @@ __device__ __forceinline__ float4 load4_bf16(const uint16_t* src) {
   const uint2 w = *reinterpret_cast<const uint2*>(src);
   return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
                      __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
-}
-
-// The finished sums of 4 consecutive features of token row `tok`, cleared
-// again for the next call.
-__device__ __forceinline__ float4 take4(const GemmCore& p, int tok, int f0) {
-  float4* src = reinterpret_cast<float4*>(p.acc + static_cast<size_t>(tok) * p.ld_out + f0);
-  const float4 v = __ldcg(src);
-  __stcg(src, make_float4(0.f, 0.f, 0.f, 0.f));
-  return v;
 }
 
 // fc finisher (CTA that completed an output tile): Y = the accumulated sum;
@@ -327,19 +319,10 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
 
   // ---- 1. fc GEMM; its finisher writes hi/lo of g_h * Y and sums of Y^2 ----
   {
-    GemmCore g = {};
+    GemmCore g = sk::gemm_dims(ntok, nL * H, plan.fc_out_tiles, 0);
     g.status = status;
-    g.k_tiles = plan.fc_k_tiles;
-    g.out_tiles = plan.fc_out_tiles;
-    g.a_split[0] = g.a_split[1] = plan.fc_out_tiles;
-    g.layer_cols = H;
-    g.n_tok = ntok;
-    g.chunk_rows = ntok < 256 ? ntok : 256;
-    g.n_chunks = plan.fc_tok_chunks;
-    g.hilo = 0;
-    g.ld_out = H;
-    g.mma_n = g.chunk_rows;
-    g.acc = part_fc;
+    g.layer_cols = H;  // the k-loop moves to the next layer's map every H columns
+    g.part = part_fc;
     g.tickets = tickets;
     sk::AMaps am;
     if ((rc = make_tmap_2d_bf16(&am.m[0], w_fc, static_cast<uint64_t>(nL) * H, H,
@@ -352,25 +335,16 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
                                   static_cast<uint64_t>(H) * 2, 64, g.chunk_rows)))
         return rc;
     for (int l = nL; l < kMaxCtxLayers; ++l) bm.m[l] = bm.m[0];
-    if ((rc = sk::run_streamk<FcFin>(g, g.chunk_rows, am, bm, fp, plan.budget_sms, st)))
+    if ((rc = sk::run_streamk<FcFin>(g, am, bm, fp, plan.budget_sms, st,
+                                     plan.off_yhat - plan.off_fc)))
       return rc;
   }
   // ---- 2. K/V GEMM on [hi; lo]; its finisher scales, normalises, rotates, stores ----
   {
-    GemmCore g = {};
+    GemmCore g = sk::gemm_dims(ntok, H, plan.kv_out_tiles, 1);
     g.status = status;
-    g.k_tiles = plan.kv_k_tiles;
-    g.out_tiles = plan.kv_out_tiles;
     g.a_split[0] = plan.kv_out_tiles / 2;
-    g.a_split[1] = plan.kv_out_tiles;
-    g.layer_cols = H;
-    g.n_tok = ntok;
-    g.chunk_rows = ntok < 128 ? ntok : 128;
-    g.n_chunks = plan.kv_tok_chunks;
-    g.hilo = 1;
-    g.ld_out = 2 * kvd;
-    g.mma_n = 2 * g.chunk_rows;
-    g.acc = part_kv;
+    g.part = part_kv;
     g.tickets = tickets + plan.fc_out_tiles * plan.fc_tok_chunks;
     sk::AMaps am;
     if ((rc = make_tmap_2d_bf16(&am.m[0], w_k, H, kvd, static_cast<uint64_t>(H) * 2, 64, 128)))
@@ -383,7 +357,8 @@ extern "C" int dflash_ctx_project(const dflash_dims* dims, const void* const* la
                                 static_cast<uint64_t>(H) * 2, 64, g.chunk_rows)))
       return rc;
     for (int l = 1; l < kMaxCtxLayers; ++l) bm.m[l] = bm.m[0];
-    if ((rc = sk::run_streamk<KvFin>(g, 2 * g.chunk_rows, am, bm, fp, plan.budget_sms, st)))
+    if ((rc = sk::run_streamk<KvFin>(g, am, bm, fp, plan.budget_sms, st,
+                                     plan.off_att_o - plan.off_kv)))
       return rc;
   }
   return DFLASH_OK;

@@ -27,6 +27,7 @@ namespace dflash {
 namespace {
 
 using sk::GemmCore;
+using sk::take4;
 
 constexpr int kTokGroup = 4;  // token rows a warp finishes together (loads in flight)
 
@@ -41,15 +42,6 @@ __device__ __forceinline__ float4 ld4_bf16(const uint16_t* src) {
   const uint2 w = *reinterpret_cast<const uint2*>(src);
   return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
                      __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
-}
-
-// The finished sums of 4 consecutive features of token row `tok`, cleared for
-// the next GEMM that uses the accumulator.
-__device__ __forceinline__ float4 take4(const GemmCore& g, int tok, int f0) {
-  float4* src = reinterpret_cast<float4*>(g.acc + static_cast<size_t>(tok) * g.ld_out + f0);
-  const float4 v = __ldcg(src);
-  __stcg(src, make_float4(0.f, 0.f, 0.f, 0.f));
-  return v;
 }
 
 // Store a (x) as the bf16 pair hi + lo at rows tok and n_tok + tok.
@@ -462,22 +454,14 @@ int hilo_token_maps(TokenMaps& am, const uint16_t* hl, int rows, int cols) {
   return rc;
 }
 
-// Fill the common GEMM fields for n_tok token rows of a K-column operand.
-void gemm_shape(GemmCore& g, const DraftPlan& plan, int k_cols, int out_tiles, int hilo,
-                uint32_t* tickets, float* acc, void* ws) {
+// The GEMM fields for n_tok token rows of a K-column operand.
+GemmCore gemm_shape(const DraftPlan& plan, int k_cols, int out_tiles, int hilo,
+                    uint32_t* tickets, float* part, void* ws) {
+  GemmCore g = sk::gemm_dims(plan.ntok, k_cols, out_tiles, hilo);
   g.status = ws_at<uint32_t>(ws, plan.off_status);
-  g.k_tiles = k_cols / 64;
-  g.out_tiles = out_tiles;
-  g.a_split[0] = g.a_split[1] = out_tiles;
-  g.pair_stride = 0;
-  g.layer_cols = k_cols;
-  g.n_tok = plan.ntok;
-  g.chunk_rows = hilo ? (plan.ntok < 128 ? plan.ntok : 128) : (plan.ntok < 256 ? plan.ntok : 256);
-  g.n_chunks = (plan.ntok + g.chunk_rows - 1) / g.chunk_rows;
-  g.hilo = hilo;
-  g.mma_n = (1 + hilo) * g.chunk_rows;
-  g.acc = acc;
+  g.part = part;
   g.tickets = tickets;
+  return g;
 }
 
 int token_map(sk::BMaps& bm, const void* base, int cols, int rows, int box_rows) {
@@ -510,10 +494,15 @@ int make_draft_plan(const dflash_dims& d, int ffn, DraftPlan* out) {
   p.gu_tiles = 2 * ffn / 128;
   p.down_tiles = H / 128;
   auto al = [](size_t x, size_t a) { return (x + a - 1) / a * a; };
-  size_t acc_a = qd + 2 * kvd;
-  if ((size_t)H > acc_a) acc_a = H;
-  size_t acc_b = 2 * (size_t)ffn;
-  if ((size_t)H > acc_b) acc_b = H;
+  // partial tiles of the stream-K GEMMs: Q/K/V and the output projection
+  // share region a, gate|up and down region b (each sized for the larger)
+  const int nt = p.ntok;
+  size_t acc_a = sk::partial_bytes(sk::gemm_dims(nt, H, p.qkv_tiles, 1), p.num_sms);
+  const size_t o_bytes = sk::partial_bytes(sk::gemm_dims(nt, qd, p.o_tiles, 0), p.num_sms);
+  if (o_bytes > acc_a) acc_a = o_bytes;
+  size_t acc_b = sk::partial_bytes(sk::gemm_dims(nt, H, p.gu_tiles, 1), p.num_sms);
+  const size_t d_bytes = sk::partial_bytes(sk::gemm_dims(nt, ffn, p.down_tiles, 1), p.num_sms);
+  if (d_bytes > acc_b) acc_b = d_bytes;
   // buffers that do not depend on ffn first, so that the Q/K/V and token
   // steps find them at the same offsets whatever ffn the workspace was sized for
   size_t off = 0;
@@ -527,12 +516,12 @@ int make_draft_plan(const dflash_dims& d, int ffn, DraftPlan* out) {
   p.off_xhl = off;     off = al(off + 2 * 2 * (size_t)p.ntok * H, 1024);
   p.off_x1 = off;      off = al(off + 4 * (size_t)p.ntok * H, 256);
   p.off_xg = off;      off = al(off + 2 * (size_t)p.ntok * H, 1024);
-  p.off_acc_a = off;   off = al(off + 4 * (size_t)p.ntok * acc_a, 256);
+  p.off_acc_a = off;   off = al(off + acc_a, 256);
   p.ffn_begin = off;
   p.off_tickets_gu = off;  off = al(off + 4 * (size_t)p.gu_tiles * chunks_hilo, 64);
   p.off_tickets_down = off; off = al(off + 4 * (size_t)p.down_tiles * chunks_hilo, 1024);
   p.off_mhl = off;     off = al(off + 2 * 2 * (size_t)p.ntok * ffn, 1024);
-  p.off_acc_b = off;   off = al(off + 4 * (size_t)p.ntok * acc_b, 256);
+  p.off_acc_b = off;   off = al(off + acc_b, 256);
   p.total = off;
   *out = p;
   return DFLASH_OK;
@@ -618,19 +607,18 @@ extern "C" int dflash_draft_qkv(const dflash_dims* dims, const void* x, const vo
     return run_tile_gemm<QkvTileEpi>(t, am, bm, fp, st, plan.budget_sms);
   }
 
-  GemmCore g = {};
-  gemm_shape(g, plan, H, plan.qkv_tiles, 1, ws_at<uint32_t>(ws, plan.off_tickets_qkv),
-             ws_at<float>(ws, plan.off_acc_a), ws);
+  GemmCore g = gemm_shape(plan, H, plan.qkv_tiles, 1, ws_at<uint32_t>(ws, plan.off_tickets_qkv),
+                          ws_at<float>(ws, plan.off_acc_a), ws);
   g.a_split[0] = qd / 128;
   g.a_split[1] = (qd + kvd) / 128;
-  g.ld_out = qd + 2 * kvd;
   sk::AMaps am;
   sk::BMaps bm;
   if ((rc = weight_map(&am.m[0], w_q, qd, H)) || (rc = weight_map(&am.m[1], w_k, kvd, H)) ||
       (rc = weight_map(&am.m[2], w_v, kvd, H)))
     return rc;
   if ((rc = token_map(bm, xhl, H, 2 * plan.ntok, g.chunk_rows))) return rc;
-  return sk::run_streamk<QkvFin>(g, 2 * g.chunk_rows, am, bm, fp, plan.budget_sms, st);
+  return sk::run_streamk<QkvFin>(g, am, bm, fp, plan.budget_sms, st,
+                                 plan.ffn_begin - plan.off_acc_a);
 }
 
 extern "C" int dflash_draft_mlp(const dflash_dims* dims, int32_t ffn, const void* x,
@@ -687,16 +675,15 @@ extern "C" int dflash_draft_mlp(const dflash_dims* dims, int32_t ffn, const void
     bm.m[1] = bm.m[2] = bm.m[0];
     if ((rc = run_tile_gemm<OprojTileEpi>(t, am, bm, fp, st, plan.budget_sms))) return rc;
   } else {
-    GemmCore g = {};
-    gemm_shape(g, plan, qd, plan.o_tiles, 0, ws_at<uint32_t>(ws, plan.off_tickets_o),
-               ws_at<float>(ws, plan.off_acc_a), ws);
-    g.ld_out = H;
+    GemmCore g = gemm_shape(plan, qd, plan.o_tiles, 0, ws_at<uint32_t>(ws, plan.off_tickets_o),
+                            ws_at<float>(ws, plan.off_acc_a), ws);
     sk::AMaps am;
     sk::BMaps bm;
     if ((rc = weight_map(&am.m[0], w_o, H, qd))) return rc;
     am.m[1] = am.m[2] = am.m[0];
     if ((rc = token_map(bm, attn_out, qd, plan.ntok, g.chunk_rows))) return rc;
-    if ((rc = sk::run_streamk<OprojFin>(g, g.chunk_rows, am, bm, fp, plan.budget_sms, st)))
+    if ((rc = sk::run_streamk<OprojFin>(g, am, bm, fp, plan.budget_sms, st,
+                                        plan.ffn_begin - plan.off_acc_a)))
       return rc;
   }
   if (plan.ntok >= kTiledDraftRows) {
@@ -743,33 +730,32 @@ extern "C" int dflash_draft_mlp(const dflash_dims* dims, int32_t ffn, const void
   }
   // 2. [gate; up] on hi/lo of x1 * ln2; paired finishing: silu(g) * u as hi/lo
   {
-    GemmCore g = {};
-    gemm_shape(g, plan, H, plan.gu_tiles, 1, ws_at<uint32_t>(ws, plan.off_tickets_gu),
-               ws_at<float>(ws, plan.off_acc_b), ws);
+    GemmCore g = gemm_shape(plan, H, plan.gu_tiles, 1, ws_at<uint32_t>(ws, plan.off_tickets_gu),
+                            ws_at<float>(ws, plan.off_acc_b), ws);
     g.a_split[0] = ffn / 128;
     g.a_split[1] = plan.gu_tiles;
     g.pair_stride = ffn / 128;
-    g.ld_out = 2 * ffn;
     sk::AMaps am;
     sk::BMaps bm;
     if ((rc = weight_map(&am.m[0], w_gate, ffn, H)) || (rc = weight_map(&am.m[1], w_up, ffn, H)))
       return rc;
     am.m[2] = am.m[1];
     if ((rc = token_map(bm, fp.xhl, H, 2 * plan.ntok, g.chunk_rows))) return rc;
-    if ((rc = sk::run_streamk<GateUpFin>(g, 2 * g.chunk_rows, am, bm, fp, plan.budget_sms, st)))
+    if ((rc = sk::run_streamk<GateUpFin>(g, am, bm, fp, plan.budget_sms, st,
+                                         plan.total - plan.off_acc_b)))
       return rc;
   }
   // 3. x2 = x1 + M W_down^T
   {
-    GemmCore g = {};
-    gemm_shape(g, plan, ffn, plan.down_tiles, 1, ws_at<uint32_t>(ws, plan.off_tickets_down),
-               ws_at<float>(ws, plan.off_acc_b), ws);
-    g.ld_out = H;
+    GemmCore g = gemm_shape(plan, ffn, plan.down_tiles, 1,
+                            ws_at<uint32_t>(ws, plan.off_tickets_down),
+                            ws_at<float>(ws, plan.off_acc_b), ws);
     sk::AMaps am;
     sk::BMaps bm;
     if ((rc = weight_map(&am.m[0], w_down, H, ffn))) return rc;
     am.m[1] = am.m[2] = am.m[0];
     if ((rc = token_map(bm, fp.mhl, ffn, 2 * plan.ntok, g.chunk_rows))) return rc;
-    return sk::run_streamk<DownFin>(g, 2 * g.chunk_rows, am, bm, fp, plan.budget_sms, st);
+    return sk::run_streamk<DownFin>(g, am, bm, fp, plan.budget_sms, st,
+                                    plan.total - plan.off_acc_b);
   }
 }

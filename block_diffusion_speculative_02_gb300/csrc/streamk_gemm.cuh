@@ -9,11 +9,14 @@
 // budget) streams units [U*i/G, U*(i+1)/G): every CTA moves the same number
 // of weight bytes whatever the tile count.  A CTA's range crosses tile
 // boundaries; each piece accumulates in one of two TMEM slots (the epilogue
-// drains one while the MMAs fill the other) and is added into an fp32
-// accumulator in the workspace with fire-and-forget atomic adds.  The CTA
-// whose atomic ticket completes a tile's count of contributions (a closed
-// form of the partition) runs the finisher policy `Fin` on it once its own
-// pipeline has drained; the finisher reads the sums and clears them.
+// drains one while the MMAs fill the other) and is stored as an fp32 partial
+// tile in the workspace, in the slot of its piece index (the CTA's rank among
+// the tile's contributors).  The CTA whose atomic ticket completes a tile's
+// count of contributions (a closed form of the partition) runs the finisher
+// policy `Fin` on it once its own pipeline has drained: the pieces are added
+// in index order into shared memory and the finisher reads those sums, so
+// the result does not depend on the order in which the CTAs arrive: the same
+// inputs and grid give the same bits on every run.
 //
 // The weight matrix may be split over up to three tensor maps (tiles below
 // a_split[0] read map 0, ...), and the token matrix over up to eight maps
@@ -60,12 +63,12 @@ struct GemmCore {
   int chunk_rows;    // token rows per chunk (B box rows)
   int n_chunks;
   int hilo;          // 1: B = [hi rows ; lo rows] of a 2*n_tok-row matrix, summed in the epilogue
-  int ld_out;        // features per accumulator row
   int mma_n;         // MMA N = chunk_rows * (1 + hilo)
   int n_stages, stage_bytes, tmem_cols;
   int kb;            // 64-column K chunks per pipeline stage
   int b_chunk;       // bytes of the token tile of one chunk (1024-aligned)
-  float* acc;        // [n_tok][ld_out] fp32 accumulator, zero between calls
+  int max_pieces;    // partial-tile slots per tile (max_pieces() of the shape)
+  float* part;       // [n_chunks * out_tiles][max_pieces][chunk_rows][128] fp32 partial tiles
   uint32_t* tickets; // [n_chunks * out_tiles] contributions so far, zero between calls
   uint32_t* status;
 };
@@ -102,6 +105,80 @@ __device__ __forceinline__ int ticket_tile(const GemmCore& p, int T) {
 __device__ __forceinline__ uint32_t ticket_target(const GemmCore& p, int Tt) {
   return p.pair_stride == 0 ? tile_contributors(p, Tt)
                             : tile_contributors(p, Tt) + tile_contributors(p, Tt + p.pair_stride);
+}
+
+// Finishing a tile: its contributors' partial tiles are first added in piece
+// order 0, 1, ... (a fixed order, so the sum is reproducible bit for bit) by
+// all 128 epilogue threads, with up to kGatherLoads loads of each thread in
+// flight, into shared memory at kFinSumsOffset (the pipeline stages are free
+// by then): slot 0 holds the ticket tile, slot 1 its partner when tiles are
+// finished in pairs, each [chunk_rows][128] fp32.  The finisher then reads
+// the sums with take4.  The first kFinSumsOffset bytes stay the finisher's
+// own scratch.
+constexpr int kFinSumsOffset = 16 * 1024;
+constexpr int kGatherPieces = 4;   // pieces of one position loaded together
+constexpr int kGatherPos = 4;      // float4 positions of one thread loaded together
+
+extern __shared__ uint8_t sk_dyn_smem[];
+
+__device__ __forceinline__ float* fin_sums() {
+  return reinterpret_cast<float*>(align_smem_1024(sk_dyn_smem) + kFinSumsOffset);
+}
+
+// Shared memory the finishing phase needs beyond the alignment slack.
+inline int fin_smem_bytes(const GemmCore& g) {
+  return kFinSumsOffset + (g.pair_stride > 0 ? 2 : 1) * g.chunk_rows * 128 * 4;
+}
+
+// Sum the pieces of tile T (token chunk c) into sums slot `slot` (epilogue
+// threads et = 0..127).
+__device__ __forceinline__ void gather_tile(const GemmCore& g, int T, int slot, int et) {
+  const int c = T / g.out_tiles;
+  const int nt = min(g.chunk_rows, g.n_tok - c * g.chunk_rows);
+  const int n = static_cast<int>(tile_contributors(g, T));
+  const float4* src = reinterpret_cast<const float4*>(
+      g.part + static_cast<size_t>(T) * g.max_pieces * g.chunk_rows * 128);
+  const size_t stride = static_cast<size_t>(g.chunk_rows) * 32;  // float4s between pieces
+  float4* dst = reinterpret_cast<float4*>(fin_sums()) + slot * g.chunk_rows * 32;
+  const int n_pos = nt * 32;                                     // float4s of the tile
+  for (int q0 = et; q0 < n_pos; q0 += 128 * kGatherPos) {
+    float4 s[kGatherPos];
+    for (int i0 = 0; i0 < n; i0 += kGatherPieces) {
+      float4 v[kGatherPos][kGatherPieces];
+#pragma unroll
+      for (int a = 0; a < kGatherPos; ++a)
+#pragma unroll
+        for (int i = 0; i < kGatherPieces; ++i)
+          if (q0 + 128 * a < n_pos && i0 + i < n)
+            v[a][i] = __ldcg(src + (i0 + i) * stride + q0 + 128 * a);
+#pragma unroll
+      for (int a = 0; a < kGatherPos; ++a)
+#pragma unroll
+        for (int i = 0; i < kGatherPieces; ++i) {
+          if (i0 + i >= n) break;
+          if (i0 + i == 0) {
+            s[a] = v[a][0];
+          } else {
+            s[a].x += v[a][i].x;
+            s[a].y += v[a][i].y;
+            s[a].z += v[a][i].z;
+            s[a].w += v[a][i].w;
+          }
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < kGatherPos; ++a)
+      if (q0 + 128 * a < n_pos) dst[q0 + 128 * a] = s[a];
+  }
+}
+
+// The finished sums of 4 consecutive features f0..f0+3 (global feature index)
+// of token row `tok`, inside a finisher: slot 1 for the partner tile of a pair.
+__device__ __forceinline__ float4 take4(const GemmCore& g, int tok, int f0) {
+  const int r = tok % g.chunk_rows;
+  const int slot = (g.pair_stride > 0 && ((f0 >> 7) % g.out_tiles) >= g.pair_stride) ? 1 : 0;
+  return *reinterpret_cast<const float4*>(fin_sums() + (slot * g.chunk_rows + r) * 128 +
+                                          (f0 & 127));
 }
 
 template <class Fin>
@@ -258,9 +335,12 @@ streamk_gemm_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ 
       if (!*seg_ok) break;  // uniform over the four warps
       tc_fence_after();
       const uint32_t tacc = tmem_base + slot * p.tmem_cols + lane_base;
-      // partial sums go to the fp32 accumulator by fire-and-forget atomic adds
-      // at L2; the tile's finisher then needs one round trip
-      float* dst = p.acc + o * 128 + q * 32 + lane;
+      // this CTA's piece of the tile goes to its own slot: rank among the
+      // tile's contributors = this CTA's index - the first contributor's
+      const int piece = static_cast<int>(blockIdx.x) - unit_owner(p, T * KS);
+      float* dst = p.part +
+                   (static_cast<size_t>(T) * p.max_pieces + piece) * p.chunk_rows * 128 +
+                   q * 32 + lane;
       for (int c0 = 0; c0 < p.chunk_rows; c0 += 16) {
         uint32_t v[16], w[16];
         tmem_ld_32x32b_x16(tacc + c0, v);
@@ -268,10 +348,10 @@ streamk_gemm_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ 
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int tok = c * p.chunk_rows + c0 + j;
+          const int r = c0 + j;
           float val = __uint_as_float(v[j]);
           if (p.hilo) val += __uint_as_float(w[j]);
-          if (tok < p.n_tok) atomicAdd(dst + static_cast<size_t>(tok) * p.ld_out, val);
+          if (c * p.chunk_rows + r < p.n_tok) __stcg(dst + static_cast<size_t>(r) * 128, val);
         }
       }
       tc_fence_before();
@@ -299,6 +379,9 @@ streamk_gemm_kernel(const __grid_constant__ AMaps tm_a, const __grid_constant__ 
     for (int i = 0; i < nf; ++i) {
       const int T = fin_tiles[i];
       const int o = T % p.out_tiles, c = T / p.out_tiles;
+      gather_tile(p, T, 0, threadIdx.x - 64);
+      if (p.pair_stride > 0) gather_tile(p, T + p.pair_stride, 1, threadIdx.x - 64);
+      named_bar_sync(1, 128);
       Fin::finish(p, fp, o, c, smem);
       named_bar_sync(1, 128);  // scratch is reused by the next tile
       if (threadIdx.x == 64) p.tickets[T] = 0u;
@@ -348,15 +431,68 @@ inline int streamk_grid(const GemmCore& g, int ctas) {
   return grid;
 }
 
+// The shape fields of a GEMM of n_tok token rows, K = k_cols, out_tiles
+// tiles of 128 features: token chunks of up to 256 rows (128 with hilo, whose
+// MMA N is twice the chunk).  The launches and the workspace plans both start
+// from it.
+inline GemmCore gemm_dims(int n_tok, int k_cols, int out_tiles, int hilo) {
+  GemmCore g = {};
+  g.k_tiles = k_cols / 64;
+  g.out_tiles = out_tiles;
+  g.a_split[0] = g.a_split[1] = out_tiles;
+  g.layer_cols = k_cols;
+  g.n_tok = n_tok;
+  const int cap = hilo ? 128 : 256;
+  g.chunk_rows = n_tok < cap ? n_tok : cap;
+  g.n_chunks = (n_tok + g.chunk_rows - 1) / g.chunk_rows;
+  g.hilo = hilo;
+  g.mma_n = (1 + hilo) * g.chunk_rows;
+  return g;
+}
+
+// Partial-tile slots per tile: an upper bound on the CTAs that add a piece
+// to one tile, over every grid streamk_grid may choose on a device of nsm SMs
+// (any SM budget).  A CTA streams at least floor(U / G) units, so a tile of
+// KS consecutive units meets at most (KS - 1) / floor(U / G) + 2 CTAs; the
+// bound grows with G, whose largest value is max(min(nsm, U), streamk_grid(g, 1)).
+// The result depends on the shape fields of gemm_dims and on nsm only.
+inline int max_pieces(const GemmCore& shape, int nsm) {
+  GemmCore g = shape;
+  setup_gemm(g, (1 + g.hilo) * g.chunk_rows);
+  int gmax = nsm < g.n_units ? nsm : g.n_units;
+  const int gstar = streamk_grid(g, 1);
+  if (gstar > gmax) gmax = gstar;
+  const int per = g.n_units / gmax;
+  int m = (g.k_stages - 1) / per + 2;
+  if (m > g.k_stages) m = g.k_stages;
+  if (m > gmax) m = gmax;
+  return m;
+}
+
+// Bytes of the partial-tile buffer of a GEMM of this shape on nsm SMs.
+inline size_t partial_bytes(const GemmCore& shape, int nsm) {
+  return sizeof(float) * static_cast<size_t>(shape.out_tiles) * shape.n_chunks *
+         max_pieces(shape, nsm) * shape.chunk_rows * 128;
+}
+
 // Launch one stream-K GEMM with finisher Fin on at most `ctas` CTAs (fills
-// the pipeline fields of g).
+// the pipeline fields of g; the token tile of a stage holds (1 + hilo) *
+// chunk_rows rows).  g.part must hold partial_bytes(g, SM count) bytes
+// (part_cap, else DFLASH_E_WORKSPACE).
 template <class Fin>
-inline int run_streamk(GemmCore& g, int b_rows_per_stage, const AMaps& a, const BMaps& b,
-                       const typename Fin::Params& fp, int ctas, cudaStream_t st) {
-  const int smem = setup_gemm(g, b_rows_per_stage);
+inline int run_streamk(GemmCore& g, const AMaps& a, const BMaps& b,
+                       const typename Fin::Params& fp, int ctas, cudaStream_t st,
+                       size_t part_cap) {
+  const int nsm = current_num_sms();
+  if (nsm <= 0) return DFLASH_E_CUDA;
+  if (partial_bytes(g, nsm) > part_cap) return DFLASH_E_WORKSPACE;
+  g.max_pieces = max_pieces(g, nsm);
+  const int smem = setup_gemm(g, (1 + g.hilo) * g.chunk_rows);
+  // the finisher's sums reuse the stage area, below the barriers
+  if (fin_smem_bytes(g) > g.n_stages * g.stage_bytes) return DFLASH_E_UNSUPPORTED;
   int rc = set_smem_limit(reinterpret_cast<const void*>(streamk_gemm_kernel<Fin>), smem);
   if (rc) return rc;
-  const int grid = streamk_grid(g, ctas);
+  const int grid = streamk_grid(g, ctas < nsm ? ctas : nsm);
   return launch(streamk_gemm_kernel<Fin>, dim3(grid), dim3(kGemmThreads), smem, st, a, b, g, fp);
 }
 

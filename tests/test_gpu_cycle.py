@@ -205,7 +205,11 @@ def test_cycle_graph_matches_direct_calls():
     assert np.array_equal(host_out[2].numpy(), a.commit_len.cpu().numpy())
     assert np.array_equal(b.out_tokens.cpu().numpy(), a.out_tokens.cpu().numpy())
     assert np.array_equal(b.draft_cache.seq_len.cpu().numpy(), a.draft_cache.seq_len.cpu().numpy())
-    np.testing.assert_allclose(host_f64(b.attn_out), host_f64(a.attn_out), atol=2e-2)
+    # the projection adds its CTAs' partial sums in a fixed order and the
+    # attention merges its splits in a fixed order: same inputs, same bits
+    for x, y in ((b.attn_out, a.attn_out), (b.draft_cache.k, a.draft_cache.k),
+                 (b.draft_cache.v, a.draft_cache.v)):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
 
 
 def test_pipelined_cycles_match_direct_calls():
@@ -295,4 +299,6 @@ def test_pipelined_cycles_match_direct_calls():
     assert np.array_equal(b0.out_tokens.cpu().numpy(), a.out_tokens.cpu().numpy())
     assert np.array_equal(b0.draft_cache.seq_len.cpu().numpy(),
                           a.draft_cache.seq_len.cpu().numpy())
-    np.testing.assert_allclose(host_f64(b0.attn_out), host_f64(a.attn_out), atol=2e-2)
+    for x, y in ((b0.attn_out, a.attn_out), (b0.draft_cache.k, a.draft_cache.k),
+                 (b0.draft_cache.v, a.draft_cache.v)):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
