@@ -29,6 +29,15 @@
 // The split that owns the tail also folds in the 16 block keys (a 16-key
 // chunk).  Partial (O, max, sum) go to the workspace and a second kernel
 // merges the splits by log-sum-exp.
+//
+// The same kernel serves the target's attention: the verify forward (causal
+// inside the block, the block's K/V appended to the cache) and the prefill
+// of a prompt chunk of T rows.  A chunk is cut into 16-row sub-blocks; its
+// rotated K and its V are first appended to the cache, then sub-block j (at
+// positions L + 16 j ..) is a causal block whose context is the cache rows
+// 0 .. L + 16 j - 1, which is causal attention over the whole chunk.  The
+// grid's z index runs over (sequence, sub-block) with the longest contexts
+// first, and with a single split the kernel writes the bf16 output itself.
 #include <type_traits>
 
 #include "common.cuh"
@@ -49,6 +58,11 @@ constexpr float kRescaleLog2 = 8.0f;
 struct AttnParams {
   int batch, n_q_heads, n_kv_heads, group, splits, rows;  // rows R = group * 16
   int paged, capacity, max_pages;
+  // block rows: q/k/v row b * tokens + 16 j + i for sub-block j of sequence
+  // b (tokens = 16, sub_blocks = 1 for a single block); a sequence is valid
+  // when 0 <= seq_len[b] and seq_len[b] + need_rows fits the cache
+  int tokens, sub_blocks, need_rows;
+  uint16_t* out_direct;  // splits == 1: bf16 output [B * tokens, Hq, D] written here
   const int32_t* seq_len;
   const int32_t* page_table;
   const uint16_t* q_blk;
@@ -70,6 +84,7 @@ struct AttnParams {
 
 struct CombineParams {
   int batch, n_q_heads, n_kv_heads, group, splits, rows, head_dim, limit;
+  int tokens, sub_blocks, need_rows;
   const int32_t* seq_len;
   const float* part_o;
   const float* part_ml;
@@ -165,7 +180,12 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
-  const int s_idx = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int s_idx = blockIdx.x, g = blockIdx.y;
+  // (sequence, sub-block): the last sub-block, with the longest context, first
+  const int b = blockIdx.z / p.sub_blocks;
+  const int jsub = p.sub_blocks - 1 - (static_cast<int>(blockIdx.z) - b * p.sub_blocks);
+  const int row0 = b * p.tokens + jsub * kBlock;      // first block row in q/k/v
+  const int n_rows = min(kBlock, p.tokens - jsub * kBlock);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -203,11 +223,12 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
   const uint32_t tmem_base = *tmem_slot;
   griddep_wait();
 
-  const int L = p.seq_len[b];
+  const int L0 = p.seq_len[b];
   const int limit = p.paged ? p.max_pages * kPage : p.capacity;
-  const bool valid_len = L >= 0 && L <= limit;
-  if (!valid_len && threadIdx.x == 0 && s_idx == 0 && g == 0)
+  const bool valid_len = L0 >= 0 && L0 + p.need_rows <= limit;
+  if (!valid_len && threadIdx.x == 0 && s_idx == 0 && g == 0 && jsub == 0)
     set_status(p.status, DFLASH_ST_CAPACITY);
+  const int L = L0 + jsub * kBlock;             // context rows of this sub-block
   const int Lc = valid_len ? L : 0;
   const int n_pg = (Lc + kPage - 1) / kPage;
   const int pps = (n_pg + p.splits - 1) / p.splits;
@@ -378,10 +399,14 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
         if (it < q_items) {
           const int rr = it / kPer, d0 = (it - rr * kPer) * 8;
           const int w = rr >> 4, i = rr & 15;
-          const size_t src =
-              (static_cast<size_t>(b * kBlock + i) * p.n_q_heads + g * G + w) * D + d0;
-          x1[u] = *reinterpret_cast<const uint4*>(p.q_blk + src);
-          x2[u] = *reinterpret_cast<const uint4*>(p.q_blk + src + D / 2);
+          if (i < n_rows) {
+            const size_t src =
+                (static_cast<size_t>(row0 + i) * p.n_q_heads + g * G + w) * D + d0;
+            x1[u] = *reinterpret_cast<const uint4*>(p.q_blk + src);
+            x2[u] = *reinterpret_cast<const uint4*>(p.q_blk + src + D / 2);
+          } else {                               // past the chunk: a zero query row
+            x1[u] = x2[u] = make_uint4(0, 0, 0, 0);
+          }
         }
       }
       // (cos, sin) of the 16 block positions L + i, i < 16, for every frequency
@@ -412,11 +437,15 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
       if (has_block) {
         for (int it = tid; it < kPage * kPer; it += 256) {
           const int j = it / kPer, d0 = (it - j * kPer) * 8;
-          const size_t src = (static_cast<size_t>(b * kBlock + j) * p.n_kv_heads + g) * D + d0;
-          const uint4 k1 = *reinterpret_cast<const uint4*>(p.k_blk + src);
-          const uint4 k2 = *reinterpret_cast<const uint4*>(p.k_blk + src + D / 2);
-          const uint4 v1 = *reinterpret_cast<const uint4*>(p.v_blk + src);
-          const uint4 v2 = *reinterpret_cast<const uint4*>(p.v_blk + src + D / 2);
+          // rows past the chunk are zero keys that the causal mask hides from
+          // every row of the chunk
+          const bool in = j < n_rows;
+          const size_t src = (static_cast<size_t>(row0 + (in ? j : 0)) * p.n_kv_heads + g) * D + d0;
+          const uint4 zero = make_uint4(0, 0, 0, 0);
+          const uint4 k1 = in ? *reinterpret_cast<const uint4*>(p.k_blk + src) : zero;
+          const uint4 k2 = in ? *reinterpret_cast<const uint4*>(p.k_blk + src + D / 2) : zero;
+          const uint4 v1 = in ? *reinterpret_cast<const uint4*>(p.v_blk + src) : zero;
+          const uint4 v2 = in ? *reinterpret_cast<const uint4*>(p.v_blk + src + D / 2) : zero;
           uint4 y1, y2;
           rope8(k1, k2, sct + j * (D / 2), d0, y1, y2);
           const int e2 = d0 + D / 2;
@@ -579,7 +608,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
     if (grp == 1 && writer) ml_odd[m] = make_float2(ok ? m_run : -INFINITY, ok ? l_run : 0.f);
     named_bar_sync(2, 256);
     if (grp == 0) {
-      const size_t unit = (static_cast<size_t>(b) * p.n_kv_heads + g) * p.splits + s_idx;
+      // partials of grid unit (z, KV head, split): z = (sequence, sub-block)
+      const size_t unit = (static_cast<size_t>(blockIdx.z) * p.n_kv_heads + g) * p.splits + s_idx;
       float* po = p.part_o + (unit * R + rr) * D;
       float* pml = p.part_ml + (unit * R + rr) * 2;
       bool have_o = ok && n_total > 0;
@@ -595,6 +625,15 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
         wb = ob.x == -INFINITY ? 0.f : fast_exp2(ob.x - M);
         l_tot = wa * l_run + wb * ob.y;
       }
+      // single split: the normalised bf16 row goes straight to the output
+      // (row i of query head g * G + w), rows past the chunk are dropped
+      const int wq = rr >> 4, iq = rr & 15;
+      uint16_t* od = p.out_direct
+                         ? p.out_direct +
+                               (static_cast<size_t>(row0 + iq) * p.n_q_heads + g * G + wq) * D
+                         : nullptr;
+      const bool direct_row = od != nullptr && iq < n_rows && valid_len;
+      const float inv_l = 1.f / l_tot;
       if (have_o) {
         tc_fence_after();
 #pragma unroll 1
@@ -609,18 +648,28 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
             for (int e = 0; e < 16; ++e)
               o[e] = odd_used ? wa * __uint_as_float(oa[e]) + wb * __uint_as_float(ob[e])
                               : __uint_as_float(oa[e]);
+            if (od) {
+              if (direct_row) {
+                uint32_t pk[8];
 #pragma unroll
-            for (int e = 0; e < 16; e += 4)
-              *reinterpret_cast<float4*>(po + c16 * 16 + e) =
-                  make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                for (int e = 0; e < 16; e += 2) pk[e >> 1] = pack_bf16(o[e] * inv_l, o[e + 1] * inv_l);
+                *reinterpret_cast<uint4*>(od + c16 * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4*>(od + c16 * 16 + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < 16; e += 4)
+                *reinterpret_cast<float4*>(po + c16 * 16 + e) =
+                    make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+            }
           }
         }
-      } else if (writer) {
+      } else if (writer && !od) {
         for (int e = 0; e < D; e += 4) *reinterpret_cast<float4*>(po + e) = make_float4(0.f, 0.f, 0.f, 0.f);
         M = -INFINITY;
         l_tot = 0.f;
       }
-      if (writer) *reinterpret_cast<float2*>(pml) = make_float2(M, l_tot);
+      if (writer && !od) *reinterpret_cast<float2*>(pml) = make_float2(M, l_tot);
     }
   }
   griddep_launch_dependents();
@@ -649,16 +698,20 @@ __global__ void __launch_bounds__(32 * kCombineRows) attn_combine_kernel(const C
   using Vec = typename std::conditional<per == 4, float4, float2>::type;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * kCombineRows + warp;
-  const int rows_out = p.batch * kBlock * p.n_q_heads;
+  const int rows_out = p.batch * p.tokens * p.n_q_heads;
   if (row >= rows_out) return;
-  const int b = row / (kBlock * p.n_q_heads);
-  const int rem = row - b * kBlock * p.n_q_heads;
-  const int i = rem / p.n_q_heads;
-  const int h = rem - i * p.n_q_heads;
+  // output row (b, t, h): block row i = t % 16 of sub-block j = t / 16, whose
+  // grid index z runs the sub-blocks of a sequence last to first
+  const int b = row / (p.tokens * p.n_q_heads);
+  const int rem = row - b * p.tokens * p.n_q_heads;
+  const int t = rem / p.n_q_heads;
+  const int h = rem - t * p.n_q_heads;
+  const int i = t & (kBlock - 1);
+  const int z = b * p.sub_blocks + (p.sub_blocks - 1 - t / kBlock);
   const int g = h / p.group, w = h - g * p.group;
   const int rr = w * kBlock + i;
-  const size_t unit0 = (static_cast<size_t>(b) * p.n_kv_heads + g) * p.splits;
-  const int L = p.seq_len[b];
+  const size_t unit0 = (static_cast<size_t>(z) * p.n_kv_heads + g) * p.splits;
+  const int L0 = p.seq_len[b];
   float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
   if (lane < p.splits) {
     const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + ((unit0 + lane) * p.rows + rr) * 2);
@@ -677,7 +730,7 @@ __global__ void __launch_bounds__(32 * kCombineRows) attn_combine_kernel(const C
 #pragma unroll
   for (int k = 0; k < kBatch; ++k)
     if (k < p.splits) v[k] = *reinterpret_cast<const Vec*>(base + k * stride);
-  if (L < 0 || L > p.limit) return;
+  if (L0 < 0 || L0 + p.need_rows > p.limit) return;
   float M = fmaxf(m0, m1);
 #pragma unroll
   for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -747,33 +800,96 @@ int plan_attention_smem(AttnParams& p) {
   return attention_smem_for<D>(p, 2);
 }
 
-// The target's verify attention appends the block at rows L .. L + 15: map
-// the pages those rows need before the attention writes them, and move the
-// length past them once every kernel that reads L has finished.
-__global__ void append_reserve_kernel(const dflash_kv_view v, int batch, uint32_t* status) {
+// The target's attention appends n rows at L .. L + n - 1 (16 for the verify
+// forward, a prompt chunk for the prefill): map the pages those rows need
+// before anything writes them, and move the length past them once every
+// kernel that reads L has finished.
+__global__ void append_reserve_kernel(const dflash_kv_view v, int batch, int n,
+                                      uint32_t* status) {
   griddep_wait();
   griddep_launch_dependents();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
   const int L = v.seq_len[b];
   const int limit = v.max_pages * v.page_size;
-  if (L >= 0 && L + kBlock <= limit) map_rows(v, b, L, kBlock, status);
+  if (L >= 0 && L + n <= limit) map_rows(v, b, L, n, status);
 }
 
-__global__ void append_length_kernel(int32_t* seq_len, int batch, int limit, uint32_t* status) {
+__global__ void append_length_kernel(int32_t* seq_len, int batch, int n, int limit,
+                                     uint32_t* status) {
   griddep_wait();
   griddep_launch_dependents();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= batch) return;
   const int L = seq_len[b];
-  if (L >= 0 && L + kBlock <= limit)
-    seq_len[b] = L + kBlock;
+  if (L >= 0 && L + n <= limit)
+    seq_len[b] = L + n;
   else
     set_status(status, DFLASH_ST_CAPACITY);
 }
 
+// Prefill: the chunk's K rotated at L + t and its V, for every row t < T and
+// KV head, written into the cache rows L + t before the attention reads them
+// (the rotation is the one the attention applies to a block's keys).  One
+// thread per (row, KV head, 8-dim item of the first half of the head).
 template <int D>
-int launch_attention(const dflash_dims& dims, const Plan& plan, const dflash_kv_view& cache,
+__global__ void __launch_bounds__(256) prefill_append_kernel(const dflash_kv_view v,
+                                                             const uint16_t* __restrict__ k,
+                                                             const uint16_t* __restrict__ vv,
+                                                             int batch, int tokens, int n_kv_heads,
+                                                             const RopeTable rope,
+                                                             uint32_t* status) {
+  griddep_wait();
+  constexpr int kItems = D / 16;                     // items of 8 dims per half head
+  const long long it = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(batch) * tokens * n_kv_heads * kItems;
+  if (it < total) {
+    const int item = static_cast<int>(it % kItems);
+    const long long rg = it / kItems;                // (b * T + t) * Hkv + g
+    const int g = static_cast<int>(rg % n_kv_heads);
+    const long long bt = rg / n_kv_heads;
+    const int b = static_cast<int>(bt / tokens), t = static_cast<int>(bt % tokens);
+    const int L = v.seq_len[b];
+    const int limit = v.page_table ? v.max_pages * v.page_size : v.capacity;
+    if (L >= 0 && L + tokens <= limit) {
+      const int pos = L + t;
+      long long row = -1;
+      if (v.page_table) {
+        const int id = v.page_table[static_cast<size_t>(b) * v.max_pages + pos / kPage];
+        if (id >= 0)
+          row = (static_cast<long long>(id) * n_kv_heads + g) * kPage + pos % kPage;
+        else
+          set_status(status, DFLASH_ST_PAGE_MISSING);
+      } else {
+        row = (static_cast<long long>(b) * n_kv_heads + g) * v.capacity + pos;
+      }
+      if (row >= 0) {
+        const int d0 = item * 8, e2 = d0 + D / 2;
+        const size_t src = static_cast<size_t>(rg) * D;
+        float2 sc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float sn, cs;
+          rope_sincos(pos, rope.hi[d0 + e], rope.lo[d0 + e], &sn, &cs);
+          sc[e] = make_float2(cs, sn);
+        }
+        uint4 y1, y2;
+        rope8(*reinterpret_cast<const uint4*>(k + src + d0),
+              *reinterpret_cast<const uint4*>(k + src + e2), sc, 0, y1, y2);
+        uint16_t* kd = static_cast<uint16_t*>(v.k) + row * D;
+        uint16_t* vd = static_cast<uint16_t*>(v.v) + row * D;
+        *reinterpret_cast<uint4*>(kd + d0) = y1;
+        *reinterpret_cast<uint4*>(kd + e2) = y2;
+        *reinterpret_cast<uint4*>(vd + d0) = *reinterpret_cast<const uint4*>(vv + src + d0);
+        *reinterpret_cast<uint4*>(vd + e2) = *reinterpret_cast<const uint4*>(vv + src + e2);
+      }
+    }
+  }
+  griddep_launch_dependents();
+}
+
+template <int D>
+int launch_attention(const dflash_dims& dims, int splits, const dflash_kv_view& cache,
                      AttnParams& p, CombineParams& cp, cudaStream_t stream) {
   using C = Cfg<D>;
   // head-major caches: contiguous [B, Hkv, cap, D] is a stack of (sequence,
@@ -811,15 +927,20 @@ int launch_attention(const dflash_dims& dims, const Plan& plan, const dflash_kv_
   // query rows are doubled across the TMEM lanes when they fill at most half
   auto kernel = p.rows <= 64 ? block_attention_kernel<D, true> : block_attention_kernel<D, false>;
   if ((rc = set_smem_limit(reinterpret_cast<const void*>(kernel), smem))) return rc;
-  rc = launch(kernel, dim3(plan.att_splits, dims.n_kv_heads, dims.batch), dim3(kAttThreads), smem,
-              stream, tm_k, tm_v, tm_k64, tm_v64, p);
+  rc = launch(kernel, dim3(splits, dims.n_kv_heads, dims.batch * p.sub_blocks),
+              dim3(kAttThreads), smem, stream, tm_k, tm_v, tm_k64, tm_v64, p);
   if (rc) return rc;
-  const int rows_out = dims.batch * kBlock * dims.n_q_heads;
-  rc = launch(attn_combine_kernel<D>, dim3((rows_out + kCombineRows - 1) / kCombineRows),
-              dim3(32 * kCombineRows), 0, stream, cp);
-  if (rc || !p.k_app) return rc;
+  if (!p.out_direct) {
+    const long long rows_out = static_cast<long long>(dims.batch) * p.tokens * dims.n_q_heads;
+    rc = launch(attn_combine_kernel<D>,
+                dim3(static_cast<unsigned>((rows_out + kCombineRows - 1) / kCombineRows)),
+                dim3(32 * kCombineRows), 0, stream, cp);
+    if (rc) return rc;
+  }
+  if (!p.k_app && p.need_rows == 0) return DFLASH_OK;
+  // the verify forward's block, or the prefill chunk, is now part of the cache
   return launch(append_length_kernel, dim3((dims.batch + 127) / 128), dim3(128), 0, stream,
-                cache.seq_len, dims.batch, cp.limit, p.status);
+                cache.seq_len, dims.batch, p.k_app ? kBlock : p.tokens, cp.limit, p.status);
 }
 
 }  // namespace
@@ -853,6 +974,9 @@ int run_attention(const dflash_dims* dims, const void* q_blk, const void* k_blk,
   if (ws_bytes < plan.total) return DFLASH_E_WORKSPACE;
 
   AttnParams p = {};
+  p.tokens = kBlock;
+  p.sub_blocks = 1;
+  p.need_rows = 0;
   p.batch = dims->batch;
   p.n_q_heads = dims->n_q_heads;
   p.n_kv_heads = dims->n_kv_heads;
@@ -874,6 +998,9 @@ int run_attention(const dflash_dims* dims, const void* q_blk, const void* k_blk,
   fill_rope_table(p.rope.hi, p.rope.lo, dims->head_dim, dims->rope_theta);
 
   CombineParams cp = {};
+  cp.tokens = kBlock;
+  cp.sub_blocks = 1;
+  cp.need_rows = 0;
   cp.batch = dims->batch;
   cp.n_q_heads = dims->n_q_heads;
   cp.n_kv_heads = dims->n_kv_heads;
@@ -894,14 +1021,156 @@ int run_attention(const dflash_dims* dims, const void* q_blk, const void* k_blk,
     p.v_app = static_cast<uint16_t*>(cache->v);
     if (paged && (!cache->free_list || !cache->free_count)) return DFLASH_E_ARG;
     if (paged && (rc = launch(append_reserve_kernel, dim3((dims->batch + 127) / 128), dim3(128),
-                              0, s, *cache, dims->batch, p.status)))
+                              0, s, *cache, dims->batch, kBlock, p.status)))
       return rc;
   }
-  return dims->head_dim == 128 ? launch_attention<128>(*dims, plan, *cache, p, cp, s)
-                               : launch_attention<64>(*dims, plan, *cache, p, cp, s);
+  return dims->head_dim == 128 ? launch_attention<128>(*dims, plan.att_splits, *cache, p, cp, s)
+                               : launch_attention<64>(*dims, plan.att_splits, *cache, p, cp, s);
 }
 
 }  // namespace
+
+namespace dflash {
+
+// Workspace of dflash_prefill_attention: the status word, then the split
+// partials when a chunk's (sequence, sub-block, KV head) units are too few to
+// fill the device with one split each.
+struct PrefillAttnPlan {
+  int sub_blocks, splits, rows;
+  size_t off_status, off_o, off_ml, total;
+};
+
+int make_prefill_attn_plan(const dflash_dims& d, int tokens, PrefillAttnPlan* out) {
+  int rc = check_dims(&d);
+  if (rc) return rc;
+  if (tokens < 1) return DFLASH_E_ARG;
+  PrefillAttnPlan q = {};
+  q.sub_blocks = (tokens + kBlock - 1) / kBlock;
+  if (static_cast<long long>(d.batch) * q.sub_blocks > 65535) return DFLASH_E_UNSUPPORTED;
+  // splits: enough (sequence, sub-block, KV head, split) CTAs for one per
+  // SM of the GB300 (152); fixed rather than read from the device, so that
+  // the workspace size is a function of the shapes alone
+  constexpr int kFillCtas = 152;
+  const long long units = static_cast<long long>(d.batch) * q.sub_blocks * d.n_kv_heads;
+  int s = units >= kFillCtas ? 1 : static_cast<int>((kFillCtas + units - 1) / units);
+  const int pages = (d.max_ctx + kPage - 1) / kPage;
+  if (s > pages) s = pages;
+  if (s > kMaxAttSplits) s = kMaxAttSplits;
+  if (s < 1) s = 1;
+  q.splits = s;
+  q.rows = (d.n_q_heads / d.n_kv_heads) * kBlock;
+  size_t off = 256;  // status word at 0
+  q.off_status = 0;
+  if (s > 1) {
+    const size_t n = static_cast<size_t>(units) * s * q.rows;
+    q.off_o = off;
+    off += sizeof(float) * n * d.head_dim;
+    q.off_ml = off;
+    off += sizeof(float) * 2 * n;
+  }
+  q.total = (off + 255) & ~static_cast<size_t>(255);
+  *out = q;
+  return DFLASH_OK;
+}
+
+size_t prefill_attention_workspace(const dflash_dims& d, int tokens_per_seq) {
+  PrefillAttnPlan p;
+  return make_prefill_attn_plan(d, tokens_per_seq, &p) ? 0 : p.total;
+}
+
+}  // namespace dflash
+
+extern "C" int dflash_prefill_attention(const dflash_dims* dims, int32_t tokens_per_seq,
+                                        const void* q, const void* k, const void* v,
+                                        const dflash_kv_view* cache, float scale, void* out,
+                                        void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  DFLASH_ENTRY("dflash_prefill_attention");
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  PrefillAttnPlan plan;
+  if ((rc = make_prefill_attn_plan(*dims, tokens_per_seq, &plan))) return rc;
+  if (!q || !k || !v || !cache || !out || !cache->k || !cache->v || !cache->seq_len)
+    return DFLASH_E_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      !aligned16(cache->k) || !aligned16(cache->v))
+    return DFLASH_E_ALIGN;
+  if (!(scale > 0.0f)) return DFLASH_E_ARG;
+  const bool paged = cache->page_table != nullptr;
+  if (paged) {
+    if (cache->page_size != 16) return DFLASH_E_UNSUPPORTED;
+    if (cache->max_pages < 1 || cache->n_pages < 1 || !cache->free_list || !cache->free_count)
+      return DFLASH_E_ARG;
+  } else if (cache->capacity < 1) {
+    return DFLASH_E_ARG;
+  }
+  if (!ws) return DFLASH_E_WORKSPACE;
+  if (ws_bytes < plan.total) return DFLASH_E_WORKSPACE;
+  const int T = tokens_per_seq;
+
+  AttnParams p = {};
+  p.batch = dims->batch;
+  p.n_q_heads = dims->n_q_heads;
+  p.n_kv_heads = dims->n_kv_heads;
+  p.group = dims->n_q_heads / dims->n_kv_heads;
+  p.splits = plan.splits;
+  p.rows = plan.rows;
+  p.paged = paged ? 1 : 0;
+  p.capacity = cache->capacity;
+  p.max_pages = cache->max_pages;
+  p.seq_len = cache->seq_len;
+  p.page_table = cache->page_table;
+  p.q_blk = static_cast<const uint16_t*>(q);
+  p.k_blk = static_cast<const uint16_t*>(k);
+  p.v_blk = static_cast<const uint16_t*>(v);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = ws_at<uint32_t>(ws, plan.off_status);
+  p.causal = 1;
+  p.tokens = T;
+  p.sub_blocks = plan.sub_blocks;
+  p.need_rows = T;
+  if (plan.splits > 1) {
+    p.part_o = ws_at<float>(ws, plan.off_o);
+    p.part_ml = ws_at<float>(ws, plan.off_ml);
+  } else {
+    p.out_direct = static_cast<uint16_t*>(out);
+  }
+  fill_rope_table(p.rope.hi, p.rope.lo, dims->head_dim, dims->rope_theta);
+
+  CombineParams cp = {};
+  cp.batch = dims->batch;
+  cp.n_q_heads = dims->n_q_heads;
+  cp.n_kv_heads = dims->n_kv_heads;
+  cp.group = p.group;
+  cp.splits = p.splits;
+  cp.rows = p.rows;
+  cp.head_dim = dims->head_dim;
+  cp.limit = paged ? cache->max_pages * 16 : cache->capacity;
+  cp.tokens = T;
+  cp.sub_blocks = plan.sub_blocks;
+  cp.need_rows = T;
+  cp.seq_len = cache->seq_len;
+  cp.part_o = p.part_o;
+  cp.part_ml = p.part_ml;
+  cp.out = static_cast<uint16_t*>(out);
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // 1. pages for the chunk's rows; 2. the chunk's rotated K and V into the
+  // cache; 3. causal attention of its sub-blocks; 4. the length
+  if (paged && (rc = launch(append_reserve_kernel, dim3((dims->batch + 127) / 128), dim3(128), 0,
+                            s, *cache, dims->batch, T, p.status)))
+    return rc;
+  const long long items =
+      static_cast<long long>(dims->batch) * T * dims->n_kv_heads * (dims->head_dim / 16);
+  const dim3 agrid(static_cast<unsigned>((items + 255) / 256));
+  rc = dims->head_dim == 128
+           ? launch(prefill_append_kernel<128>, agrid, dim3(256), 0, s, *cache, p.k_blk, p.v_blk,
+                    dims->batch, T, dims->n_kv_heads, p.rope, p.status)
+           : launch(prefill_append_kernel<64>, agrid, dim3(256), 0, s, *cache, p.k_blk, p.v_blk,
+                    dims->batch, T, dims->n_kv_heads, p.rope, p.status);
+  if (rc) return rc;
+  return dims->head_dim == 128 ? launch_attention<128>(*dims, plan.splits, *cache, p, cp, s)
+                               : launch_attention<64>(*dims, plan.splits, *cache, p, cp, s);
+}
 
 extern "C" int dflash_block_attention(const dflash_dims* dims, const void* q_blk,
                                       const void* k_blk, const void* v_blk,

@@ -121,6 +121,10 @@ int tiled_projection(const dflash_dims& d, int tokens_per_seq, const void* const
                      float* ss, uint16_t* yhat, uint16_t* yhat_lo, int max_ctas,
                      cudaStream_t st);
 
+// Workspace bytes of dflash_prefill_attention for this chunk length (0 on bad
+// arguments); dflash_prefill_workspace_bytes covers it.
+size_t prefill_attention_workspace(const dflash_dims& d, int tokens_per_seq);
+
 // Raise the dynamic shared-memory limit of a kernel once per device.
 int set_smem_limit(const void* func, int bytes);
 

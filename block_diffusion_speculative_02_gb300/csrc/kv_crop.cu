@@ -48,11 +48,14 @@ __global__ void kv_crop_kernel(const CropViews views, const int32_t* __restrict_
       const int slot = atomicAdd(v.free_count, 1);
       if (slot < v.n_pages) {
         v.free_list[slot] = page;
+        row[pg] = -1;
       } else {
+        // the free list is already full (the pool's pages were counted twice
+        // somewhere): the page stays mapped to this sequence, which reuses it
+        // when it grows again, so no page is lost
         atomicSub(v.free_count, 1);
         set_status(status, DFLASH_ST_CAPACITY);
       }
-      row[pg] = -1;
     }
   }
   v.seq_len[b] = nl;

@@ -22,6 +22,7 @@
 //
 // Warp roles (192 threads): warp 0 issues TMA, warp 1 owns TMEM and issues the
 // MMAs, warps 2-5 drain the accumulators.
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -76,8 +77,9 @@ struct LmParams {
   int32_t* commit_len;
   int32_t* out_tokens;
   int out_cap;
-  // drafting (dflash_draft_tokens): the argmaxes become the next block instead
-  // of being checked against one
+  // drafting (dflash_draft_tokens, draft = 1): the argmaxes become the next
+  // block instead of being checked against one; the prefill's staged token
+  // (dflash_prefill_staged, draft = 2): one row per sequence, its argmax
   int draft;
   const int32_t* staged;                 // [B] token for block position 0, or null
   int32_t* block_out;                    // [B, 16]
@@ -132,6 +134,22 @@ __device__ __forceinline__ void write_draft(const LmParams& p, int b) {
     if (i > 0) p.block_out[b * kBlock + i] = t;
   }
   if (p.staged) p.block_out[b * kBlock] = p.staged[b];
+}
+
+// The prefill's staged token ("dflash-mlx" 单次前向验证 ②): the argmax of
+// sequence b's single row.
+__device__ __forceinline__ void write_staged(const LmParams& p, int b) {
+  const unsigned long long k = __ldcg(&p.keys[b]);
+  p.block_out[b] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
+}
+
+__device__ __forceinline__ void finish_sequence(const LmParams& p, int b) {
+  if (p.draft == 2)
+    write_staged(p, b);
+  else if (p.draft)
+    write_draft(p, b);
+  else
+    accept_and_commit(p, b);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -359,9 +377,7 @@ lmhead_argmax_accept_kernel(const __grid_constant__ CUtensorMap tm_w,
     named_bar_sync(1, 128);
     if (*last_flag) {
       __threadfence();
-      for (int b = et; b < p.batch; b += 128) {
-        if (p.draft) write_draft(p, b); else accept_and_commit(p, b);
-      }
+      for (int b = et; b < p.batch; b += 128) finish_sequence(p, b);
       named_bar_sync(1, 128);
       for (int i = et; i < p.ntok; i += 128) p.keys[i] = 0ull;
       if (et == 0) *p.ticket = 0u;
@@ -418,7 +434,7 @@ __global__ void lm_finish_kernel(const LmParams p) {
   griddep_launch_dependents();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= p.batch) return;
-  if (p.draft) write_draft(p, b); else accept_and_commit(p, b);
+  finish_sequence(p, b);
   for (int i = 0; i < kBlock; ++i) p.keys[b * kBlock + i] = 0ull;
 }
 
@@ -450,14 +466,17 @@ int launch_lmhead_wide(const dflash_dims& d, int budget_sms, const void* hidden,
 }  // namespace
 
 // Pipeline shape, tensor maps and launch of the LM-head kernel for `p` (whose
-// workspace pointers and per-call outputs the caller has set).
+// workspace pointers and per-call outputs the caller has set).  Token rows:
+// 16 per sequence, or -- x_rows > 0 -- x_rows rows x_pitch bytes apart (the
+// MMA then takes them rounded up to 16, the rows past x_rows read as zeros).
 int launch_lmhead(const dflash_dims& d, int budget_sms, const void* hidden, const void* w_lm,
-                  LmParams& p, cudaStream_t st) {
+                  LmParams& p, cudaStream_t st, int x_rows = 0, uint64_t x_pitch = 0) {
   p.vocab = d.vocab;
   p.hidden = d.hidden;
-  p.ntok = d.batch * kBlock;
+  p.ntok = x_rows > 0 ? (x_rows + 15) / 16 * 16 : d.batch * kBlock;
   p.batch = d.batch;
-  if (p.ntok >= kWideMinRows) return launch_lmhead_wide(d, budget_sms, hidden, w_lm, p, st);
+  if (x_rows == 0 && p.ntok >= kWideMinRows)
+    return launch_lmhead_wide(d, budget_sms, hidden, w_lm, p, st);
   p.ntok_box = p.ntok <= 256 ? p.ntok : 256;
   p.n_xbox = (p.ntok + p.ntok_box - 1) / p.ntok_box;
   p.n_units = (p.vocab + kUnitRows - 1) / kUnitRows;
@@ -484,7 +503,9 @@ int launch_lmhead(const dflash_dims& d, int budget_sms, const void* hidden, cons
   for (int bi = 0; bi < 4; ++bi)
     if ((rc = make_tmap_2d_bf16(&tm_part.m[bi], w_lm, d.hidden, d.vocab, pitch, 64, 64 >> bi)))
       return rc;
-  if ((rc = make_tmap_2d_bf16(&tm_x, hidden, d.hidden, p.ntok, pitch, 64, p.ntok_box))) return rc;
+  if ((rc = make_tmap_2d_bf16(&tm_x, hidden, d.hidden, x_rows > 0 ? x_rows : p.ntok,
+                              x_rows > 0 ? x_pitch : pitch, 64, p.ntok_box)))
+    return rc;
   const int smem = p.n_stages * (p.stage_bytes + 16) + fixed;
   if ((rc = set_smem_limit(reinterpret_cast<const void*>(lmhead_argmax_accept_kernel), smem)))
     return rc;
@@ -549,6 +570,8 @@ namespace dflash {
 namespace {
 
 constexpr int kNoAllocMaxTokens = 512;   // batch * 16 at most (batch <= 32)
+// every batch that check_dims accepts fits the array
+static_assert(kNoAllocMaxTokens >= kMaxTokens, "the scratch array must cover every batch");
 constexpr size_t kNoAllocKeyBytes = sizeof(unsigned long long) * kNoAllocMaxTokens;
 constexpr size_t kNoAllocBytes = kNoAllocKeyBytes + 256;  // keys, then ticket and status
 
@@ -557,23 +580,28 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+std::atomic<void*> g_noalloc_addr[kNoAllocMaxDevices] = {};
 
 // Device address of the scratch array on the current device, looked up once
 // per device (with that device current).  In host code the array's name is
 // only a host-side stand-in, so kernels must be given this address instead.
+// Once a device's address is known, a call reads it with one acquire load;
+// only the first lookup on a device takes the lock.
 int noalloc_scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DFLASH_E_CUDA;
   if (dev < 0 || dev >= kNoAllocMaxDevices) return DFLASH_E_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return DFLASH_E_CUDA;
-    g_noalloc_addr[dev] = p;
+  void* p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    p = g_noalloc_addr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+        return DFLASH_E_CUDA;
+      g_noalloc_addr[dev].store(p, std::memory_order_release);
+    }
   }
-  *out = g_noalloc_addr[dev];
+  *out = p;
   return DFLASH_OK;
 }
 
@@ -587,9 +615,8 @@ extern "C" int dflash_verify_accept_noalloc(const dflash_dims* dims, const void*
                                             int32_t* commit_len, int32_t* out_tokens,
                                             int32_t out_cap, dflash_stream_t stream) {
   DFLASH_ENTRY("dflash_verify_accept_noalloc");
-  int rc = check_dims(dims);
+  int rc = check_dims(dims);   // batch * 16 <= 512 = the array's token rows
   if (rc) return rc;
-  if (dims->batch * kBlock > kNoAllocMaxTokens) return DFLASH_E_UNSUPPORTED;
   if (!hidden || !w_lm || !block_ids || !len_before || !posterior || !accept_len ||
       !next_staged || !commit_len || !out_tokens || out_cap < 1)
     return DFLASH_E_ARG;
@@ -618,6 +645,30 @@ extern "C" int dflash_verify_accept_noalloc(const dflash_dims* dims, const void*
   // the keys and the ticket must start at zero; the status word is cleared too
   if ((rc = cuda_err(cudaMemsetAsync(scratch, 0, kNoAllocKeyBytes + 8, st)))) return rc;
   return launch_lmhead(*dims, plan.budget_sms, hidden, w_lm, p, st);
+}
+
+extern "C" int dflash_prefill_staged(const dflash_dims* dims, const void* hidden,
+                                     int64_t row_pitch, const void* w_lm, int32_t* staged,
+                                     void* ws, size_t ws_bytes, dflash_stream_t stream) {
+  DFLASH_ENTRY("dflash_prefill_staged");
+  int rc = check_dims(dims);
+  if (rc) return rc;
+  if (!hidden || !w_lm || !staged) return DFLASH_E_ARG;
+  if (row_pitch < dims->hidden) return DFLASH_E_ARG;
+  if (!aligned16(hidden) || !aligned16(w_lm) || (row_pitch * 2) % 16) return DFLASH_E_ALIGN;
+  if (!ws) return DFLASH_E_WORKSPACE;
+  Plan plan;
+  if ((rc = make_plan(*dims, &plan))) return rc;
+  if (ws_bytes < plan.total) return DFLASH_E_WORKSPACE;
+  LmParams p = {};
+  p.keys = ws_at<unsigned long long>(ws, plan.off_keys);
+  p.ticket = ws_at<uint32_t>(ws, plan.off_tickets);
+  p.status = ws_at<uint32_t>(ws, plan.off_status);
+  p.draft = 2;
+  p.block_out = staged;
+  return launch_lmhead(*dims, plan.budget_sms, hidden, w_lm, p,
+                       reinterpret_cast<cudaStream_t>(stream), dims->batch,
+                       static_cast<uint64_t>(row_pitch) * 2);
 }
 
 extern "C" int dflash_draft_tokens(const dflash_dims* dims, const void* x,

@@ -37,7 +37,8 @@ EXPORTED = ["dflash_workspace_bytes", "dflash_workspace_init", "dflash_ctx_proje
             "dflash_verify_accept_noalloc", "dflash_cycle_sm_split",
             "dflash_draft_workspace_bytes", "dflash_draft_qkv", "dflash_draft_mlp",
             "dflash_draft_tokens", "dflash_verify_attention", "dflash_gdn_replay",
-            "dflash_prefill_workspace_bytes", "dflash_ctx_prefill", "dflash_selftest_wait"]
+            "dflash_prefill_workspace_bytes", "dflash_ctx_prefill", "dflash_selftest_wait",
+            "dflash_prefill_attention", "dflash_prefill_staged"]
 
 
 class DFlashError(RuntimeError):
@@ -98,6 +99,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_ctx_prefill.restype = ctypes.c_int
     lib.dflash_ctx_prefill.argtypes = [ctypes.POINTER(Dims), i32, ctypes.POINTER(vp), vp, vp, vp,
                                        vp, vp, vp, ctypes.POINTER(KVViewC), vp, sz, vp]
+    lib.dflash_prefill_attention.restype = ctypes.c_int
+    lib.dflash_prefill_attention.argtypes = [ctypes.POINTER(Dims), i32, vp, vp, vp,
+                                             ctypes.POINTER(KVViewC), ctypes.c_float, vp, vp, sz,
+                                             vp]
+    lib.dflash_prefill_staged.restype = ctypes.c_int
+    lib.dflash_prefill_staged.argtypes = [ctypes.POINTER(Dims), vp, ctypes.c_int64, vp, vp, vp,
+                                          sz, vp]
     lib.dflash_gdn_replay.restype = ctypes.c_int
     lib.dflash_gdn_replay.argtypes = [i32, i32, i32, i32] + [vp] * 6 + [vp, sz, vp]
     lib.dflash_verify_accept.restype = ctypes.c_int
@@ -264,6 +272,32 @@ def dflash_ctx_prefill(dims: Dims, tokens_per_seq: int, layer_hidden: Sequence[t
         _dev(w_v, torch.bfloat16, "w_v"), _dev(k_norm_w, torch.bfloat16, "k_norm_w"),
         _dev(write_pos, torch.int32, "write_pos"), ctypes.byref(view), _dev(ws, name="ws"),
         ws.numel(), _stream(stream)), "dflash_ctx_prefill")
+
+
+def dflash_prefill_attention(dims: Dims, tokens_per_seq: int, q, k, v, cache: KVView,
+                             scale: float, out, ws, stream=None):
+    """The target's attention over a prompt chunk of tokens_per_seq rows per
+    sequence (causal), the chunk's K/V appended to ``cache``."""
+    view = cache.c()
+    _check(load_library().dflash_prefill_attention(
+        ctypes.byref(dims), int(tokens_per_seq), _dev(q, torch.bfloat16, "q"),
+        _dev(k, torch.bfloat16, "k"), _dev(v, torch.bfloat16, "v"), ctypes.byref(view),
+        float(scale), _dev(out, torch.bfloat16, "out"), _dev(ws, name="ws"), ws.numel(),
+        _stream(stream)), "dflash_prefill_attention")
+
+
+def dflash_prefill_staged(dims: Dims, last_hidden, w_lm, staged, ws, stream=None):
+    """The first staged token per sequence: argmax of the LM head at the last
+    prompt row.  ``last_hidden``: bf16 [B, H] whose rows may be strided (e.g.
+    ``h[:, -1]`` of a [B, T, H] tensor); its row stride is passed on."""
+    if not isinstance(last_hidden, torch.Tensor) or not last_hidden.is_cuda:
+        raise ValueError("last_hidden must be a CUDA tensor")
+    if last_hidden.dtype != torch.bfloat16 or last_hidden.dim() != 2 or last_hidden.stride(1) != 1:
+        raise ValueError("last_hidden must be bf16 [B, H] with unit column stride")
+    _check(load_library().dflash_prefill_staged(
+        ctypes.byref(dims), last_hidden.data_ptr(), int(last_hidden.stride(0)),
+        _dev(w_lm, torch.bfloat16, "w_lm"), _dev(staged, torch.int32, "staged"),
+        _dev(ws, name="ws"), ws.numel(), _stream(stream)), "dflash_prefill_staged")
 
 
 def dflash_block_attention(dims: Dims, q_blk, k_blk, v_blk, cache: KVView, scale: float, out,

@@ -238,7 +238,7 @@ DFLASH_API int dflash_verify_accept(const dflash_dims* dims, const void* hidden,
  * owns every device allocation and offers no allocator, processes held to a
  * fixed device-memory budget, and code that must not allocate while a stream
  * is being captured.
- * Same arguments, results and errors as dflash_verify_accept, minus ws and
+ * Same arguments and results as dflash_verify_accept, minus ws and
  * ws_bytes.  Its scratch (one 64-bit key per token row, a ticket, a status
  * word) is a library-owned static device array sized for batch * 16 <= 512
  * token rows (about 4 KB), held by every GPU that loads the library until the
@@ -250,8 +250,10 @@ DFLASH_API int dflash_verify_accept(const dflash_dims* dims, const void* hidden,
  * before its kernel.  All calls share the one array and it keeps the last
  * call's contents, so calls that overlap on the GPU (other streams, other
  * threads) race: order them.  Device-side status bits of this variant are not
- * reported (there is no workspace to read them from); commits that would pass
- * out_cap are still skipped.
+ * reported (there is no workspace to read them from): block ids outside the
+ * vocabulary still never match and a commit that would pass out_cap is still
+ * skipped, but nothing tells the caller, and if an in-kernel wait gives up
+ * (DFLASH_ST_TIMEOUT in the workspace variant) the outputs are undefined.
  */
 DFLASH_API int dflash_verify_accept_noalloc(const dflash_dims* dims, const void* hidden,
                                             const void* w_lm, const int32_t* block_ids,
@@ -267,7 +269,10 @@ DFLASH_API int dflash_verify_accept_noalloc(const dflash_dims* dims, const void*
  * Paged views: every mapped page that starts at or after new_len[b] is pushed
  * back on the free list and its table slot set to -1 (the partly used last
  * page is kept).  new_len > seq_len or new_len < 0 sets DFLASH_ST_CROP_GROW
- * and leaves that sequence unchanged.  n_views <= 4.  views is a HOST array.
+ * and leaves that sequence unchanged.  A page that would overflow a full free
+ * list (*free_count == n_pages: an inconsistent pool) stays mapped to its
+ * sequence, which reuses it when it grows again, and sets DFLASH_ST_CAPACITY;
+ * the length is still cut.  n_views <= 4.  views is a HOST array.
  */
 DFLASH_API int dflash_kv_crop(const dflash_kv_view* views, int32_t n_views, const int32_t* new_len,
                    int32_t batch, void* ws, size_t ws_bytes, dflash_stream_t stream);
@@ -335,7 +340,8 @@ DFLASH_API int dflash_draft_tokens(const dflash_dims* dims, const void* x,
  *   layer_hidden: HOST array of nL device pointers, each bf16 [B*T, H]
  *                 (row b*T + t).  w_fc, hidden_norm_w, w_k, w_v, k_norm_w as
  *                 for dflash_ctx_project.  write_pos: int32 [B] device.
- *   ws: dflash_prefill_workspace_bytes(dims, T) bytes, zeroed once.
+ *   ws: dflash_prefill_workspace_bytes(dims, T) bytes, zeroed once (it also
+ *   serves dflash_prefill_attention for the same T).
  * Requires hidden % 128 == 0, n_kv_heads * head_dim % 128 == 0.
  * Errors: DFLASH_ST_CAPACITY (no room for T rows: that sequence is left
  * alone), DFLASH_ST_POOL_EMPTY / DFLASH_ST_PAGE_MISSING (rows without a page
@@ -348,6 +354,51 @@ DFLASH_API int dflash_ctx_prefill(const dflash_dims* dims, int32_t tokens_per_se
                                   const void* k_norm_w, const int32_t* write_pos,
                                   const dflash_kv_view* cache, void* ws, size_t ws_bytes,
                                   dflash_stream_t stream);
+
+/*
+ * Next: the target's side of the prefill ([P2] 单次前向验证 ①: the target
+ * prefills the prompt in chunks, which initialises its KV cache; ②: the
+ * target's greedy token after the prompt is the first staged token).
+ *
+ * dflash_prefill_attention — one layer's attention over a prompt chunk of
+ * T = tokens_per_seq rows per sequence.  With L = cache->seq_len[b], chunk
+ * row t sits at position L + t and sees the cache rows 0..L-1 and the chunk
+ * rows 0..t (causal):
+ *   out[b,t,h] = softmax(RoPE_{L+t}(q[b,t,h]) K^T * scale) V
+ *   K = cache K rows 0..L-1 of KV head h / (Hq/Hkv) ⊕ RoPE_{L+j}(k[b,j,g]), j <= t
+ *   V = cache V rows 0..L-1 ⊕ v[b,j,g], j <= t.
+ * The chunk's rotated K and its V are appended to `cache` at rows L..L+T-1
+ * (for a paged cache the pages they need are first taken from its free
+ * list), after which cache->seq_len[b] = L + T; a prompt fed chunk by chunk
+ * gives the rows of the prompt fed at once.  Any T >= 1 (ceil(T/16) * batch
+ * <= 65535).
+ *   q: bf16 [B, T, Hq, D]; k, v: bf16 [B, T, Hkv, D] (before RoPE);
+ *   out: bf16 [B, T, Hq, D].
+ *   ws: dflash_prefill_workspace_bytes(dims, T) bytes, zeroed once (the same
+ *   workspace serves dflash_ctx_prefill); its status word reads with
+ *   dflash_read_status.  dims->max_ctx bounds L + T (it sizes the split
+ *   scratch).
+ * Errors: L < 0 or L + T past the capacity sets DFLASH_ST_CAPACITY and leaves
+ * that sequence (cache, length, output) untouched; DFLASH_ST_POOL_EMPTY /
+ * DFLASH_ST_PAGE_MISSING as for dflash_verify_attention.
+ */
+DFLASH_API int dflash_prefill_attention(const dflash_dims* dims, int32_t tokens_per_seq,
+                                        const void* q, const void* k, const void* v,
+                                        const dflash_kv_view* cache, float scale, void* out,
+                                        void* ws, size_t ws_bytes, dflash_stream_t stream);
+
+/*
+ * dflash_prefill_staged — the first staged token: staged[b] = argmax over the
+ * vocabulary of hidden_b W_lm^T (lowest index on exact ties; logits never
+ * written), hidden_b being the final-normed hidden state of sequence b's
+ * last prompt row, bf16 [H] at hidden + b * row_pitch elements (row_pitch >=
+ * H, a multiple of 8: e.g. T * H to take row T-1 of a [B, T, H] array).
+ * w_lm: bf16 [V, H]; staged: int32 [B].  ws: a workspace of
+ * dflash_workspace_bytes(dims) bytes (the verification's), zeroed once.
+ */
+DFLASH_API int dflash_prefill_staged(const dflash_dims* dims, const void* hidden,
+                                     int64_t row_pitch, const void* w_lm, int32_t* staged,
+                                     void* ws, size_t ws_bytes, dflash_stream_t stream);
 
 /*
  * Next: rollback of the recurrent state of a hybrid target ([P2] 保证三:
@@ -387,7 +438,7 @@ DFLASH_API const char* dflash_status_string(int code);
  */
 DFLASH_API int dflash_selftest_wait(int arrive, void* ws, size_t ws_bytes, dflash_stream_t stream);
 
-/* Library ABI version (major * 100 + minor): 107. */
+/* Library ABI version (major * 100 + minor): 108. */
 DFLASH_API int dflash_version(void);
 
 #ifdef __cplusplus

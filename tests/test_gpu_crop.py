@@ -63,3 +63,25 @@ def test_crop_rejects_bad_arguments():
         dfl.dflash_kv_crop([v] * 5, dev_i32([1]), 1, ws)       # too many views
     with pytest.raises(dfl.DFlashError):
         dfl.dflash_kv_crop([v], dev_i32([1]), 0, ws)           # empty batch
+
+
+def test_crop_keeps_a_page_that_would_overflow_a_full_free_list():
+    """An inconsistent pool (free list already holding n_pages entries while a
+    sequence still maps pages): the length is cut, the page that cannot be
+    pushed stays mapped (nothing is lost or written past the list) and
+    DFLASH_ST_CAPACITY is set."""
+    dfl = _dfl()
+    n_pages = 4
+    table = np.array([[0, 1, -1, -1]], np.int32)          # sequence 0 maps pages 0 and 1
+    free = np.array([0, 1, 2, 3], np.int32)               # ... and all four are listed free
+    dims = dfl.make_dims(1, 128, 1, 1, 128, 16, 1, 64)
+    ws = dfl.alloc_workspace(dims)
+    view = dfl.KVView(None, None, dev_i32([30]), capacity=64, page_table=dev_i32(table),
+                      free_list=dev_i32(free), free_count=dev_i32([n_pages]), page_size=16)
+    dfl.dflash_kv_crop([view], dev_i32([5]), 1, ws)
+    torch.cuda.synchronize()
+    assert dfl.dflash_read_status(ws) == dfl.dflash.STATUS_BITS["capacity"]
+    assert int(view.seq_len.item()) == 5
+    assert view.page_table.cpu().numpy().tolist() == [[0, 1, -1, -1]]
+    assert int(view.free_count.item()) == n_pages
+    assert view.free_list.cpu().numpy().tolist() == free.tolist()

@@ -1,8 +1,9 @@
 """The allocation-free verify entry point, for callers that cannot allocate
 device memory (plugins without an allocator, fixed memory budgets, code that
 must not allocate during stream capture): called through the C ABI, its
-results must equal those of dflash_verify_accept on the same inputs, on two
-calls in a row (the shared scratch must come back clean).
+results must equal those of dflash_verify_accept on the same inputs on every
+one of two calls in a row, with the second call reusing the shared scratch
+the first one left behind.
 
 Collected last on purpose, so that a run stopping at the first failure has
 already run every other test."""
@@ -61,6 +62,7 @@ def test_noalloc_matches_workspace_entry_point_twice(B, H, V):
                 lb.data_ptr(), *[t.data_ptr() for t in got], cap, stream)
         assert rc == 0, dfl.status_string(rc)
         torch.cuda.synchronize()
+        # the workspace entry point's status (the variant reports none)
         assert dfl.dflash_read_status(ws) == 0
         for r, g in zip(ref, got):
             assert torch.equal(r, g), call
@@ -74,7 +76,10 @@ def test_noalloc_rejects_batches_past_its_scratch():
     lib = dfl.load_library()
     fn = lib.dflash_verify_accept_noalloc
     fn.restype = ctypes.c_int
-    dims = dfl.make_dims(33, 256, 4, 4, 128, 1000, 1, 64)   # 528 token rows > 512
+    # 528 token rows > 512: refused by the shape check every entry point shares,
+    # whose 512-row limit the scratch array covers (a static assertion in the
+    # library ties the two), before anything is launched
+    dims = dfl.make_dims(33, 256, 4, 4, 128, 1000, 1, 64)
     t = torch.zeros(16, dtype=torch.int32, device="cuda")
     rc = fn(ctypes.byref(dims), *([ctypes.c_void_p(t.data_ptr())] * 9), ctypes.c_int32(16),
             ctypes.c_void_p(0))
