@@ -62,6 +62,36 @@ def assert_close_bf16(got: np.ndarray, ref: np.ndarray, max_abs: float = 2e-2,
     return {"max_abs": mx, "rel_l2": rl2, "max_ref": float(np.abs(ref).max()) if ref.size else 0}
 
 
+def half_ulp_bf16(ref: np.ndarray) -> np.ndarray:
+    """Half a bf16 unit in the last place at |ref| (7 fraction bits):
+    2^(e - 8) for |ref| in [2^e, 2^(e + 1)); 0 where ref is 0."""
+    a = np.abs(ref)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(e - 8), 0.0)
+
+
+def assert_close_bf16_wide(got: np.ndarray, ref: np.ndarray, max_abs: float = 2e-2,
+                           rel_l2: float = 1e-2) -> dict:
+    """The float bar for bf16 outputs that may pass 8 in magnitude: an element
+    with |ref| < 8 is within max_abs of float64, one with |ref| >= 8 within
+    max_abs plus half a bf16 ulp of ref (rounding the result to bf16 alone
+    costs up to that much there); relative-L2 as usual.  Returns the error
+    figures and how many elements took the wider bound."""
+    err = np.abs(got - ref)
+    wide = np.abs(ref) >= 8
+    bound = max_abs + np.where(wide, half_ulp_bf16(ref), 0.0)
+    bad = err > bound
+    assert not bad.any(), (int(bad.sum()), float(err[bad].max()),
+                           np.unravel_index(int(np.argmax(err - bound)), err.shape))
+    denom = float(np.linalg.norm(ref)) or 1.0
+    rl2 = float(np.linalg.norm(got - ref)) / denom
+    assert rl2 <= rel_l2, rl2
+    return {"max_abs": float(err.max()) if err.size else 0.0, "rel_l2": rl2,
+            "max_ref": float(np.abs(ref).max()) if ref.size else 0.0,
+            "n_wide": int(wide.sum()),
+            "max_abs_narrow": float(err[~wide].max()) if (~wide).any() else 0.0}
+
+
 class Guarded:
     """A device output buffer with guard bands on both sides (filled with the
     byte 0xA5); ``t`` is the buffer proper, ``check()`` asserts that nothing

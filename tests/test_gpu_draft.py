@@ -11,8 +11,8 @@ from oracle.dflash_oracle import bf16_to_f64
 from oracle.dflash_oracle import block_attention as ref_attention
 from oracle.dflash_oracle import draft_out_mlp, draft_qkv, draft_tokens
 from synthetic import normal_bf16, pack_contiguous_heads, unit_rms_rows_bf16
-from tests.gpu_helpers import (Guarded, assert_close_bf16, check_verify, dev_bf16, dev_i32,
-                               host_bits, host_f64)
+from tests.gpu_helpers import (Guarded, assert_close_bf16, assert_close_bf16_wide, check_verify,
+                               dev_bf16, dev_i32, host_bits, host_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -203,9 +203,13 @@ def test_drafter_layer_composed():
     assert np.array_equal(got[~tie], t["posterior"][~tie])
 
 
-@pytest.mark.parametrize("name", ["qwen3_8b_b1"])
+@pytest.mark.parametrize("name", ["qwen3_8b_b1", "qwen3_32b_b4_32k"])
 def test_drafter_layer_full_size(name):
-    """Qwen3-8B / Qwen3-32B shapes (MLP width 12288 / 25600), batch 1 / 4."""
+    """Qwen3-8B / Qwen3-32B shapes (MLP width 12288 / 25600), batch 1 / 4, with
+    the workload's weight distribution (std 0.02 throughout).  The layer output
+    then passes 8 in places; there the bar is max-abs 2e-2 plus half a bf16 ulp
+    of the float64 value (the rounding of the stored result alone), and the
+    number of such elements is printed."""
     from synthetic import CONFIG_BY_NAME
     dfl = _dfl()
     cfg = CONFIG_BY_NAME[name]
@@ -213,9 +217,6 @@ def test_drafter_layer_full_size(name):
     rng = np.random.default_rng(5)
     B, H, Hq, Hkv, D = cfg.batch, cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
     w = layer_weights(rng, H, Hq, Hkv, D, F)
-    # a smaller down projection keeps the layer output below 8, where the bf16
-    # half-ulp of the stored result stays inside the 2e-2 tolerance
-    w["wd"] = normal_bf16(rng, (H, F), 0.005)
     x = unit_rms_rows_bf16(rng, (B * 16, H))
     o = normal_bf16(rng, (B * 16, Hq * D), 0.3)
     dims = dfl.make_dims(B, H, Hq, Hkv, D, cfg.vocab, 1, 64)
@@ -228,9 +229,11 @@ def test_drafter_layer_full_size(name):
     torch.cuda.synchronize()
     assert dfl.dflash_read_status(dws) == 0
     r = draft_qkv(x, w["ln1"], w["wq"], w["wk"], w["wv"], w["qn"], w["kn"], Hq, Hkv, D, 1e-6)
-    assert_close_bf16(host_f64(q).reshape(-1, Hq, D), r["q"])
-    assert_close_bf16(host_f64(k).reshape(-1, Hkv, D), r["k"])
-    assert_close_bf16(host_f64(v).reshape(-1, Hkv, D), r["v"])
+    assert_close_bf16_wide(host_f64(q).reshape(-1, Hq, D), r["q"])
+    assert_close_bf16_wide(host_f64(k).reshape(-1, Hkv, D), r["k"])
+    assert_close_bf16_wide(host_f64(v).reshape(-1, Hkv, D), r["v"])
     x2 = draft_out_mlp(x, o, w["wo"], w["ln2"], w["wg"], w["wu"], w["wd"], 1e-6)["x2"]
-    assert np.abs(x2).max() < 8
-    assert_close_bf16(host_f64(xo), x2)
+    info = assert_close_bf16_wide(host_f64(xo), x2)
+    print(f"{name}: layer output max |x2| {info['max_ref']:.2f}, {info['n_wide']} of {x2.size} "
+          f"elements at |x2| >= 8, max-abs error {info['max_abs']:.4f} "
+          f"({info['max_abs_narrow']:.4f} below 8), rel-L2 {info['rel_l2']:.2e}")
