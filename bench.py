@@ -37,6 +37,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "draft+verify cycles/s at Qwen3-8B shapes, block 16; % of HBM roofline"
+from synthetic import CONFIG_BY_NAME  # noqa: E402  (input generators only; no arithmetic)
 UNIT = "cycles/s"
 DEFAULT_CONFIG = "qwen3_8b_b1"
 L2_BYTES = 129 * 1024 * 1024
@@ -57,7 +58,12 @@ def parse_args(argv=None):
     ap.add_argument("--sets", type=int, default=0,
                     help="rotating input sets (0: enough to exceed twice the L2 size)")
     ap.add_argument("--prefill-tokens", type=int, default=8192,
-                    help="prompt length of the prefill-projection pass (0 = skip)")
+                    help="prompt length of the prefill passes (0 = skip)")
+    ap.add_argument("--prefill-chunk", type=int, default=2048,
+                    help="prompt chunk of the prefill-attention pass")
+    ap.add_argument("--b32-steps", type=int, default=50,
+                    help="timed cycles of the batch-32 paged workload reported beside the "
+                         "headline (0 = skip)")
     ap.add_argument("--draft-steps", type=int, default=100,
                     help="extra steps timing the rest of the drafter layer (Q/K/V, attention, "
                          "output projection + MLP, tokens), reported beside the cycle")
@@ -377,60 +383,103 @@ def build_draft(cfg, device="cuda"):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (bounded sample)
 # ---------------------------------------------------------------------------
-def oracle_cycle_seconds(cfg, frac_vocab: float, frac_feat: float) -> dict:
-    """Time the float64 oracle's four steps on a row sample of the workload and
-    scale each step's time back to the full workload.
-
-    Sample: LM head over frac_vocab of the vocabulary rows; context
-    projection over frac_feat of W_fc's output features (full input width)
-    with one KV head of W_k/W_v; attention for one KV head group with the full
-    context; crop in full.  Scaling is linear in the sampled rows/heads."""
+def oracle_inputs(cfg, frac: float = 1.0) -> dict:
+    """Seeded inputs of the oracle's cycle (bf16 bit patterns), the whole
+    workload when frac == 1, else a row sample: frac of the LM head's
+    vocabulary rows and of the projection's output features, one KV head of
+    the attention.  Weights are drawn with a seeded CPU torch generator (the
+    same distributions as the GPU workload)."""
     import numpy as np
+    import torch
 
-    from oracle.dflash_oracle import block_attention, ctx_project, kv_crop_lengths, verify_accept
-    from synthetic import normal_bf16, unit_rms_rows_bf16
+    from synthetic import device_generator, device_normal_bf16, normal_bf16, unit_rms_rows_bf16
+
+    def bits(t):
+        return t.view(torch.int16).numpy().view(np.uint16)
 
     rng = np.random.default_rng(7)
     B, H, V = cfg.batch, cfg.hidden, cfg.vocab
     Hq, Hkv, D, nL = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.n_ctx_layers
     L = int(cfg.ctx_len or cfg.ctx_len_range[1])
-    nv = max(64, int(V * frac_vocab))
-    nf = max(D, int(H * frac_feat) // D * D)
-    G = Hq // Hkv
-    hidden = unit_rms_rows_bf16(rng, (B, 16, H))
-    w_lm = normal_bf16(rng, (nv, H), 0.02)
-    layers = [unit_rms_rows_bf16(rng, (B * 16, H)) for _ in range(nL)]
-    w_fc = normal_bf16(rng, (nf, nL * H), 0.02)
-    gh = normal_bf16(rng, (nf,), 0.02, 1.0)
-    wk = normal_bf16(rng, (D, nf), 0.02)
-    wv = normal_bf16(rng, (D, nf), 0.02)
-    gk = normal_bf16(rng, (D,), 0.02, 1.0)
-    q = normal_bf16(rng, (B, 16, G, D))
-    kb = normal_bf16(rng, (B, 16, 1, D))
-    vb = normal_bf16(rng, (B, 16, 1, D))
-    ck = [normal_bf16(rng, (L, 1, D)) for _ in range(B)]
-    cv = [normal_bf16(rng, (L, 1, D)) for _ in range(B)]
+    full = frac >= 1.0
+    nv = V if full else max(64, int(V * frac))
+    nf = H if full else max(D, int(H * frac) // D * D)
+    hk = Hkv if full else 1
+    g = device_generator(cfg, "w_lm", "cpu")
+    inp = {
+        "frac": frac, "nv": nv, "nf": nf, "hk": hk, "L": L,
+        "hidden": unit_rms_rows_bf16(rng, (B, 16, H)),
+        "w_lm": bits(device_normal_bf16(g, (nv, H), 0.02, device="cpu")),
+        "layers": [unit_rms_rows_bf16(rng, (B * 16, H)) for _ in range(nL)],
+        "w_fc": bits(device_normal_bf16(g, (nf, nL * H), 0.02, device="cpu")),
+        "gh": normal_bf16(rng, (nf,), 0.02, 1.0),
+        "wk": normal_bf16(rng, (hk * D, nf), 0.02), "wv": normal_bf16(rng, (hk * D, nf), 0.02),
+        "gk": normal_bf16(rng, (D,), 0.02, 1.0),
+        "q": normal_bf16(rng, (B, 16, hk * (Hq // Hkv), D)),
+        "kb": normal_bf16(rng, (B, 16, hk, D)), "vb": normal_bf16(rng, (B, 16, hk, D)),
+        "ck": [normal_bf16(rng, (L, hk, D)) for _ in range(B)],
+        "cv": [normal_bf16(rng, (L, hk, D)) for _ in range(B)]}
+    return inp
+
+
+def oracle_cycle_seconds(cfg, inp: dict) -> dict:
+    """Time the float64 oracle's four steps on `inp` (oracle_inputs).  On the
+    whole workload (frac 1) the times are the cycle's own; on a row sample
+    each step's time is scaled by the inverse of its sampled fraction (the
+    steps are linear in the sampled rows and heads), and the result says it
+    is extrapolated."""
+    import numpy as np
+
+    from oracle.dflash_oracle import block_attention, ctx_project, kv_crop_lengths, verify_accept
+
+    B, H, V, D = cfg.batch, cfg.hidden, cfg.vocab, cfg.head_dim
+    Hkv, L = cfg.n_kv_heads, inp["L"]
+    nv, nf, hk = inp["nv"], inp["nf"], inp["hk"]
     blk = np.zeros((B, 16), np.int32)
     t = {}
     t0 = time.perf_counter()
-    verify_accept(hidden, w_lm, blk, np.zeros(B, np.int32), out_cap=32)
+    verify_accept(inp["hidden"], inp["w_lm"], blk, np.zeros(B, np.int32), out_cap=32)
     t["lm_head"] = (time.perf_counter() - t0) * (V / nv)
     t0 = time.perf_counter()
-    ctx_project(layers, w_fc, gh, wk, wv, gk, np.arange(B * 16) + L, 1, D, cfg.rope_theta,
-                cfg.rms_eps)
+    ctx_project(inp["layers"], inp["w_fc"], inp["gh"], inp["wk"], inp["wv"], inp["gk"],
+                np.arange(B * 16) + L, hk, D, cfg.rope_theta, cfg.rms_eps)
     t["ctx_project"] = (time.perf_counter() - t0) * (H / nf)
     t0 = time.perf_counter()
-    block_attention(q, kb, vb, ck, cv, np.full(B, L), cfg.rope_theta, 1 / math.sqrt(D))
-    t["attention"] = (time.perf_counter() - t0) * Hkv
+    block_attention(inp["q"], inp["kb"], inp["vb"], inp["ck"], inp["cv"], np.full(B, L),
+                    cfg.rope_theta, 1 / math.sqrt(D))
+    t["attention"] = (time.perf_counter() - t0) * (Hkv / hk)
     t0 = time.perf_counter()
     kv_crop_lengths(np.full(B, L + 16), np.full(B, L + 9))
     kv_crop_lengths(np.full(B, L + 16), np.full(B, L + 9))
     t["crop"] = time.perf_counter() - t0
     t["total"] = sum(t.values())
-    t["sample"] = (f"LM head over {nv}/{V} vocab rows (x{V / nv:.0f}); ctx projection over "
-                   f"{nf}/{H} output features (x{H / nf:.0f}); attention of 1/{Hkv} KV heads "
-                   f"(x{Hkv}) at context {L}; crop in full; batch {B}")
+    t["extrapolated"] = nv < V or nf < H or hk < Hkv
+    if t["extrapolated"]:
+        t["sample"] = (f"extrapolated linearly from a row sample: LM head over {nv}/{V} vocab "
+                       f"rows (x{V / nv:.1f}); projection over {nf}/{H} output features "
+                       f"(x{H / nf:.1f}); attention of {hk}/{Hkv} KV heads (x{Hkv / hk:.0f}) "
+                       f"at context {L}; crop in full; batch {B}")
+    else:
+        t["sample"] = (f"the whole cycle, no sampling: LM head over all {V} vocab rows, "
+                       f"projection of all {H} features, attention of all {Hkv} KV heads at "
+                       f"context {L}, crop; batch {B}")
     return t
+
+
+def host_threads() -> dict:
+    """The host threads the oracle may use: the CPU count, this process's
+    affinity and the BLAS library's thread count (threadpoolctl when present,
+    else the thread environment variables)."""
+    info = {"os_cpu_count": os.cpu_count(), "affinity": cpu_cores()}
+    try:
+        from threadpoolctl import threadpool_info
+        info["blas"] = [{"api": d.get("internal_api"), "threads": d.get("num_threads")}
+                        for d in threadpool_info() if d.get("user_api") == "blas"]
+    except ImportError:
+        info["blas_env"] = {k: os.environ.get(k) for k in (
+            "OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS") if os.environ.get(k)}
+        info["blas"] = "threadpoolctl not installed; BLAS uses its default (all affinity cores)"
+    return info
 
 
 def cpu_cores() -> int:
@@ -441,24 +490,29 @@ def cpu_cores() -> int:
 
 
 def run_reference(args, cfg):
-    """The oracle, timed on the host cores, on bounded samples of the workload."""
-    budget_s = 150.0
+    """The oracle, timed on the host cores: the whole cycle of the workload per
+    step when the run fits the time budget, else a row sample per step
+    (extrapolated, and said so)."""
+    budget_s = 200.0
     n = args.steps + args.warmup
-    frac_v, frac_f = 1 / 64, 1 / 8
-    t0 = time.perf_counter()
-    oracle_cycle_seconds(cfg, frac_v, frac_f)
-    wall = time.perf_counter() - t0
-    while n * wall > budget_s and frac_v > 1 / 8192:
-        frac_v /= 2
-        frac_f = max(1 / 32, frac_f / 2)
-        wall /= 2
+    inp = oracle_inputs(cfg, 1.0)
+    first = oracle_cycle_seconds(cfg, inp)           # also the first warm-up step
+    frac = 1.0
+    while n * first["total"] * frac > budget_s and frac > 1 / 4096:
+        frac /= 2
+    if frac < 1.0:
+        inp = oracle_inputs(cfg, frac)
     times = []
-    sample = None
-    for i in range(n):
-        r = oracle_cycle_seconds(cfg, frac_v, frac_f)
-        sample = r["sample"]
+    wall0 = time.perf_counter()
+    sample, extrap = first["sample"], first["extrapolated"]
+    for i in range(1, n):
+        r = oracle_cycle_seconds(cfg, inp)
+        sample, extrap = r["sample"], r["extrapolated"]
         if i >= args.warmup:
             times.append(r["total"])
+    while len(times) < args.steps:                  # steps > 0 and warmup == 0
+        times.append(oracle_cycle_seconds(cfg, inp)["total"])
+    measured_s = time.perf_counter() - wall0
     total = sum(times)
     value = args.steps / total
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
@@ -467,47 +521,42 @@ def run_reference(args, cfg):
             "data": "synthetic", "config": {"workload": cfg.name, "batch": cfg.batch,
                                             "block": 16, "context": cfg.ctx_len},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(),
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample, "extrapolated": extrap,
+                             "threads": host_threads(),
+                             "host_seconds_of_timed_steps": measured_s},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
 
 # ---------------------------------------------------------------------------
-def main(argv=None):
-    args = parse_args(argv)
-    world, rank, local = dist_env()
-    from synthetic import CONFIG_BY_NAME
-    cfg = CONFIG_BY_NAME[args.config]
-    if args.impl == "reference":
-        if rank == 0:
-            run_reference(args, cfg)
-        return 0
+# the timed cycle
+# ---------------------------------------------------------------------------
+def cycle_pass(cfg, steps, warmup, concurrent, sm_split_arg, sets, rank, local,
+               sample_clocks=False):
+    """Build the workload `cfg` on the GPU, fix the verify || projection SM
+    split (measured around the proportional one unless given), run `warmup`
+    untimed and `steps` timed cycles (CUDA events on the launching stream,
+    events around every LM-head launch and the verify || projection phase),
+    and return everything the other passes reuse."""
+    import types
 
-    import numpy as np
     import torch
 
-    import __graft_entry__
-    torch.cuda.set_device(local)
-    __graft_entry__.build()
-    world, rank = init_dist("nccl")
     import block_diffusion_speculative_02_gb300 as dfl
-    from block_diffusion_speculative_02_gb300.cycle import (CycleGraph, PipelinedCycles,
-                                                            packed_tensors, side_stream,
-                                                            tune_sm_split)
+    from block_diffusion_speculative_02_gb300.cycle import side_stream, tune_sm_split
 
     kv_bytes_per_set = 2 * cfg.n_kv_heads * cfg.head_dim * 2 * (
         cfg.batch * (cfg.ctx_len or cfg.ctx_len_range[1]) + 32)
-    n_sets = args.sets or max(1, min(16, math.ceil(2 * L2_BYTES / max(1, kv_bytes_per_set))))
+    n_sets = sets or max(1, min(16, math.ceil(2 * L2_BYTES / max(1, kv_bytes_per_set))))
     dims, w, states, accepts, ws, lens = build_workload(cfg, n_sets)
     stream = torch.cuda.current_stream()
-    concurrent = not args.serial
     if concurrent:
         # verify on this stream, the projection on a side stream, each on its
         # own share of the SMs (measured once around the proportional split,
         # before the warm-up); joined before the crop
-        if args.sm_split:
-            verify_sms, project_sms = (int(x) for x in args.sm_split.split(","))
+        if sm_split_arg:
+            verify_sms, project_sms = (int(x) for x in sm_split_arg.split(","))
         else:
             verify_sms, project_sms = tune_sm_split(dims, w, states, ws)
         side = side_stream(stream.device)
@@ -556,7 +605,7 @@ def main(argv=None):
             dfl.dflash_block_attention(dims, st.q_blk, st.k_blk, st.v_blk, st.draft_cache,
                                        1.0 / math.sqrt(cfg.head_dim), st.attn_out, ws, stream)
 
-    for i in range(args.warmup):
+    for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
     status = dfl.dflash_read_status(ws)
@@ -564,29 +613,63 @@ def main(argv=None):
         raise RuntimeError(f"device status {status:#x} after warm-up")
     sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
                            if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
-    if rank == 0:
+    if sample_clocks and rank == 0:
         sampler.start()
         time.sleep(0.3)
     lm_events = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3))
-                 for _ in range(args.steps)]
+                 for _ in range(steps)]
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     e0.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i, lm_events[i])
+    for i in range(steps):
+        step(warmup + i, lm_events[i])
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    clocks = sampler.stop() if rank == 0 else None
+    clocks = sampler.stop() if (sample_clocks and rank == 0) else None
     elapsed_s = e0.elapsed_time(e1) / 1e3
-    max_s = max_over_ranks(elapsed_s, device="cuda")
     lm_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in lm_events)
     phase_ms = statistics.mean(a.elapsed_time(c) for a, _, c in lm_events)
     status = dfl.dflash_read_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {status:#x} after the timed region")
+    return types.SimpleNamespace(
+        dims=dims, w=w, states=states, accepts=accepts, ws=ws, lens=lens, n_sets=n_sets,
+        concurrent=concurrent, verify_sms=verify_sms, project_sms=project_sms, stream=stream,
+        clocks=clocks, elapsed_s=elapsed_s, lm_ms=lm_ms, phase_ms=phase_ms, steps=steps)
+
+
+# ---------------------------------------------------------------------------
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_env()
+    cfg = CONFIG_BY_NAME[args.config]
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, cfg)
+        return 0
+
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    torch.cuda.set_device(local)
+    __graft_entry__.build()
+    world, rank = init_dist("nccl")
+    import block_diffusion_speculative_02_gb300 as dfl
+    from block_diffusion_speculative_02_gb300.cycle import (CycleGraph, PipelinedCycles,
+                                                            packed_tensors)
+
+    cp = cycle_pass(cfg, args.steps, args.warmup, not args.serial, args.sm_split, args.sets,
+                    rank, local, sample_clocks=True)
+    dims, w, states, accepts, ws, lens = cp.dims, cp.w, cp.states, cp.accepts, cp.ws, cp.lens
+    n_sets, concurrent = cp.n_sets, cp.concurrent
+    verify_sms, project_sms = cp.verify_sms, cp.project_sms
+    stream = cp.stream
+    clocks, elapsed_s, lm_ms, phase_ms = cp.clocks, cp.elapsed_s, cp.lm_ms, cp.phase_ms
+    max_s = max_over_ranks(elapsed_s, device="cuda")
 
     # launches of our kernels per step: verify 1, ctx_project 2, crop 1, attention 2
     launches_per_step = 6
@@ -888,6 +971,67 @@ def main(argv=None):
                            "not in the cycle metric"}
         del pl_hidden, pws, pk, pview
 
+    # ---- the target's prefill attention: one layer over the prompt, in chunks ----
+    prefill_att = None
+    if args.prefill_tokens > 0:
+        T, C = args.prefill_tokens, min(args.prefill_chunk, args.prefill_tokens)
+        Hq_, Hkv_, D_ = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim
+        ga = torch.Generator(device="cuda")
+        ga.manual_seed(13)
+        qa = torch.randn((1, T, Hq_, D_), generator=ga, device="cuda").to(torch.bfloat16)
+        ka = torch.randn((1, T, Hkv_, D_), generator=ga, device="cuda").to(torch.bfloat16)
+        va = torch.randn((1, T, Hkv_, D_), generator=ga, device="cuda").to(torch.bfloat16)
+        chunks = [(a, min(C, T - a)) for a in range(0, T, C)]
+        qc = [qa[:, a:a + n].contiguous() for a, n in chunks]
+        kc = [ka[:, a:a + n].contiguous() for a, n in chunks]
+        vc = [va[:, a:a + n].contiguous() for a, n in chunks]
+        oc = [torch.empty_like(x) for x in qc]
+        adims = dfl.make_dims(1, cfg.hidden, Hq_, Hkv_, D_, cfg.vocab, cfg.n_ctx_layers, T,
+                              rope_theta=cfg.rope_theta)
+        aws = [dfl.dflash.alloc_prefill_workspace(adims, n) for _, n in chunks]
+        ak = torch.empty((1, Hkv_, T, D_), dtype=torch.bfloat16, device="cuda")
+        aview = dfl.KVView(ak, torch.empty_like(ak),
+                           torch.zeros(1, dtype=torch.int32, device="cuda"), capacity=T)
+
+        def prompt_pass():
+            aview.seq_len.zero_()
+            for j, (_, n) in enumerate(chunks):
+                dfl.dflash.dflash_prefill_attention(adims, n, qc[j], kc[j], vc[j], aview,
+                                                    1.0 / math.sqrt(D_), oc[j], aws[j])
+
+        for _ in range(2):
+            prompt_pass()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        reps = 5
+        a0.record(stream)
+        for _ in range(reps):
+            prompt_pass()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        for x in aws:
+            if dfl.dflash_read_status(x) != 0:
+                raise RuntimeError("device status set by the prefill attention")
+        a_us = 1e3 * a0.elapsed_time(a1) / reps
+        # causal attention: row t scores t + 1 keys; QK^T and PV, 2 flops per MAC each
+        aflops = 4.0 * Hq_ * D_ * (T * (T + 1) / 2)
+        # bytes it must move: Q, K, V in, O out, the appended K/V rows
+        abytes = 2 * T * (2 * Hq_ + 4 * Hkv_) * D_
+        tpk, tpk_kind = measured_peak_tflops()
+        prefill_att = {
+            "tokens": T, "chunk": C, "us": a_us,
+            "roofline": {"bound": "tensor", "achieved": aflops / (a_us / 1e6) / 1e12,
+                         "peak": tpk, "peak_kind": tpk_kind, "unit": "TFLOP/s",
+                         "frac": aflops / (a_us / 1e6) / 1e12 / tpk, "flops_per_prompt": aflops,
+                         "hbm_gbs": abytes / (a_us / 1e6) / 1e9, "bytes_per_prompt": abytes},
+            "note": "one layer of the target's prefill: causal attention over the prompt fed in "
+                    "chunks, each chunk's K/V appended to the cache (append + attention + "
+                    "length launches per chunk); the query rows of a KV head (4 heads x 16 "
+                    "rows) are staged twice in the 128-row MMA, so half the tensor issue "
+                    "carries duplicates; not in the cycle metric"}
+        del qa, ka, va, qc, kc, vc, oc, aws, ak, aview
+
     # ---- end to end: host buffers in, results out, every step ----
     e2e = None
     if args.e2e_steps > 0:
@@ -937,12 +1081,39 @@ def main(argv=None):
                "loop": "PipelinedCycles: one graph per step; the next step's host-to-device "
                        "copy overlaps the current step; results read back every step"}
 
+    # ---- the batch-32 paged serving step, timed the same way (beside the headline) ----
+    b32 = None
+    if args.b32_steps > 0 and cfg.name == DEFAULT_CONFIG and not args.serial:
+        cfg32 = CONFIG_BY_NAME["qwen3_8b_b32_paged"]
+        c32 = cycle_pass(cfg32, args.b32_steps, 5, True, "", 0, rank, local)
+        s32 = max_over_ranks(c32.elapsed_s, device="cuda")
+        v32 = whole_job_value(args.b32_steps, world, s32)
+        by32 = algorithmic_bytes(cfg32, c32.lens)
+        acc32 = float(np.mean([np.mean(a) for a in c32.accepts]))
+        rl32 = lm_head_roofline(cfg32, by32["lm_head"], c32.lm_ms, (peak, peak_kind),
+                                measured_peak_tflops(), None)
+        b32 = {"workload": cfg32.name, "value": v32, "unit": UNIT, "steps": args.b32_steps,
+               "warmup": 5, "ms_per_step": 1e3 * s32 / args.b32_steps,
+               "committed_tokens_per_s": v32 * cfg32.batch * (1 + acc32),
+               "cycle_gbs": by32["total"] * args.b32_steps / c32.elapsed_s / 1e9,
+               "cycle_roofline_frac": by32["total"] * args.b32_steps / c32.elapsed_s / 1e9 / peak,
+               "verify_project_phase_us": 1e3 * c32.phase_ms,
+               "roofline": rl32,
+               "verify_project": "side by side, SM budgets %d + %d" % (c32.verify_sms,
+                                                                        c32.project_sms),
+               "note": "32 sequences, contexts U[512, 16384] in a shuffled paged cache, same "
+                       "cycle, rotating-set and timing rules as the headline; the LM head and "
+                       "the fc GEMM are bound by the tensor cores at this batch"}
+        del c32
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        reps = [oracle_cycle_seconds(cfg, 1 / 16, 1 / 8) for _ in range(3)]
+        inp = oracle_inputs(cfg, 1.0)
+        reps = [oracle_cycle_seconds(cfg, inp) for _ in range(3)]
         tot = statistics.median(r["total"] for r in reps)
         cpu = {"value": 1.0 / tot, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-               "sample": reps[0]["sample"] + "; median of 3"}
+               "sample": reps[0]["sample"] + "; median of 3",
+               "extrapolated": reps[0]["extrapolated"], "threads": host_threads()}
 
     if rank == 0:
         line = {
@@ -973,6 +1144,8 @@ def main(argv=None):
             "verify_attention": vatt,
             "gdn_replay": gdn,
             "prefill_projection": prefill,
+            "prefill_attention": prefill_att,
+            "configs": {"qwen3_8b_b32_paged": b32} if b32 else None,
             "clocks": clocks,
             "e2e": e2e,
             "cpu_baseline": cpu,
