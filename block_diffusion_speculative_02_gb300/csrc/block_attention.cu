@@ -49,10 +49,9 @@ namespace {
 constexpr int kChunk = 64;     // keys per pipeline stage
 constexpr int kPage = 16;      // rows per TMA box
 constexpr int kAttThreads = 320;  // TMA, MMA, two softmax warpgroups
-// TMEM columns: S buffers at 0 and 64, O of the even-chunk group at 128, O of
-// the odd-chunk group at 128 + D
+// TMEM columns: S buffers at 0 and 64, the O accumulator at 128
 template <int D>
-__host__ __device__ constexpr int tmem_cols() { return 128 + 2 * D <= 256 ? 256 : 512; }
+__host__ __device__ constexpr int tmem_cols() { return 128 + D <= 256 ? 256 : 512; }
 constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnParams {
@@ -78,7 +77,7 @@ struct AttnParams {
   uint16_t* k_app;
   uint16_t* v_app;
   // shared-memory plan (byte offsets from the 1024-aligned base)
-  int n_stages, off_q, off_st, off_blk, off_sc, off_ml, off_rope, off_bar;
+  int n_stages, off_q, off_st, off_blk, off_sc, off_xch, off_rope, off_bar;
   RopeTable rope;
 };
 
@@ -164,7 +163,6 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
   uint8_t* stg = smem + p.off_st;
   uint8_t* blk = smem + p.off_blk;
   float2* sct = reinterpret_cast<float2*>(smem + p.off_sc);  // [16 positions][D/2] (cos, sin)
-  float2* ml_odd = reinterpret_cast<float2*>(smem + p.off_ml);  // [128] odd group's (max, sum)
   float* rope_hi = reinterpret_cast<float*>(smem + p.off_rope);
   float* rope_lo = rope_hi + D / 2;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar);
@@ -194,7 +192,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&p_full[i], 256);
       mbar_init(&pv_done[i], 1);
     }
     mbar_init(q_ready, 256);
@@ -370,7 +368,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
         for (int ks = 0; ks < ksteps; ++ks) {
           const uint64_t a = umma_sdesc_sw128(p_addr + (j & 1) * kPBytes + ks * 32);
           const uint64_t bd = umma_sdesc_sw128_mn(vb + ks * 2048, C::kHalf, 1024);
-          umma_bf16(o_tmem + (j & 1) * D, a, bd, idesc_pv, (j >= 2 || ks > 0) ? 1u : 0u);
+          umma_bf16(o_tmem, a, bd, idesc_pv, (j >= 1 || ks > 0) ? 1u : 0u);
         }
         umma_commit(&pv_done[j & 1]);
         if (!is_blk) umma_commit(&empty[c % NS]);
@@ -480,89 +478,115 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
       mbar_arrive(q_ready);
     }
 
+    // ---- softmax: all eight warps work on every chunk ----
+    // Warp w reads TMEM quadrant q4 = w & 3 (rows 32 q4 ..) and the key half
+    // kh = (w - 2) >> 2 of the 64-key chunk (S columns 32 kh ..); with rows
+    // doubled (R <= 64) lanes l and l + 16 hold the same row and split the
+    // half again.  A row's keys are spread over 4 threads (16 each), else 2
+    // (32 each); the row max is combined within the warp (shuffle) and with
+    // the quadrant's other warp through shared memory (one named barrier per
+    // chunk and quadrant, which also carries the two warps' ok flags so that
+    // they stop together).  S(j + 1) runs on the tensor cores while this
+    // softmax works on chunk j.
     const int q4 = warp & 3;                    // TMEM lane quadrant of this warp
-    const int grp = (warp - 2) >> 2;            // 0: even chunks, 1: odd chunks
-    // this thread's query row: lane i of the quadrant (i < rq real); with
-    // doubled rows lanes i and i + 16 hold the same row and split its keys
+    const int kh = (warp - 2) >> 2;             // key half of the chunk
     const int i_row = dup ? (lane & 15) : lane;
-    const int khalf = dup ? (lane >> 4) : 0;    // which 32 keys of a chunk (doubled rows)
+    const int khalf = dup ? (lane >> 4) : 0;
     const bool real = i_row < rq;
     const int rr = q4 * rq + i_row;             // row in the partial outputs
     const int m = q4 * 32 + i_row;              // MMA row that carries P of this query row
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q4 * 32) << 16);
-    const uint32_t o_col = 128 + grp * D;       // this group's O accumulator
-    constexpr int kMine = dup ? 32 : 64;        // keys of a chunk per thread
+    const uint32_t o_col = 128;                 // the O accumulator
+    constexpr int kMine = dup ? 16 : 32;        // keys of a chunk per thread
+    const int kbase = 32 * kh + kMine * khalf;  // this thread's first key of a chunk
+    // exchange slots: [chunk parity][key half][128 lanes] maxima, ok flags
+    float* xmax = reinterpret_cast<float*>(smem + p.off_xch);
+    int* xok = reinterpret_cast<int*>(smem + p.off_xch + 2 * 2 * 128 * 4);  // [parity][kh][4 q]
+    const uint32_t bar_q = 3 + q4;              // the quadrant's two warps
     float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int j = grp; j < n_total; j += 2) {
+    bool ok = true, okp_prev = true;
+    for (int j = 0; j < n_total; ++j) {
       const int nk = chunk_keys(j);
-      ok = mbar_wait(&s_full[j & 1], static_cast<uint32_t>((j >> 1) & 1), abort_flag, p.status);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sv[4][16];
-#pragma unroll
-      for (int c16 = 0; c16 < 4; ++c16)
-        if (c16 * 16 < nk) tmem_ld_32x32b_x16(lane_addr + (j & 1) * 64 + c16 * 16, sv[c16]);
-      tmem_ld_wait();
-      // this thread's keys kbase .. kbase + kMine - 1, masked past nk
-      const int kbase = 32 * khalf;
+      // a wait of the previous chunk that gave up stops the pair here, together
+      bool okw = okp_prev && mbar_wait(&s_full[j & 1], static_cast<uint32_t>((j >> 1) & 1),
+                                       abort_flag, p.status);
+      okw = __all_sync(0xffffffffu, okw);
+      float x[kMine];
+      float mx = -INFINITY;
       // keys of this row: all valid ones, or -- causal block chunk -- block
       // rows 0 .. i of the row's own block position i
       const int n_see = (p.causal && has_block && j == 0) ? min(nk, (rr & 15) + 1) : nk;
-      float x[kMine];
+      if (okw) {
+        tc_fence_after();
+        uint32_t sv[2][16];
 #pragma unroll
-      for (int e = 0; e < kMine; ++e) {
-        uint32_t v;
-        if (dup) v = khalf ? sv[2 + (e >> 4)][e & 15] : sv[e >> 4][e & 15];
-        else v = sv[e >> 4][e & 15];
-        x[e] = kbase + e < n_see ? __uint_as_float(v) : -INFINITY;
-      }
-      float mx4[4] = {x[0], x[1], x[2], x[3]};
+        for (int c16 = 0; c16 < 2; ++c16)
+          if (32 * kh + c16 * 16 < nk)
+            tmem_ld_32x32b_x16(lane_addr + (j & 1) * 64 + 32 * kh + c16 * 16, sv[c16]);
+        tmem_ld_wait();
 #pragma unroll
-      for (int e = 4; e < kMine; e += 4) {
-        mx4[0] = fmaxf(mx4[0], x[e]);
-        mx4[1] = fmaxf(mx4[1], x[e + 1]);
-        mx4[2] = fmaxf(mx4[2], x[e + 2]);
-        mx4[3] = fmaxf(mx4[3], x[e + 3]);
+        for (int e = 0; e < kMine; ++e) {
+          // column within the warp's 32: e, or 16 khalf + e with rows doubled
+          const uint32_t v = dup ? (khalf ? sv[1][e & 15] : sv[0][e & 15]) : sv[e >> 4][e & 15];
+          x[e] = kbase + e < n_see ? __uint_as_float(v) : -INFINITY;
+          mx = fmaxf(mx, x[e]);
+        }
+        if (dup) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       }
-      float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      if (dup) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      xmax[((j & 1) * 2 + kh) * 128 + q4 * 32 + lane] = mx;
+      if (lane == 0) xok[((j & 1) * 2 + kh) * 4 + q4] = okw ? 1 : 0;
+      named_bar_sync(bar_q, 64);
+      const bool ok_pair = okw && xok[((j & 1) * 2 + (kh ^ 1)) * 4 + q4] != 0;
+      if (!ok_pair) {
+        ok = false;
+        break;
+      }
+      mx = fmaxf(mx, xmax[((j & 1) * 2 + (kh ^ 1)) * 128 + q4 * 32 + lane]);
       const float mx_s = mx * p.scale_log2;
       float alpha = 1.f;
       if (m_run == -INFINITY) {
-        m_run = mx_s;                         // first chunk of this group: O and l empty
+        m_run = mx_s;                         // first chunk: O and l empty
       } else if (mx_s > m_run + kRescaleLog2) {
         alpha = fast_exp2(m_run - mx_s);
         m_run = mx_s;
       }
-      // the group's previous P V (chunk j - 2) must be done before its P buffer
-      // is rewritten or its O rescaled
-      if (j >= 2) {
-        ok = mbar_wait(&pv_done[j & 1], static_cast<uint32_t>(((j - 2) >> 1) & 1), abort_flag,
-                       p.status);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-      }
-      if (__any_sync(0xffffffffu, real && alpha != 1.f)) {
-        tc_fence_after();
-#pragma unroll 1
-        for (int c16 = 0; c16 < D / 16; ++c16) {
-          uint32_t ov[16];
-          tmem_ld_32x32b_x16(lane_addr + o_col + c16 * 16, ov);
-          tmem_ld_wait();
+      // P of this thread's keys, packed bf16 pairs (0 where masked)
+      uint32_t pk[kMine / 2];
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st_32x32b_x16(lane_addr + o_col + c16 * 16, ov);
-        }
-        tmem_st_wait();
+      for (int e = 0; e < kMine; e += 2) {
+        const float p0 = fast_exp2(fmaf(x[e], p.scale_log2, -m_run));
+        const float p1 = fast_exp2(fmaf(x[e + 1], p.scale_log2, -m_run));
+        sum4[(e >> 1) & 3] += p0 + p1;
+        pk[e >> 1] = pack_bf16(p0, p1);
       }
-      l_run *= alpha;
-      if (q4 == 0 && (nk & 15) && !(has_block && j == 0)) {
+      l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+      // P buffer j & 1 is free once P(j - 2) V(j - 2) has completed
+      bool okp = true;
+      if (j >= 2)
+        okp = mbar_wait(&pv_done[j & 1], static_cast<uint32_t>(((j - 2) >> 1) & 1), abort_flag,
+                        p.status);
+      // a rescale of O needs P(j - 1) V(j - 1) completed (warps of key half 0
+      // rescale their lanes; P(j) V(j) waits for every thread's arrival)
+      if (kh == 0 && __any_sync(0xffffffffu, real && alpha != 1.f)) {
+        if (j >= 1)
+          okp = okp && mbar_wait(&pv_done[(j - 1) & 1], static_cast<uint32_t>(((j - 1) >> 1) & 1),
+                                 abort_flag, p.status);
+        if (__all_sync(0xffffffffu, okp)) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int c16 = 0; c16 < D / 16; ++c16) {
+            uint32_t ov[16];
+            tmem_ld_32x32b_x16(lane_addr + o_col + c16 * 16, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st_32x32b_x16(lane_addr + o_col + c16 * 16, ov);
+          }
+          tmem_st_wait();
+        }
+      }
+      if (q4 == 0 && kh == 0 && (nk & 15) && !(has_block && j == 0)) {
         // rows past the length inside the last 16-key group came with their
         // page: zero their V so that 0-probability keys cannot inject
         // NaN/Inf from stale memory into O
@@ -575,56 +599,45 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
               make_uint4(0, 0, 0, 0);
         }
       }
+      // P(j) into shared buffer j & 1: row m, this thread's keys
       uint8_t* prow = smem + (j & 1) * kPBytes;
       const int ncol = (nk + 15) & ~15;         // keys the P V MMA reads (p = 0 past nk)
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c8 = 0; c8 < kMine / 8; ++c8) {  // 8 keys = one 16-byte chunk of the P row
         const int key0 = kbase + 8 * c8;
-        if (key0 < ncol) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const float p0 = fast_exp2(fmaf(x[8 * c8 + e], p.scale_log2, -m_run));
-            const float p1 = fast_exp2(fmaf(x[8 * c8 + e + 1], p.scale_log2, -m_run));
-            sum4[e >> 1] += p0 + p1;
-            pk[e >> 1] = pack_bf16(p0, p1);
-          }
-          if (real)
-            *reinterpret_cast<uint4*>(prow + swz_off(m, key0 >> 3)) =
-                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        }
+        if (real && key0 < ncol)
+          *reinterpret_cast<uint4*>(prow + swz_off(m, key0 >> 3)) =
+              make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
       }
-      l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full[j & 1]);
+      // an abandoned wait ends the loop at the next chunk's exchange, where
+      // the quadrant's other warp learns of it too (the MMA thread stops at
+      // its own bounded wait)
+      okp_prev = __all_sync(0xffffffffu, okp);
+      if (!okp_prev && j == n_total - 1) ok = false;
     }
+    // the row's sum over its 4 (2) threads: shuffle, then the other warp
     if (dup) l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
-    // epilogue: the odd group hands its (max, sum) to the even group, which
-    // merges the two O accumulators into this split's partial (O, max, sum)
-    const bool writer = real && khalf == 0;
-    const bool odd_used = n_total > 1;
-    if (grp == 1 && writer) ml_odd[m] = make_float2(ok ? m_run : -INFINITY, ok ? l_run : 0.f);
+    float* lx = xmax;                           // the exchange slots are free now
     named_bar_sync(2, 256);
-    if (grp == 0) {
+    if (kh == 1) lx[q4 * 32 + lane] = ok ? l_run : 0.f;
+    if (kh == 1 && lane == 0) xok[q4] = ok ? 1 : 0;
+    named_bar_sync(2, 256);
+    if (kh == 0) {
+      const bool writer = real && khalf == 0;
       // partials of grid unit (z, KV head, split): z = (sequence, sub-block)
       const size_t unit = (static_cast<size_t>(blockIdx.z) * p.n_kv_heads + g) * p.splits + s_idx;
       float* po = p.part_o + (unit * R + rr) * D;
       float* pml = p.part_ml + (unit * R + rr) * 2;
-      bool have_o = ok && n_total > 0;
+      bool have_o = ok && xok[q4] != 0 && n_total > 0;
+      have_o = __all_sync(0xffffffffu, have_o);
       if (have_o) {
         const bool done = mbar_wait(o_done, 0, abort_flag, p.status);
         have_o = __all_sync(0xffffffffu, done);
       }
-      float M = m_run, wa = 1.f, wb = 0.f, l_tot = l_run;
-      if (have_o && odd_used) {
-        const float2 ob = ml_odd[m];
-        M = fmaxf(m_run, ob.x);
-        wa = fast_exp2(m_run - M);
-        wb = ob.x == -INFINITY ? 0.f : fast_exp2(ob.x - M);
-        l_tot = wa * l_run + wb * ob.y;
-      }
+      float M = m_run, l_tot = l_run + lx[q4 * 32 + lane];
       // single split: the normalised bf16 row goes straight to the output
       // (row i of query head g * G + w), rows past the chunk are dropped
       const int wq = rr >> 4, iq = rr & 15;
@@ -637,30 +650,38 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
       if (have_o) {
         tc_fence_after();
 #pragma unroll 1
-        for (int c16 = 0; c16 < D / 16; ++c16) {
+        for (int c16 = 0; c16 < D / 16; c16 += 2) {
           uint32_t oa[16], ob[16];
-          tmem_ld_32x32b_x16(lane_addr + 128 + c16 * 16, oa);
-          if (odd_used) tmem_ld_32x32b_x16(lane_addr + 128 + D + c16 * 16, ob);
+          tmem_ld_32x32b_x16(lane_addr + o_col + c16 * 16, oa);
+          tmem_ld_32x32b_x16(lane_addr + o_col + c16 * 16 + 16, ob);
           tmem_ld_wait();
           if (writer) {
-            float o[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              o[e] = odd_used ? wa * __uint_as_float(oa[e]) + wb * __uint_as_float(ob[e])
-                              : __uint_as_float(oa[e]);
             if (od) {
               if (direct_row) {
-                uint32_t pk[8];
+                uint32_t pa[8], pb[8];
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) pk[e >> 1] = pack_bf16(o[e] * inv_l, o[e + 1] * inv_l);
-                *reinterpret_cast<uint4*>(od + c16 * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                *reinterpret_cast<uint4*>(od + c16 * 16 + 8) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                for (int e = 0; e < 16; e += 2) {
+                  pa[e >> 1] = pack_bf16(__uint_as_float(oa[e]) * inv_l,
+                                         __uint_as_float(oa[e + 1]) * inv_l);
+                  pb[e >> 1] = pack_bf16(__uint_as_float(ob[e]) * inv_l,
+                                         __uint_as_float(ob[e + 1]) * inv_l);
+                }
+                uint4* d4 = reinterpret_cast<uint4*>(od + c16 * 16);
+                d4[0] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+                d4[1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
+                d4[2] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
+                d4[3] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
               }
             } else {
+              float4* d4 = reinterpret_cast<float4*>(po + c16 * 16);
 #pragma unroll
-              for (int e = 0; e < 16; e += 4)
-                *reinterpret_cast<float4*>(po + c16 * 16 + e) =
-                    make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+              for (int e = 0; e < 16; e += 4) {
+                d4[e >> 2] = make_float4(__uint_as_float(oa[e]), __uint_as_float(oa[e + 1]),
+                                         __uint_as_float(oa[e + 2]), __uint_as_float(oa[e + 3]));
+                d4[4 + (e >> 2)] =
+                    make_float4(__uint_as_float(ob[e]), __uint_as_float(ob[e + 1]),
+                                __uint_as_float(ob[e + 2]), __uint_as_float(ob[e + 3]));
+              }
             }
           }
         }
@@ -785,8 +806,8 @@ int attention_smem_for(AttnParams& p, int n_stages) {
   p.off_st = p.off_q + C::kHalves * 128 * 128;
   p.off_blk = p.off_st + n_stages * C::kStage;
   p.off_sc = p.off_blk + C::kBlkTile;                   // [16][D/2] float2
-  p.off_ml = p.off_sc + kPage * (D / 2) * 8;            // [128] float2
-  p.off_rope = p.off_ml + 128 * 8;
+  p.off_xch = p.off_sc + kPage * (D / 2) * 8;           // [2][2][128] float + [2][2][4] int
+  p.off_rope = p.off_xch + 2 * 2 * 128 * 4 + 2 * 2 * 4 * 4;
   p.off_bar = p.off_rope + D * 4;
   return 1024 + p.off_bar + (2 * n_stages + 9) * 8 + 8;
 }
