@@ -77,6 +77,11 @@ def _rand(seed, B, Hq, Hkv, D, lens):
     (2, 16, 2, 128, [515, 64], False),        # G = 8 (128 query rows per KV head)
     (2, 2, 2, 64, [90, 5], True),             # G = 1, head_dim 64, paged
     (1, 4, 1, 128, [4000], False),            # many splits
+    # more (sequence, KV head, split) CTAs than SMs (several waves) over
+    # ragged lengths, empty and one-key contexts among them
+    (20, 32, 8, 128, [9000, 0, 17, 4096, 4097, 300, 8191, 1, 5000, 2500,
+                      16, 6000, 700, 8192, 3333, 64, 7777, 1200, 4500, 90], True),
+    (24, 16, 8, 64, [5000, 4100, 12, 0, 900] * 4 + [8200, 33, 4096, 2], False),
 ])
 def test_attention_parity_small(B, Hq, Hkv, D, lens, paged):
     q, k, v, ck, cv = _rand(sum(lens) + B, B, Hq, Hkv, D, lens)

@@ -25,6 +25,8 @@ def _dfl():
     (3, 32, 8, 128, [1000, 64, 5], False),
     (1, 4, 4, 64, [4096], True),
     (1, 32, 8, 128, [8192], False),        # the Qwen3-8B batch-1 shape the bench times
+    # more CTAs than SMs (several waves) over ragged lengths
+    (20, 16, 8, 128, [6000, 15, 0, 4097, 300, 9000, 64, 2000, 1, 5000] * 2, True),
 ])
 def test_verify_attention(B, Hq, Hkv, D, lens, paged):
     dfl = _dfl()
