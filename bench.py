@@ -200,23 +200,49 @@ def measured_peak_gbs():
     return PEAK_FALLBACK_GBS, "fallback"
 
 
-def profiled_traffic(kernel_src: str, profile_name: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source (matched by its sha256)."""
+def profiled_traffic(profile_name: str, kernel: str = ""):
+    """DRAM bytes per launch (read + write) and the algorithmic bytes per launch
+    from a committed ncu summary under profiles/, while every source file it
+    lists (`source_sha256: path=sha16 ...`, paths relative to the package)
+    still has the SHA-256 it was captured on; else None.  `kernel` selects a
+    `traffic_bytes_per_launch[kernel]` entry of a summary with several."""
     import hashlib
     p = os.path.join(ROOT, "profiles", profile_name)
     if not os.path.exists(p):
         return None
-    src = open(kernel_src, "rb").read()
-    sha = hashlib.sha256(src).hexdigest()[:16]
     vals = {}
     for line in open(p, encoding="utf-8"):
-        if ":" in line and line.strip().startswith(("source_sha256", "traffic_bytes_per_launch")):
-            k, v = line.split(":", 1)
+        s = line.strip()
+        if ":" in s and s.startswith(("source_sha256", "traffic_bytes_per_launch",
+                                      "algorithmic_bytes_per_launch")):
+            k, v = s.split(":", 1)
             vals[k.strip()] = v.strip()
-    if vals.get("source_sha256") == sha and "traffic_bytes_per_launch" in vals:
-        return float(vals["traffic_bytes_per_launch"])
-    return None
+    pairs = [x.split("=", 1) for x in vals.get("source_sha256", "").split()]
+    if not pairs or any(len(x) != 2 for x in pairs):
+        return None
+    pkg = os.path.join(ROOT, "block_diffusion_speculative_02_gb300")
+    for rel, sha in pairs:
+        f = os.path.join(pkg, rel)
+        if not os.path.exists(f) or hashlib.sha256(open(f, "rb").read()).hexdigest()[:16] != sha:
+            return None
+    tag = f"[{kernel}]" if kernel else ""
+    t, a = vals.get("traffic_bytes_per_launch" + tag), vals.get("algorithmic_bytes_per_launch" + tag)
+    if t is None or a is None:
+        return None
+    return {"traffic": float(t), "algorithmic": float(a), "ratio": float(t) / float(a),
+            "profile": "profiles/" + profile_name}
+
+
+def traffic_check():
+    """DRAM traffic / algorithmic bytes per launch of the four kernels of the
+    Qwen3-8B batch-1 cycle, from the committed ncu summaries (None where the
+    kernel's sources changed since the capture)."""
+    return {"lmhead_argmax_accept": profiled_traffic("lmhead_argmax_accept_qwen3_8b_b1.md"),
+            "block_attention": profiled_traffic("block_attention_qwen3_8b_b1.md"),
+            "streamk_gemm_fc": profiled_traffic("streamk_gemm_qwen3_8b_b1.md", "FcFin"),
+            "streamk_gemm_kv": profiled_traffic("streamk_gemm_qwen3_8b_b1.md", "KvFin"),
+            "note": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch (cold, "
+                    "alone) over the algorithmic bytes of that launch; 1.0 = every byte once"}
 
 
 # ---------------------------------------------------------------------------
@@ -679,11 +705,10 @@ def main(argv=None):
     bytes_ = algorithmic_bytes(cfg, lens)
     peak, peak_kind = measured_peak_gbs()
     cycle_gbs = bytes_["total"] * args.steps / elapsed_s / 1e9
-    # the committed DRAM capture is of the Qwen3-8B batch-1 launch only
-    traffic = profiled_traffic(os.path.join(ROOT, "block_diffusion_speculative_02_gb300", "csrc",
-                                            "verify_accept.cu"),
-                               "lmhead_argmax_accept_qwen3_8b_b1.md") \
-        if cfg.name == "qwen3_8b_b1" else None
+    # the committed DRAM captures are of the Qwen3-8B batch-1 launches only
+    tchk = traffic_check() if cfg.name == "qwen3_8b_b1" else None
+    traffic = tchk["lmhead_argmax_accept"]["traffic"] \
+        if tchk and tchk["lmhead_argmax_accept"] else None
 
     lm_roofline = lm_head_roofline(cfg, bytes_["lm_head"], lm_ms, (peak, peak_kind),
                                    measured_peak_tflops(), traffic)
@@ -1137,6 +1162,7 @@ def main(argv=None):
                 "us": 1e3 * phase_ms,
                 "gbs": (bytes_["lm_head"] + bytes_["ctx_project"]) / (phase_ms / 1e3) / 1e9},
             "roofline": lm_roofline,
+            "traffic_check": tchk,
             "gpu_launches": launches_per_step * args.steps,
             "graph_replay": graph_cycle,
             "breakdown": breakdown,
