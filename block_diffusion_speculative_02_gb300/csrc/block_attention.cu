@@ -55,12 +55,19 @@ __host__ __device__ constexpr int tmem_cols() { return 128 + D <= 256 ? 256 : 51
 constexpr float kRescaleLog2 = 8.0f;
 
 struct AttnParams {
-  int batch, n_q_heads, n_kv_heads, group, splits, rows;  // rows R = group * 16
+  int batch, n_q_heads, n_kv_heads, group, splits, rows;  // rows R = group << sub_shift
   int paged, capacity, max_pages;
-  // block rows: q/k/v row b * tokens + 16 j + i for sub-block j of sequence
-  // b (tokens = 16, sub_blocks = 1 for a single block); a sequence is valid
-  // when 0 <= seq_len[b] and seq_len[b] + need_rows fits the cache
+  // block rows: q/k/v row b * tokens + (j << sub_shift) + i for sub-block j
+  // of sequence b (tokens = 16, sub_blocks = 1 for a single block); a
+  // sequence is valid when 0 <= seq_len[b] and seq_len[b] + need_rows fits
+  // the cache
   int tokens, sub_blocks, need_rows;
+  // rows per sub-block = 1 << sub_shift (16, or 32 for the prompt attention
+  // when G * 32 query rows fit the 128 MMA rows); self_cached: the sub-block's
+  // own keys are already in the cache (the prompt attention appends first)
+  // and are read with the context under a per-row causal limit, with no
+  // block tile
+  int sub_shift, self_cached;
   uint16_t* out_direct;  // splits == 1: bf16 output [B * tokens, Hq, D] written here
   const int32_t* seq_len;
   const int32_t* page_table;
@@ -83,7 +90,7 @@ struct AttnParams {
 
 struct CombineParams {
   int batch, n_q_heads, n_kv_heads, group, splits, rows, head_dim, limit;
-  int tokens, sub_blocks, need_rows;
+  int tokens, sub_blocks, need_rows, sub_shift;
   const int32_t* seq_len;
   const float* part_o;
   const float* part_ml;
@@ -182,8 +189,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
   // (sequence, sub-block): the last sub-block, with the longest context, first
   const int b = blockIdx.z / p.sub_blocks;
   const int jsub = p.sub_blocks - 1 - (static_cast<int>(blockIdx.z) - b * p.sub_blocks);
-  const int row0 = b * p.tokens + jsub * kBlock;      // first block row in q/k/v
-  const int n_rows = min(kBlock, p.tokens - jsub * kBlock);
+  const int sub_rows = 1 << p.sub_shift;
+  const int row0 = b * p.tokens + (jsub << p.sub_shift);  // first block row in q/k/v
+  const int n_rows = min(sub_rows, p.tokens - (jsub << p.sub_shift));
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -226,8 +234,11 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
   const bool valid_len = L0 >= 0 && L0 + p.need_rows <= limit;
   if (!valid_len && threadIdx.x == 0 && s_idx == 0 && g == 0 && jsub == 0)
     set_status(p.status, DFLASH_ST_CAPACITY);
-  const int L = L0 + jsub * kBlock;             // context rows of this sub-block
-  const int Lc = valid_len ? L : 0;
+  const int L = L0 + (jsub << p.sub_shift);     // position of the sub-block's first row
+  // keys read from the cache: the context, and the sub-block's own rows too
+  // when they are already there
+  const int Lc = valid_len ? (p.self_cached ? L + n_rows : L) : 0;
+  const int Lq = valid_len ? L : 0;             // position of the block's row 0
   const int n_pg = (Lc + kPage - 1) / kPage;
   const int pps = (n_pg + p.splits - 1) / p.splits;
   const int pg_begin = s_idx * pps;
@@ -236,7 +247,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
   const int key_end = min(pg_end * kPage, Lc);
   const int n_keys = key_end > key_begin ? key_end - key_begin : 0;
   const int n_chunks = (n_keys + kChunk - 1) / kChunk;
-  const int has_block = (valid_len && s_idx == p.splits - 1) ? 1 : 0;
+  const int has_block = (valid_len && !p.self_cached && s_idx == p.splits - 1) ? 1 : 0;
   const int n_total = n_chunks + has_block;    // chunk 0 is the block when has_block
   auto chunk_keys = [&](int j) {               // valid keys of chunk j
     if (has_block && j == 0) return kPage;
@@ -396,7 +407,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
         const int it = u * 256 + tid;
         if (it < q_items) {
           const int rr = it / kPer, d0 = (it - rr * kPer) * 8;
-          const int w = rr >> 4, i = rr & 15;
+          const int w = rr >> p.sub_shift, i = rr & (sub_rows - 1);
           if (i < n_rows) {
             const size_t src =
                 (static_cast<size_t>(row0 + i) * p.n_q_heads + g * G + w) * D + d0;
@@ -407,11 +418,12 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
           }
         }
       }
-      // (cos, sin) of the 16 block positions L + i, i < 16, for every frequency
-      for (int k = tid; k < kPage * (D / 2); k += 256) {
+      // (cos, sin) of the sub-block's positions L + i, i < sub_rows, for every
+      // frequency
+      for (int k = tid; k < sub_rows * (D / 2); k += 256) {
         const int i = k / (D / 2), d = k - i * (D / 2);
         float sn, cs;
-        rope_sincos(Lc + i, rope_hi[d], rope_lo[d], &sn, &cs);
+        rope_sincos(Lq + i, rope_hi[d], rope_lo[d], &sn, &cs);
         sct[k] = make_float2(cs, sn);
       }
       named_bar_sync(1, 256);
@@ -421,7 +433,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
         if (it < q_items) {
           const int rr = it / kPer, d0 = (it - rr * kPer) * 8;
           uint4 y1, y2;
-          rope8(x1[u], x2[u], sct + (rr & 15) * (D / 2), d0, y1, y2);
+          rope8(x1[u], x2[u], sct + (rr & (sub_rows - 1)) * (D / 2), d0, y1, y2);
           const int e2 = d0 + D / 2;
           const int m = 32 * (rr / rq) + rr % rq;
           *reinterpret_cast<uint4*>(qs + (d0 >> 6) * kQHalf + swz_off(m, (d0 & 63) >> 3)) = y1;
@@ -515,7 +527,11 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
       float mx = -INFINITY;
       // keys of this row: all valid ones, or -- causal block chunk -- block
       // rows 0 .. i of the row's own block position i
-      const int n_see = (p.causal && has_block && j == 0) ? min(nk, (rr & 15) + 1) : nk;
+      // (the prompt attention: keys up to the row's own position L + i)
+      const int n_see =
+          p.self_cached ? max(0, min(nk, L + (rr & (sub_rows - 1)) + 1 - (key_begin + j * kChunk)))
+          : (p.causal && has_block && j == 0) ? min(nk, (rr & 15) + 1)
+                                              : nk;
       if (okw) {
         tc_fence_after();
         uint32_t sv[2][16];
@@ -550,13 +566,16 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
         alpha = fast_exp2(m_run - mx_s);
         m_run = mx_s;
       }
-      // P of this thread's keys, packed bf16 pairs (0 where masked)
+      // P of this thread's keys, packed bf16 pairs (0 where masked; a row
+      // that has seen no key yet -- the prompt attention's later splits --
+      // keeps m = -inf and gets P = 0)
+      const float m_sub = m_run == -INFINITY ? 0.f : m_run;
       uint32_t pk[kMine / 2];
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int e = 0; e < kMine; e += 2) {
-        const float p0 = fast_exp2(fmaf(x[e], p.scale_log2, -m_run));
-        const float p1 = fast_exp2(fmaf(x[e + 1], p.scale_log2, -m_run));
+        const float p0 = fast_exp2(fmaf(x[e], p.scale_log2, -m_sub));
+        const float p1 = fast_exp2(fmaf(x[e + 1], p.scale_log2, -m_sub));
         sum4[(e >> 1) & 3] += p0 + p1;
         pk[e >> 1] = pack_bf16(p0, p1);
       }
@@ -640,7 +659,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) block_attention_kernel(
       float M = m_run, l_tot = l_run + lx[q4 * 32 + lane];
       // single split: the normalised bf16 row goes straight to the output
       // (row i of query head g * G + w), rows past the chunk are dropped
-      const int wq = rr >> 4, iq = rr & 15;
+      const int wq = rr >> p.sub_shift, iq = rr & (sub_rows - 1);
       uint16_t* od = p.out_direct
                          ? p.out_direct +
                                (static_cast<size_t>(row0 + iq) * p.n_q_heads + g * G + wq) * D
@@ -727,10 +746,10 @@ __global__ void __launch_bounds__(32 * kCombineRows) attn_combine_kernel(const C
   const int rem = row - b * p.tokens * p.n_q_heads;
   const int t = rem / p.n_q_heads;
   const int h = rem - t * p.n_q_heads;
-  const int i = t & (kBlock - 1);
-  const int z = b * p.sub_blocks + (p.sub_blocks - 1 - t / kBlock);
+  const int i = t & ((1 << p.sub_shift) - 1);
+  const int z = b * p.sub_blocks + (p.sub_blocks - 1 - (t >> p.sub_shift));
   const int g = h / p.group, w = h - g * p.group;
-  const int rr = w * kBlock + i;
+  const int rr = (w << p.sub_shift) + i;
   const size_t unit0 = (static_cast<size_t>(z) * p.n_kv_heads + g) * p.splits;
   const int L0 = p.seq_len[b];
   float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
@@ -806,7 +825,7 @@ int attention_smem_for(AttnParams& p, int n_stages) {
   p.off_st = p.off_q + C::kHalves * 128 * 128;
   p.off_blk = p.off_st + n_stages * C::kStage;
   p.off_sc = p.off_blk + C::kBlkTile;                   // [16][D/2] float2
-  p.off_xch = p.off_sc + kPage * (D / 2) * 8;           // [2][2][128] float + [2][2][4] int
+  p.off_xch = p.off_sc + (1 << p.sub_shift) * (D / 2) * 8;  // [2][2][128] float + [2][2][4] int
   p.off_rope = p.off_xch + 2 * 2 * 128 * 4 + 2 * 2 * 4 * 4;
   p.off_bar = p.off_rope + D * 4;
   return 1024 + p.off_bar + (2 * n_stages + 9) * 8 + 8;
@@ -997,6 +1016,7 @@ int run_attention(const dflash_dims* dims, const void* q_blk, const void* k_blk,
   AttnParams p = {};
   p.tokens = kBlock;
   p.sub_blocks = 1;
+  p.sub_shift = 4;
   p.need_rows = 0;
   p.batch = dims->batch;
   p.n_q_heads = dims->n_q_heads;
@@ -1021,6 +1041,7 @@ int run_attention(const dflash_dims* dims, const void* q_blk, const void* k_blk,
   CombineParams cp = {};
   cp.tokens = kBlock;
   cp.sub_blocks = 1;
+  cp.sub_shift = 4;
   cp.need_rows = 0;
   cp.batch = dims->batch;
   cp.n_q_heads = dims->n_q_heads;
@@ -1057,7 +1078,7 @@ namespace dflash {
 // partials when a chunk's (sequence, sub-block, KV head) units are too few to
 // fill the device with one split each.
 struct PrefillAttnPlan {
-  int sub_blocks, splits, rows;
+  int sub_shift, sub_blocks, splits, rows;
   size_t off_status, off_o, off_ml, total;
 };
 
@@ -1066,7 +1087,12 @@ int make_prefill_attn_plan(const dflash_dims& d, int tokens, PrefillAttnPlan* ou
   if (rc) return rc;
   if (tokens < 1) return DFLASH_E_ARG;
   PrefillAttnPlan q = {};
-  q.sub_blocks = (tokens + kBlock - 1) / kBlock;
+  // 32 prompt rows per CTA when the G query heads of a KV head then fill the
+  // 128 MMA rows (G <= 4), else 16: every CTA streams its KV head's prefix
+  // once, so more rows per CTA means fewer passes over the prefix
+  const int G = d.n_q_heads / d.n_kv_heads;
+  q.sub_shift = G * 32 <= 128 ? 5 : 4;
+  q.sub_blocks = (tokens + (1 << q.sub_shift) - 1) >> q.sub_shift;
   if (static_cast<long long>(d.batch) * q.sub_blocks > 65535) return DFLASH_E_UNSUPPORTED;
   // splits: enough (sequence, sub-block, KV head, split) CTAs for one per
   // SM of the GB300 (152); fixed rather than read from the device, so that
@@ -1079,7 +1105,7 @@ int make_prefill_attn_plan(const dflash_dims& d, int tokens, PrefillAttnPlan* ou
   if (s > kMaxAttSplits) s = kMaxAttSplits;
   if (s < 1) s = 1;
   q.splits = s;
-  q.rows = (d.n_q_heads / d.n_kv_heads) * kBlock;
+  q.rows = G << q.sub_shift;
   size_t off = 256;  // status word at 0
   q.off_status = 0;
   if (s > 1) {
@@ -1148,6 +1174,8 @@ extern "C" int dflash_prefill_attention(const dflash_dims* dims, int32_t tokens_
   p.causal = 1;
   p.tokens = T;
   p.sub_blocks = plan.sub_blocks;
+  p.sub_shift = plan.sub_shift;
+  p.self_cached = 1;
   p.need_rows = T;
   if (plan.splits > 1) {
     p.part_o = ws_at<float>(ws, plan.off_o);
@@ -1168,6 +1196,7 @@ extern "C" int dflash_prefill_attention(const dflash_dims* dims, int32_t tokens_
   cp.limit = paged ? cache->max_pages * 16 : cache->capacity;
   cp.tokens = T;
   cp.sub_blocks = plan.sub_blocks;
+  cp.sub_shift = plan.sub_shift;
   cp.need_rows = T;
   cp.seq_len = cache->seq_len;
   cp.part_o = p.part_o;

@@ -20,9 +20,11 @@ def test_prefill_workspace_layout():
     status (256 B) | write-position snapshot | per-tile sums of Y^2 |
     bf16(g_h * Y), each region 256-byte aligned, 256-feature tiles when the
     hidden size allows them.  The attention's: status (256 B) | split partials
-    (O, then max and sum) when the chunk's (sequence, 16-row sub-block, KV
-    head) units are fewer than 152, split ceil(152 / units) ways (at most 64,
-    at most one per 16 context rows)."""
+    (O, then max and sum) when the chunk's (sequence, sub-block, KV head)
+    units are fewer than 152, split ceil(152 / units) ways (at most 64, at
+    most one per 16 context rows); a sub-block is 32 prompt rows when the G
+    query heads of a KV head fill the 128 MMA rows with them (G <= 4), else
+    16."""
     dflash, _ = _lib()
     al = lambda x: (x + 255) // 256 * 256  # noqa: E731
     for B, T, H in ((1, 8192, 4096), (2, 100, 512), (3, 7, 384)):
@@ -30,11 +32,13 @@ def test_prefill_workspace_layout():
         rows = B * T
         tiles = H // 256 if H % 256 == 0 else H // 128
         proj = 256 + al(4 * B) + al(4 * tiles * rows) + al(2 * rows * H)
-        units = B * -(-T // 16) * 8
+        G = 32 // 8
+        sub = 32 if G * 32 <= 128 else 16             # prompt rows per CTA
+        units = B * -(-T // sub) * 8
         splits = 1 if units >= 152 else min(-(-152 // units), -(-T // 16), 64)
         att = 256
         if splits > 1:
-            n = units * splits * (32 // 8) * 16
+            n = units * splits * G * sub
             att = al(256 + 4 * n * 128 + 8 * n)
         assert dflash.dflash_prefill_workspace_bytes(dims, T) == max(proj, att), (B, T, H)
 
