@@ -27,6 +27,10 @@ def _dfl():
     (1, 32, 8, 128, [8192], False),        # the Qwen3-8B batch-1 shape the bench times
     # more CTAs than SMs (several waves) over ragged lengths
     (20, 16, 8, 128, [6000, 15, 0, 4097, 300, 9000, 64, 2000, 1, 5000] * 2, True),
+    # G = 8 (the Qwen3-32B heads: 128 query rows per KV head, no doubled rows)
+    (2, 16, 2, 128, [515, 64], False),
+    (4, 64, 8, 128, [3000, 2500, 100, 0], True),
+    (4, 64, 8, 128, [32768] * 4, False),   # the Qwen3-32B batch-4 long-context shape
 ])
 def test_verify_attention(B, Hq, Hkv, D, lens, paged):
     dfl = _dfl()
