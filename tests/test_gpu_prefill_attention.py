@@ -186,16 +186,17 @@ def test_prefill_attention_capacity_is_refused_on_the_device():
     assert_close_bf16(host_f64(out[:1]), ref["o"])
 
 
-@pytest.mark.parametrize("chunk,paged", [(2048, False), (512, True)])
-def test_prefill_attention_full_size(chunk, paged):
-    """Qwen3-8B heads (32 / 8, D 128), one 8192-token prompt fed in chunks of
-    2048 (contiguous cache) or 512 (paged, shuffled pool).  Sampled rows of
+@pytest.mark.parametrize("chunk,paged,Hq", [(2048, False, 32), (512, True, 32), (2048, True, 64)])
+def test_prefill_attention_full_size(chunk, paged, Hq):
+    """Qwen3-8B heads (32 / 8, D 128; 32 prompt rows per CTA), one 8192-token
+    prompt fed in chunks of 2048 (contiguous cache) or 512 (paged, shuffled
+    pool), and the Qwen3-32B heads (64 / 8: 16 rows per CTA).  Sampled rows of
     every chunk are checked against the oracle computed one row at a time
     (a row's attention only needs the rows before it, which the chunked ==
     whole pin makes exact), and every appended K row against the rotation."""
     dfl = _dfl()
-    rng = np.random.default_rng(81 + chunk)
-    B, Hq, Hkv, D, P = 1, 32, 8, 128, 8192
+    rng = np.random.default_rng(81 + chunk + Hq)
+    B, Hkv, D, P = 1, 8, 128, 8192
     q = normal_bf16(rng, (B, P, Hq, D))
     k = normal_bf16(rng, (B, P, Hkv, D))
     v = normal_bf16(rng, (B, P, Hkv, D))
