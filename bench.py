@@ -13,7 +13,9 @@ the SMs (the split is measured once before the warm-up; --sm-split fixes it,
 --serial queues everything on one stream); the crop then runs on the side
 stream beside the attention, which reads the committed length directly.
 Beside `value` (calls issued step by step) the line reports the same cycle
-replayed from CUDA graphs (`graph_replay`).
+replayed from CUDA graphs (`graph_replay`), and the same workload with its
+draft match lengths drawn truncated-geometric with mean 13 instead of
+uniform in 0..15 (`geometric_draw`).
 
 Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 N > 1 runs under torchrun: every rank runs an independent replica (sequences
@@ -61,6 +63,10 @@ def parse_args(argv=None):
                     help="prompt length of the prefill passes (0 = skip)")
     ap.add_argument("--prefill-chunk", type=int, default=2048,
                     help="prompt chunk of the prefill-attention pass")
+    ap.add_argument("--alt-draw-steps", type=int, default=400,
+                    help="timed cycles of the headline workload with the draft match lengths "
+                         "drawn truncated-geometric with mean 13 (reported beside the "
+                         "uniform headline; 0 = skip)")
     ap.add_argument("--b32-steps", type=int, default=50,
                     help="timed cycles of the batch-32 paged workload reported beside the "
                          "headline (0 = skip)")
@@ -1106,6 +1112,24 @@ def main(argv=None):
                "loop": "PipelinedCycles: one graph per step; the next step's host-to-device "
                        "copy overlaps the current step; results read back every step"}
 
+    # ---- the headline workload with the other draft-match draw (mean 13) ----
+    alt = None
+    if args.alt_draw_steps > 0 and cfg.accept[0] == "uniform" and cfg.name == DEFAULT_CONFIG:
+        cfg_g = dataclasses.replace(cfg, accept=("geometric", 13.0))
+        split = "%d,%d" % (verify_sms, project_sms) if concurrent else ""
+        cg = cycle_pass(cfg_g, args.alt_draw_steps, 5, concurrent, split, args.sets, rank, local)
+        sg = max_over_ranks(cg.elapsed_s, device="cuda")
+        vg = whole_job_value(args.alt_draw_steps, world, sg)
+        accg = float(np.mean([np.mean(a) for a in cg.accepts]))
+        alt = {"draw": "truncated geometric, mean 13", "value": vg, "unit": UNIT,
+               "steps": args.alt_draw_steps, "warmup": 5,
+               "ms_per_step": 1e3 * sg / args.alt_draw_steps,
+               "committed_tokens_per_s": vg * cfg.batch * (1 + accg),
+               "tokens_per_cycle": cfg.batch * (1 + accg), "acceptance_rate": accg / 15.0,
+               "note": "same workload, SM split and timing rules as the headline, whose "
+                       "draft match lengths are uniform in 0..15"}
+        del cg
+
     # ---- the batch-32 paged serving step, timed the same way (beside the headline) ----
     b32 = None
     if args.b32_steps > 0 and cfg.name == DEFAULT_CONFIG and not args.serial:
@@ -1156,6 +1180,7 @@ def main(argv=None):
             "committed_tokens_per_s": value * cfg.batch * (1 + acc_mean),
             "tokens_per_cycle": cfg.batch * (1 + acc_mean),
             "acceptance_rate": acc_mean / 15.0,
+            "geometric_draw": alt,
             "cycle_gbs": cycle_gbs, "cycle_roofline_frac": cycle_gbs / peak,
             "algorithmic_bytes_per_cycle": bytes_,
             "verify_project_phase": {
