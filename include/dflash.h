@@ -370,8 +370,10 @@ DFLASH_API int dflash_ctx_prefill(const dflash_dims* dims, int32_t tokens_per_se
  * The chunk's rotated K and its V are appended to `cache` at rows L..L+T-1
  * (for a paged cache the pages they need are first taken from its free
  * list), after which cache->seq_len[b] = L + T; a prompt fed chunk by chunk
- * gives the rows of the prompt fed at once.  Any T >= 1 (ceil(T/16) * batch
- * <= 65535).
+ * gives the rows of the prompt fed at once.  Any T >= 1 with ceil(T/S) *
+ * batch <= 65535, S = 32 when Hq/Hkv <= 4, else 16 (the prompt rows one CTA
+ * takes: S times the group fills at most 128 MMA rows); else
+ * DFLASH_E_UNSUPPORTED.
  *   q: bf16 [B, T, Hq, D]; k, v: bf16 [B, T, Hkv, D] (before RoPE);
  *   out: bf16 [B, T, Hq, D].
  *   ws: dflash_prefill_workspace_bytes(dims, T) bytes, zeroed once (the same
